@@ -1,0 +1,387 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Every check here compares the oracle with something other than itself: a
+printed example, an independent dense formulation (tests/dense_ref.py), a
+library routine on a special case, a closed form, or an invariant.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_ref import dense_attention
+from workloads import build_case, random_case, workload_lengths
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _run(case, **over):
+    kw = case.oracle_kwargs()
+    kw.update(over)
+    return oracle.attention(case.q, case.key_cache, case.value_cache, case.block_table,
+                            case.cache_seqlens, case.cu_seqlens_q, **kw)
+
+
+def _dense(case, **over):
+    kw = case.oracle_kwargs()
+    kw.update(over)
+    return dense_attention(case.q, case.key_cache, case.value_cache, case.block_table,
+                           case.cache_seqlens, case.cu_seqlens_q, **kw)
+
+
+def _close(a, b, tol):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    assert a.shape == b.shape
+    fa, fb = np.isfinite(a), np.isfinite(b)
+    assert np.array_equal(fa, fb), "finite / -inf pattern differs"
+    assert np.array_equal(a[~fa], b[~fb])
+    if fa.any():
+        err = np.max(np.abs(a[fa] - b[fb]))
+        assert err <= tol, f"max abs diff {err}"
+
+
+# --- printed examples ---------------------------------------------------------
+
+def test_page_index_csr_printed_examples():
+    g = _golden("page_index_csr.json")
+    for c in g["cases"]:
+        indptr, indices, last = oracle.page_index_csr(c["block_table"], c["seq_lens"], g["block_size"],
+                                                      count=c["count"])
+        assert indptr == c["indptr"]
+        assert indices == c["indices"]
+        assert last == c["last_page_len"]
+
+
+def test_cu_seqlens_printed_examples():
+    for c in _golden("cu_seqlens.json")["cases"]:
+        assert oracle.cu_seqlens_from_lengths(c["lengths"]) == c["cu_seqlens"]
+
+
+def test_bucket_max_seqlen_q():
+    g = _golden("bucket_max_seqlen_q.json")
+    for n, want in g["printed"] + g["from_the_formula"]:
+        assert oracle.bucket_max_seqlen_q(n) == want
+
+
+def test_page_num_splits_reading_at_workloads():
+    for c in _golden("page_num_splits_workloads.json")["cases"]:
+        kw = {k: c[k] for k in ("is_local", "batch_size", "max_query_len", "num_heads", "num_kv_heads",
+                                "max_kv_len")}
+        if "capability_major" in c:
+            kw["capability_major"] = c["capability_major"]
+        assert oracle.page_num_splits(**kw) == c["splits"], c["workload"]
+
+
+def test_workload_shapes_match_heuristic_inputs():
+    # the golden shapes above are the workloads' own maxima
+    _, kv = workload_lengths("decode_batch")
+    assert max(kv) <= 32768 and min(kv) >= 1024
+    q, kv = workload_lengths("chunked_prefill")
+    assert max(q) == 2048 and max(kv) == 16384
+
+
+def test_slot_mapping_brute_force():
+    g = torch.Generator().manual_seed(3)
+    bs = 4
+    block_table = torch.randperm(40, generator=g)[:30].view(3, 10).tolist()
+    seq_lens = [13, 1, 29]
+    query_lens = [5, 1, 29]
+    got = oracle.slot_mapping(block_table, seq_lens, query_lens, bs)
+    want = []
+    for row, n, ql in zip(block_table, seq_lens, query_lens):
+        dense = [p * bs + o for p in row for o in range(bs)]  # logical position -> slot
+        want += dense[n - ql:n]
+    assert got == want
+
+
+# --- attention core against the independent dense formulation ---------------
+
+@pytest.mark.parametrize("seed", range(240))
+def test_oracle_matches_dense_bruteforce(seed):
+    case = random_case(seed, D=[8, 16, 32][seed % 3])
+    out, lse = _run(case)
+    dout, dlse = _dense(case)
+    _close(out, dout, 1e-12)
+    _close(lse, dlse, 1e-12)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_oracle_matches_dense_head_dim_128(seed):
+    case = random_case(500 + seed, D=128)
+    out, lse = _run(case)
+    dout, dlse = _dense(case)
+    _close(out, dout, 1e-12)
+    _close(lse, dlse, 1e-12)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_zero_bias_is_sdpa_with_explicit_mask(seed):
+    """rel_logits == 0 reduces to plain causal GQA attention (fp64 SDPA)."""
+    case = random_case(900 + seed, D=32, E=16)
+    case.rel_logits = torch.zeros_like(case.rel_logits)
+    out, lse = _run(case)
+    out0, _ = _run(case, rel_extent=0, rel_logits=None)
+    _close(out, out0, 0.0)
+    G = case.H // case.Hkv
+    for b in range(case.B):
+        t0, t1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        Lq, Lk = t1 - t0, case.kv_lens[b]
+        if Lq == 0:
+            continue
+        npg = -(-Lk // case.BS)
+        pages = case.block_table[b, :npg].long()
+        K = case.key_cache[pages].reshape(-1, case.Hkv, case.D)[:Lk].double()
+        V = case.value_cache[pages].reshape(-1, case.Hkv, case.D)[:Lk].double()
+        K = K.repeat_interleave(G, dim=1).permute(1, 0, 2)
+        V = V.repeat_interleave(G, dim=1).permute(1, 0, 2)
+        Q = case.q[t0:t1].double().permute(1, 0, 2)
+        i = torch.arange(Lq)[:, None] + (Lk - Lq)
+        j = torch.arange(Lk)[None, :]
+        mask = torch.ones(Lq, Lk, dtype=torch.bool)
+        if case.causal:
+            mask &= j <= i
+        if case.window_left >= 0:
+            mask &= j >= i - case.window_left
+        if case.window_right >= 0:
+            mask &= j <= i + case.window_right
+        rows = mask.any(dim=1)
+        if not rows.any():
+            assert np.all(out[t0:t1] == 0)
+            continue
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q[:, rows], K, V, attn_mask=mask[rows], scale=case.softmax_scale)
+        got = torch.from_numpy(out[t0:t1][rows.numpy()]).permute(1, 0, 2)
+        assert torch.max(torch.abs(got - ref)) < 1e-12
+        assert np.all(out[t0:t1][~rows.numpy()] == 0)
+
+
+# --- closed forms -------------------------------------------------------------
+
+def test_single_key_decode_closed_form():
+    """Lk = 1: the output is the single V row and lse the single score."""
+    case = build_case("one", [1, 1], [1, 1], H=4, Hkv=2, D=16, BS=4, E=3, seed=7)
+    out, lse = _run(case)
+    for b in range(2):
+        t = b
+        page = int(case.block_table[b, 0])
+        for h in range(4):
+            g = h // 2
+            v = case.value_cache[page, 0, g].double().numpy()
+            k = case.key_cache[page, 0, g].double().numpy()
+            qv = case.q[t, h].double().numpy()
+            s = case.softmax_scale * float(np.dot(qv, k)) + float(case.rel_logits[t, h, 0])
+            assert np.array_equal(out[t, h], v)
+            assert abs(lse[t, h] - s) <= 1e-12 * max(1.0, abs(s))
+
+
+def test_zero_query_is_mean_of_visible_values():
+    case = build_case("zq", [3, 1], [9, 20], H=2, Hkv=1, D=8, BS=4, E=0, seed=9, window=(5, -1))
+    case.q = torch.zeros_like(case.q)
+    out, lse = _run(case)
+    for b, (t0, Lq, Lk) in enumerate([(0, 3, 9), (3, 1, 20)]):
+        npg = -(-Lk // 4)
+        V = case.value_cache[case.block_table[b, :npg].long()].reshape(-1, 1, 8)[:Lk, 0].double().numpy()
+        for i in range(Lq):
+            qa = i + Lk - Lq
+            lo = max(0, qa - 5)
+            vis = V[lo:qa + 1]
+            for h in range(2):
+                assert np.max(np.abs(out[t0 + i, h] - vis.mean(axis=0))) < 1e-14
+                assert abs(lse[t0 + i, h] - math.log(len(vis))) < 1e-14
+
+
+# --- bias algebra ---------------------------------------------------------------
+
+def test_constant_bias_shifts_lse_only():
+    case = random_case(77, D=16, E=64, max_kv_extra=40, max_q=20, causal=True, window=(-1, -1))
+    assert case.E >= max(case.kv_lens)
+    out0, lse0 = _run(case, rel_extent=0, rel_logits=None)
+    c = 0.625
+    case.rel_logits = torch.full_like(case.rel_logits, c)
+    out, lse = _run(case)
+    # every visible key has 0 <= rd <= q_abs < Lk <= E, so the bias is c everywhere
+    _close(out, out0, 1e-13)
+    fin = np.isfinite(lse0)
+    assert fin.any()
+    assert np.max(np.abs(lse[fin] - (lse0[fin] + c))) < 1e-12
+
+
+def test_extent_one_biases_only_the_diagonal():
+    """E = 1 equals a wider table that is zero except at rd = 0."""
+    case = build_case("diag", [4, 1, 7], [6, 5, 7], H=2, Hkv=1, D=8, BS=2, E=1, seed=11)
+    out, lse = _run(case)
+    wide = torch.zeros(case.T, case.H, 9)
+    wide[:, :, 0] = case.rel_logits[:, :, 0]
+    out9, lse9 = _run(case, rel_extent=9, rel_logits=wide)
+    _close(out, out9, 0.0)
+    _close(lse, lse9, 0.0)
+    z_out, _ = _run(case, rel_extent=0, rel_logits=None)
+    assert not np.allclose(out, z_out)
+
+
+def test_unread_bias_entries_have_no_effect():
+    """Entries at rd > q_abs (no such key) or beyond a left window are never read."""
+    case = build_case("nan", [3, 1, 6], [3, 9, 14], H=4, Hkv=2, D=16, BS=4, E=12, seed=13,
+                      window=(4, -1))
+    ref_out, ref_lse = _run(case)
+    rel = case.rel_logits.clone()
+    for b in range(case.B):
+        t0 = int(case.cu_seqlens_q[b])
+        Lq, Lk = case.q_lens[b], case.kv_lens[b]
+        for i in range(Lq):
+            qa = i + Lk - Lq
+            rel[t0 + i, :, min(case.E, qa + 1):] = float("nan")   # rd > q_abs
+            rel[t0 + i, :, min(case.E, 5):] = float("nan")        # rd > window_left
+    case.rel_logits = rel
+    out, lse = _run(case)
+    assert np.all(np.isfinite(out))
+    _close(out, ref_out, 0.0)
+    _close(lse, ref_lse, 0.0)
+
+
+# --- split-and-merge and invariances ------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(30))
+def test_split_merge_equals_unsplit(seed):
+    case = random_case(2000 + seed, D=16)
+    out, lse = _run(case)
+    for chunk in (1, 3, 16, 64):
+        so, sl = _run(case, chunk_keys=chunk)
+        _close(so, out, 1e-12)
+        _close(sl, lse, 1e-12)
+
+
+def test_unnormalised_partials_with_page_weights_would_be_wrong():
+    """Reading of the PagedAttention V2 Phase-2 weights exp(m_c - gmax) * l_c:
+    they are right for partition outputs normalised by l_c, and count l_c
+    twice for the unnormalised sum the page's partition step stores."""
+    rng = np.random.default_rng(5)
+    s = rng.normal(size=40) * 2
+    v = rng.normal(size=(40, 3))
+    p = np.exp(s - s.max())
+    exact = (p[:, None] * v).sum(0) / p.sum()
+    chunks = [slice(0, 7), slice(7, 25), slice(25, 40)]
+    m = np.array([s[c].max() for c in chunks])
+    l = np.array([np.exp(s[c] - s[c].max()).sum() for c in chunks])
+    acc = np.array([(np.exp(s[c] - s[c].max())[:, None] * v[c]).sum(0) for c in chunks])
+    w = np.exp(m - m.max()) * l
+    normalised = (w[:, None] * (acc / l[:, None])).sum(0) / w.sum()
+    unnormalised = (w[:, None] * acc).sum(0) / w.sum()
+    assert np.allclose(normalised, exact, atol=1e-14)
+    assert not np.allclose(unnormalised, exact, atol=1e-3)
+
+
+def test_page_permutation_is_bit_identical():
+    case = random_case(31, D=32, BS=4, B=3, max_q=12, max_kv_extra=60, E=5)
+    out, lse = _run(case)
+    g = torch.Generator().manual_seed(99)
+    NB = case.num_blocks
+    perm = torch.randperm(NB, generator=g)          # new physical slot of old page p is perm[p]
+    kc = torch.empty_like(case.key_cache)
+    vc = torch.empty_like(case.value_cache)
+    kc[perm] = case.key_cache
+    vc[perm] = case.value_cache
+    bt = case.block_table.clone()
+    valid = bt >= 0
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    case.key_cache, case.value_cache, case.block_table = kc, vc, bt
+    out2, lse2 = _run(case)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_block_size_one_equals_block_size_sixteen():
+    case16 = random_case(41, D=16, BS=16, B=2, E=7)
+    out16, lse16 = _run(case16)
+    # re-page the same logical K/V with one token per page
+    K, V, rows = [], [], []
+    off = 0
+    for b in range(case16.B):
+        Lk = case16.kv_lens[b]
+        npg = -(-Lk // 16)
+        pages = case16.block_table[b, :npg].long()
+        K.append(case16.key_cache[pages].reshape(-1, case16.Hkv, case16.D)[:Lk])
+        V.append(case16.value_cache[pages].reshape(-1, case16.Hkv, case16.D)[:Lk])
+        rows.append(list(range(off, off + Lk)))
+        off += Lk
+    kc = torch.cat(K).unsqueeze(1)
+    vc = torch.cat(V).unsqueeze(1)
+    width = max(len(r) for r in rows)
+    bt = torch.full((case16.B, width), -1, dtype=torch.int32)
+    for b, r in enumerate(rows):
+        bt[b, :len(r)] = torch.tensor(r, dtype=torch.int32)
+    out1, lse1 = oracle.attention(case16.q, kc, vc, bt, case16.cache_seqlens, case16.cu_seqlens_q,
+                                  **case16.oracle_kwargs())
+    assert np.array_equal(out1, out16) and np.array_equal(lse1, lse16)
+
+
+def test_request_permutation_and_one_at_a_time():
+    case = random_case(51, D=16, B=4, E=9, max_q=10)
+    out, lse = _run(case)
+    cu = case.cu_seqlens_q.tolist()
+    for b in range(case.B):
+        t0, t1 = cu[b], cu[b + 1]
+        sub = build_case("one", [case.q_lens[b]], [case.kv_lens[b]], H=case.H, Hkv=case.Hkv, D=case.D,
+                         BS=case.BS, E=0, seed=0)
+        sub.q = case.q[t0:t1]
+        sub.key_cache, sub.value_cache = case.key_cache, case.value_cache
+        sub.block_table = case.block_table[b:b + 1]
+        sub.cache_seqlens = case.cache_seqlens[b:b + 1]
+        sub.E = case.E
+        sub.rel_logits = case.rel_logits[t0:t1]
+        sub.causal, sub.window_left, sub.window_right = case.causal, case.window_left, case.window_right
+        o1, l1 = _run(sub)
+        assert np.array_equal(o1, out[t0:t1]) and np.array_equal(l1, lse[t0:t1])
+    # reverse the request order
+    order = list(reversed(range(case.B)))
+    q = torch.cat([case.q[cu[b]:cu[b + 1]] for b in order])
+    rel = torch.cat([case.rel_logits[cu[b]:cu[b + 1]] for b in order])
+    cu2 = oracle.cu_seqlens_from_lengths([case.q_lens[b] for b in order])
+    o2, l2 = oracle.attention(q, case.key_cache, case.value_cache, case.block_table[order],
+                              case.cache_seqlens[order], torch.tensor(cu2, dtype=torch.int32),
+                              **{**case.oracle_kwargs(), "rel_logits": rel})
+    want = np.concatenate([out[cu[b]:cu[b + 1]] for b in order])
+    assert np.array_equal(o2, want)
+
+
+def test_sampled_rows_equal_full_rows():
+    case = random_case(61, D=16, B=3, E=9)
+    out, lse = _run(case)
+    rows = np.array([0, 5, case.T * case.H - 1, 3], dtype=np.int64)
+    rows = rows[rows < case.T * case.H]
+    o, l = _run(case, rows=rows)
+    flat_o = out.reshape(-1, case.D)
+    flat_l = lse.reshape(-1)
+    assert np.array_equal(o, flat_o[rows]) and np.array_equal(l, flat_l[rows])
+
+
+# --- error behaviour ---------------------------------------------------------------
+
+def test_bad_page_id_is_reported():
+    case = build_case("bad", [2], [20], H=2, Hkv=1, D=8, BS=4, E=0, seed=1)
+    case.block_table[0, 2] = case.num_blocks + 3
+    with pytest.raises(oracle.OracleError):
+        _run(case)
+
+
+def test_non_monotone_cu_is_reported():
+    case = build_case("cu", [2, 3], [4, 5], H=2, Hkv=1, D=8, BS=4, E=0, seed=1)
+    case.cu_seqlens_q = torch.tensor([0, 4, 5], dtype=torch.int32)  # request 0 claims 4 tokens
+    case.cu_seqlens_q[1] = 6
+    with pytest.raises(oracle.OracleError):
+        _run(case)
+
+
+def test_round_to_bf16_matches_torch():
+    x = np.random.default_rng(0).normal(size=10000) * 10.0 ** np.random.default_rng(1).integers(-6, 6, 10000)
+    want = torch.from_numpy(x).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.round_to_bf16(x), want)
