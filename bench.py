@@ -1,0 +1,467 @@
+"""Benchmark of the paged varlen rel-bias attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one call of the whole hot path (device plan, decode and/or prefill
+kernels, split-KV merge) over one batch of synthetic input already resident
+in HBM.  The headline line is the decode batch (64 decodes, Lk ~ U{1024..32768},
+H 32, Hkv 8, E 1024): `value` = algorithmic KV bytes read / step time (GB/s).
+The chunked-prefill (TFLOP/s on unmasked pairs), long batch-1 decode and
+continuous-batch workloads are measured in the same run and reported under
+"workloads".  Inputs are larger than L2 (no flush needed).  `--impl reference`
+times the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged rel-bias attn: decode KV-read GB/s & prefill TFLOP/s (% of roofline)"
+HEADLINE = "decode_batch"
+SECONDARY = ["chunked_prefill", "long_decode", "continuous_batch"]
+D = 128
+
+
+# ---------------------------------------------------------------------------------- work model
+
+def work_of(case):
+    """Algorithmic work of one step: KV bytes of decode-shaped rows, flops of visible pairs.
+
+    Decode: sum over decode requests of (#visible keys) * Hkv * D * 2 (K and V) * 2 bytes.
+    Prefill: 4 * D * H * (#visible (q, k) pairs) over prefill requests.
+    """
+    G = case.H // case.Hkv
+    kv_bytes = 0
+    flops = 0
+    pairs = 0
+    for lq, lk in zip(case.q_lens, case.kv_lens):
+        n_pairs = 0
+        for i in range(lq):
+            qa = i + lk - lq
+            lo = max(0, qa - case.window_left) if case.window_left >= 0 else 0
+            hi = lk - 1
+            if case.causal:
+                hi = min(hi, qa)
+            if case.window_right >= 0:
+                hi = min(hi, qa + case.window_right)
+            n_pairs += max(0, hi - lo + 1)
+        if lq * G <= 16:
+            # each key of the union of visible ranges is read once for all heads
+            qa0, qa1 = lk - lq, lk - 1
+            lo = max(0, qa0 - case.window_left) if case.window_left >= 0 else 0
+            hi = min(lk - 1, qa1) if case.causal else lk - 1
+            if case.window_right >= 0:
+                hi = min(hi, qa1 + case.window_right)
+            kv_bytes += max(0, hi - lo + 1) * case.Hkv * D * 2 * 2
+        else:
+            pairs += n_pairs
+            flops += 4 * D * case.H * n_pairs
+    return kv_bytes, flops, pairs
+
+
+def total_bytes(case):
+    """Compulsory HBM bytes of one step (reported beside the algorithmic headline)."""
+    kv, _, _ = work_of(case)
+    G = case.H // case.Hkv
+    b = case.q.numel() * 2 * 2  # q in, out
+    pre_keys = 0
+    for lq, lk in zip(case.q_lens, case.kv_lens):
+        if lq * G > 16:
+            pre_keys += lk
+    b += pre_keys * case.Hkv * D * 2 * 2
+    if case.E > 0:
+        b += _bias_bytes(case)
+    return kv + b
+
+
+def _bias_bytes(case):
+    n = 0
+    for lq, lk in zip(case.q_lens, case.kv_lens):
+        # row i reads rd in [0, min(E, visible extent)) : count with a closed form per row
+        for i in range(lq):
+            qa = i + lk - lq
+            hi_rd = qa  # keys j >= 0
+            if case.window_left >= 0:
+                hi_rd = min(hi_rd, case.window_left)
+            n += max(0, min(case.E, hi_rd + 1))
+    return n * case.H * 4
+
+
+# ---------------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_varlen_attention_causal_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        if t.get("source_hash") != kernel_source_hash():
+            return None
+        return t["kernels"][kernel][workload]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import paged_varlen_attention_causal_gb300 as ink
+    from workloads import WORKLOADS, workload
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ink.build()
+    ink.load()
+    peaks = load_peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def call(case, out, lse, splits=0, stream=None):
+        return ink.ink_rel_attn_varlen(
+            case.q, case.key_cache, case.value_cache, block_table=case.block_table,
+            cache_seqlens=case.cache_seqlens, cu_seqlens_q=case.cu_seqlens_q, max_seqlen_q=case.max_seqlen_q,
+            softmax_scale=case.softmax_scale, causal=case.causal, window_left=case.window_left,
+            window_right=case.window_right, rel_extent=case.E, rel_logits=case.rel_logits, num_splits=splits,
+            out=out, lse=lse)
+
+    def measure(name, steps, warmup, main_kernel):
+        case = workload(name, device=dev)
+        out = torch.empty_like(case.q)
+        lse = torch.empty(case.T, case.H, dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(warmup):
+            call(case, out, lse)
+        torch.cuda.synchronize(dev)
+        flags = ink.read_device_errors()
+        if flags & ~ink.DEVERR["EMPTY_ROWS"]:
+            raise RuntimeError(f"{name}: device error flags {flags:#x}")
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = ink.launch_count()
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local_rank) as clk:
+            start.record(stream)
+            for k in range(steps):
+                ink.set_timing_events(main_kernel, kev[k][0], kev[k][1])
+                call(case, out, lse)
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+        ink.set_timing_events(main_kernel, None, None)
+        barrier()
+        launches = ink.launch_count() - n0
+        ms = start.elapsed_time(end) / steps
+        kms = sum(a.elapsed_time(b) for a, b in kev) / steps
+        t = torch.tensor([ms], device=dev)
+        if dist is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+        kv, flops, pairs = work_of(case)
+        res = {"workload": name, "desc": WORKLOADS[name], "ms_per_step": ms_max, "kernel_ms": kms,
+               "kv_bytes": kv, "flops": flops, "launches": launches, "clocks": clk.summary()}
+        # end-to-end through the public API with host buffers
+        pin = {k: getattr(case, k).to("cpu").pin_memory() for k in
+               ("q", "block_table", "cache_seqlens", "cu_seqlens_q")}
+        if case.rel_logits is not None:
+            pin["rel_logits"] = case.rel_logits.to("cpu").pin_memory()
+        host_out = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+        host_lse = torch.empty(case.T, case.H, dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+        e_steps = max(2, steps // 2)
+        for k in range(e_steps + 1):
+            if k == 1:
+                torch.cuda.synchronize(dev)
+                barrier()
+                t0 = time.perf_counter()
+            for key, v in pin.items():
+                getattr(case, key).copy_(v, non_blocking=True)
+            call(case, out, lse)
+            host_out.copy_(out, non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
+        te = torch.tensor([e2e_ms], device=dev)
+        if dist is not None:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        res["e2e_ms"] = float(te.item())
+        res["h2d_bytes"] = h2d
+        res["d2h_bytes"] = d2h
+        del case, out, lse, pin
+        torch.cuda.empty_cache()
+        return res
+
+    steps, warmup = args.steps, args.warmup
+    head = measure(HEADLINE, steps, warmup, "decode")
+    sec = {}
+    if not args.headline_only:
+        for name in SECONDARY:
+            kern = "prefill" if name == "chunked_prefill" else "decode"
+            sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
+
+    def roof_decode(r, name):
+        bytes_ = r["kv_bytes"]
+        ach = bytes_ / (r["kernel_ms"] * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic_of("ink_decode_kernel", name),
+                "peak_source": peaks["source"], "kernel": "ink_decode_kernel"}
+
+    def roof_prefill(r, name):
+        ach = r["flops"] / (r["kernel_ms"] * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic_of("ink_prefill_kernel", name),
+                "peak_source": peaks["source"], "kernel": "ink_prefill_kernel"}
+
+    if rank != 0:
+        return
+    value = world * head["kv_bytes"] / (head["ms_per_step"] * 1e-3) / 1e9
+    e2e = world * head["kv_bytes"] / (head["e2e_ms"] * 1e-3) / 1e9
+    workloads_out = {}
+    for name, r in sec.items():
+        entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
+                 "gpu_launches": r["launches"], "clocks": r["clocks"]}
+        if name == "chunked_prefill":
+            entry.update({"metric": "prefill TFLOP/s (visible pairs)",
+                          "value": round(r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                          "roofline": roof_prefill(r, name)})
+        elif name == "long_decode":
+            entry.update({"metric": "decode KV-read GB/s", "value": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
+                          "unit": "GB/s", "roofline": roof_decode(r, name)})
+        else:
+            entry.update({"metric": "decode KV-read GB/s + prefill TFLOP/s",
+                          "decode_gbs": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
+                          "prefill_tflops": round(r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12, 2),
+                          "roofline_time_frac": round(max(r["kv_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                                                          r["flops"] / (peaks["bf16_tflops"] * 1e12))
+                                                      / (r["ms_per_step"] * 1e-3), 4)})
+        workloads_out[name] = entry
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(HEADLINE, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(head["ms_per_step"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads/)",
+        "config": {"workload": HEADLINE, "desc": WORKLOADS[HEADLINE], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (KV cache 4.4 GB), no flush"},
+        "roofline": roof_decode(head, HEADLINE),
+        "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": head["h2d_bytes"],
+                "d2h_bytes_per_step": head["d2h_bytes"], "ms_per_step": round(head["e2e_ms"], 4),
+                "note": "q, rel_logits and metadata copied from pinned host memory and out/lse read back "
+                        "every step; the paged KV cache is resident state in HBM"},
+        "gpu_launches": head["launches"],
+        "clocks": head["clocks"],
+        "cpu_baseline": cpu,
+        "workloads": workloads_out,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- oracle arm
+
+def cpu_baseline(name, seconds):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample of the workload:
+    whole requests (all heads) in order until about `seconds` of CPU work; returns the same metric."""
+    import numpy as np
+
+    import oracle
+    from workloads import workload
+
+    case = workload(name, device="cpu")
+    oracle.build()
+    threads = oracle.threads()
+    kw = case.oracle_kwargs()
+    G = case.H // case.Hkv
+    done_bytes = 0
+    done_flops = 0
+    reqs = 0
+    t0 = time.perf_counter()
+    cu = case.cu_seqlens_q.tolist()
+    for b in range(case.B):
+        rows = np.arange(cu[b] * case.H, cu[b + 1] * case.H, dtype=np.int64)
+        if rows.size == 0:
+            continue
+        oracle.attention(case.q, case.key_cache, case.value_cache, case.block_table, case.cache_seqlens,
+                         case.cu_seqlens_q, rows=rows, **kw)
+        lq, lk = case.q_lens[b], case.kv_lens[b]
+        sub = type("S", (), {})()
+        sub.H, sub.Hkv, sub.E, sub.causal = case.H, case.Hkv, case.E, case.causal
+        sub.window_left, sub.window_right = case.window_left, case.window_right
+        sub.q_lens, sub.kv_lens = [lq], [lk]
+        kvb, fl, _ = work_of(sub)
+        done_bytes += kvb
+        done_flops += fl
+        reqs += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    cpu_name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    cpu_name = ln.split(":", 1)[1].strip()
+                    break
+    except Exception:
+        pass
+    return {"value": round(done_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reqs} of {case.B} requests of {name} (all heads), {dt:.1f} s",
+            "seconds": round(dt, 2), "cpu": cpu_name}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from workloads import WORKLOADS, workload  # noqa: F401
+
+    times = []
+    val = None
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline(HEADLINE, args.cpu_seconds / max(1, args.steps))
+        if k >= args.warmup:
+            times.append(r)
+    vals = [r["value"] for r in times]
+    val = statistics.median(vals)
+    last = times[-1]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads/)",
+        "config": {"workload": HEADLINE, "desc": WORKLOADS[HEADLINE], "parallelism": "host cores"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * ink_attn.h -- C ABI of the GB300 (sm_103a) paged varlen causal GQA
+ * attention with the Inkling additive relative bias.
+ *
+ * The operation is the one `inkling_fa4_rel_attention` performs in vLLM's
+ * fa4_rel_attention.py, as quoted and explained by the article
+ * "vllm中提取Inkling FA4 Relative Attention算子基础的base优化版本"
+ * (nxmr.cn/news/19446): its wrapper signature (source lines L101-L117, the
+ * article's layer 3 "参数签名"), the score modification that adds the bias
+ * (score_mod_rel_bias, source lines L25-L57) and the split-KV count
+ * (inkling_fa4_num_splits, source lines L60-L98).  The split-KV merge
+ * follows the log-sum-exp Phase 2 of the "paged_attention_v2_pytorch.py"
+ * page (dev.modelhub.org.cn), and the paged/varlen conventions follow the
+ * mini-vllm tutorial "Step 15: FlashAttention 封装" (block_table and
+ * cu_seqlens sections).
+ *
+ * Definition.  For request b with Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b]
+ * and Lk = cache_seqlens[b], token i < Lq (global row t = cu_seqlens_q[b] + i)
+ * and query head h (KV head g = h / (num_heads / num_kv_heads)):
+ *     q_abs = i + Lk - Lq                      (bottom-right causal alignment)
+ *     key j < Lk is visible iff (!causal || j <= q_abs)
+ *                             && (window_left  < 0 || j >= q_abs - window_left)
+ *                             && (window_right < 0 || j <= q_abs + window_right)
+ *     s_j = softmax_scale * <q[t][h], K_j[g]> + bias,  rd = q_abs - j,
+ *     bias = rel_logits[t][h][rd] if 0 <= rd < rel_extent, else 0
+ *     K_j = key_cache[block_table[b][j / block_size]][j % block_size]
+ *     out[t][h] = sum_j softmax(s)_j V_j[g]   (bf16, round to nearest even)
+ *     lse[t][h] = ln sum_j exp(s_j)           (natural log, fp32)
+ * A row with no visible key gets out = 0 and lse = -inf.
+ *
+ * Every call is asynchronous on `stream`, allocates nothing, keeps no state
+ * between calls and performs no host synchronisation.
+ */
+#ifndef INK_ATTN_H
+#define INK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define INK_API __attribute__((visibility("default")))
+#else
+#define INK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *ink_stream_t;
+
+/* Shapes a C interface cannot read from tensors. */
+typedef struct {
+    int32_t num_tokens;          /* T: rows of q, out, lse, rel_logits      */
+    int32_t batch;               /* B: requests                               */
+    int32_t num_heads;           /* H: query heads                            */
+    int32_t num_kv_heads;        /* Hkv: KV heads, H % Hkv == 0               */
+    int32_t head_dim;            /* D: must be 128                            */
+    int32_t num_blocks;          /* physical pages in each cache              */
+    int32_t block_size;          /* keys per page: a multiple of 16           */
+    int32_t max_blocks_per_seq;  /* width of block_table                      */
+} ink_attn_dims;
+
+typedef enum {
+    INK_OK = 0,
+    INK_ERR_INVALID_ARG = 1,  /* bad pointer, shape, scalar or alignment     */
+    INK_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, ...   */
+    INK_ERR_WORKSPACE = 3,    /* workspace smaller than the size query says  */
+    INK_ERR_CUDA = 4          /* a CUDA runtime / driver call failed         */
+} ink_status;
+
+/* Device-side data errors, OR-ed into the workspace's error word by the
+ * kernels (they never trap); read with ink_rel_attn_read_device_errors.
+ * A request that raises CU_SEQLENS, SEQLEN_Q or SEQLEN_K is skipped: its
+ * rows of out and lse are left as they were.  With PAGE_ID the keys of the
+ * bad page read as zeros. */
+#define INK_DEVERR_PAGE_ID    0x01u /* block_table entry needed for a visible key is outside [0, num_blocks) */
+#define INK_DEVERR_CU_SEQLENS 0x02u /* cu_seqlens_q not non-decreasing within [0, T], or cu[0] != 0, cu[B] != T */
+#define INK_DEVERR_SEQLEN_Q   0x04u /* a request has more query tokens than max_seqlen_q */
+#define INK_DEVERR_SEQLEN_K   0x08u /* cache_seqlens[b] < 0 or > max_blocks_per_seq * block_size */
+#define INK_DEVERR_EMPTY_ROWS 0x10u /* informational: some rows saw no key (out 0, lse -inf), e.g. causal with Lk < Lq */
+#define INK_DEVERR_TIMEOUT    0x100u /* a bounded pipeline wait gave up; outputs of the call are undefined */
+
+/*
+ * Bytes of device workspace one call needs.  `num_splits` as in
+ * ink_rel_attn_varlen (0 = the library's choice; the size then covers every
+ * choice the library can make for these dims).  The workspace holds the
+ * error word, the device-built work lists and, when splits are used, the
+ * per-split partial outputs (fp32) and log-sum-exps.  Returns 0 for
+ * invalid dims.
+ */
+INK_API size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t max_seqlen_q,
+                                   int32_t num_splits);
+
+/*
+ * The split-KV count the library picks when called with num_splits = 0:
+ * the cap on splits per work unit for decode-shaped calls
+ * (max_seqlen_q * H / Hkv <= 16) and for prefill-shaped calls otherwise.
+ * It is re-derived for the GB300 SM count from the page's heuristic
+ * (inkling_fa4_num_splits, source lines L60-L98): enough units to fill every
+ * SM several times, with at least 16 keys per split.  `max_kv_len` bounds
+ * cache_seqlens.  Returns 0 for invalid dims.  Needs a current CUDA device.
+ */
+INK_API int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_seqlen_q,
+                                int32_t max_kv_len, int32_t window_left, int32_t window_right);
+
+/*
+ * The attention itself.
+ *   q             bf16 (T, H, D), contiguous, 16-byte aligned.
+ *   key_cache     bf16 (num_blocks, block_size, Hkv, D), contiguous, 16-byte aligned.
+ *   value_cache   same shape and alignment as key_cache (two pointers into a
+ *                 stacked (2, ...) cache are fine).
+ *   block_table   int32 (B, max_blocks_per_seq): logical page -> physical page.
+ *                 Entries at or beyond ceil(Lk / block_size) are never read
+ *                 (padding with -1 is fine); pages may be shared.
+ *   cache_seqlens int32 (B): KV length of each request, including this
+ *                 step's query tokens (the KV write happens first).
+ *   cu_seqlens_q  int32 (B+1): cu[0] = 0, non-decreasing, cu[B] = T.
+ *   max_seqlen_q  host bound on every Lq (a scheduling bound only: results
+ *                 do not depend on it as long as it is >= every Lq).
+ *   softmax_scale multiplies q.k before the bias is added; finite and > 0.
+ *   causal        nonzero: bottom-right causal mask.
+ *   window_left/right  -1 = unbounded on that side; (-1, -1) = no window.
+ *   rel_extent    E >= 0; rel_logits fp32 (T, H, E) contiguous, may be NULL
+ *                 when E == 0.  Entries at rd >= Lk or beyond a window are
+ *                 never read.
+ *   num_splits    0 = library choice, 1 = no split (no combine pass),
+ *                 S > 1: each work unit's visible KV range is cut into
+ *                 chunks of ceil(max visible keys / S) keys (rounded to 16).
+ *   out           bf16 (T, H, D), contiguous, 16-byte aligned.
+ *   lse           fp32 (T, H) or NULL.
+ *   workspace     device memory of at least
+ *                 ink_rel_attn_workspace_size(dims, max_seqlen_q, num_splits)
+ *                 bytes, 256-byte aligned; it must not be used by another
+ *                 call that overlaps this one on the GPU.
+ *   stream        CUDA stream the kernels are launched on.
+ * Host-side checks return INK_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE
+ * before anything is launched; a launch failure returns INK_ERR_CUDA.
+ * Data errors found on the device are reported through the error word.
+ */
+INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
+                               const void *q, const void *key_cache, const void *value_cache,
+                               const int32_t *block_table, const int32_t *cache_seqlens,
+                               const int32_t *cu_seqlens_q, int32_t max_seqlen_q,
+                               float softmax_scale, int causal,
+                               int32_t window_left, int32_t window_right,
+                               int32_t rel_extent, const float *rel_logits,
+                               int32_t num_splits,
+                               void *out, float *lse,
+                               void *workspace, size_t workspace_bytes,
+                               ink_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+INK_API const char *ink_status_string(ink_status status);
+
+/*
+ * Debug helper: copies the error word of the last call that used
+ * `workspace` into *flags (INK_DEVERR_* bits).  Synchronises `stream`.
+ */
+INK_API ink_status ink_rel_attn_read_device_errors(const void *workspace, ink_stream_t stream,
+                                           uint32_t *flags);
+
+/* Library version, e.g. 100 for 0.1.0. */
+INK_API int32_t ink_attn_version(void);
+
+/*
+ * Measurement hooks (no effect on results).
+ * ink_set_timing_events: while set, every call records `start_event` on its
+ * stream just before launching the named kernel and `stop_event` just after
+ * it (both cudaEvent_t, owned by the caller; NULL clears the hook).
+ * ink_launch_count: number of kernels this library has launched in the
+ * process so far.
+ */
+typedef enum {
+    INK_KERNEL_PREPASS = 1,
+    INK_KERNEL_DECODE = 2,
+    INK_KERNEL_PREFILL = 3,
+    INK_KERNEL_COMBINE = 4
+} ink_kernel_id;
+
+INK_API void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event);
+INK_API uint64_t ink_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INK_ATTN_H */

@@ -1,0 +1,237 @@
+"""GB300 (sm_103a) paged varlen causal GQA attention with the Inkling relative bias.
+
+Thin Python binding over the C ABI in ``include/ink_attn.h`` (libinkattn.so):
+argument checking and marshalling only; every step of the computation runs in
+the library's CUDA kernels.  PyTorch provides device memory and the stream.
+The binding raises if the library is not built: there is no fallback path.
+
+    out = ink_rel_attn_varlen(q, key_cache, value_cache, block_table=...,
+                              cache_seqlens=..., cu_seqlens_q=..., max_seqlen_q=...,
+                              softmax_scale=..., causal=True, window_left=-1,
+                              window_right=-1, rel_extent=E, rel_logits=...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "LibraryNotBuilt", "InkError", "Dims", "build", "load", "ink_rel_attn_varlen", "workspace_size",
+    "num_splits", "read_device_errors", "version", "DEVERR", "set_timing_events", "launch_count",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libinkattn.so")
+
+DEVERR = {
+    "PAGE_ID": 0x01, "CU_SEQLENS": 0x02, "SEQLEN_Q": 0x04, "SEQLEN_K": 0x08, "EMPTY_ROWS": 0x10,
+    "TIMEOUT": 0x100,
+}
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace too small",
+           4: "CUDA error"}
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class InkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_tokens", "batch", "num_heads", "num_kv_heads", "head_dim", "num_blocks", "block_size",
+        "max_blocks_per_seq")]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libinkattn.so in-tree (nvcc, sm_103a)."""
+    from ._build import build as _b
+
+    return _b(force=force, verbose=verbose)
+
+
+def load(path: Optional[str] = None):
+    """Load the C-ABI library (raises LibraryNotBuilt when it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise LibraryNotBuilt(f"{p} is missing: run paged_varlen_attention_causal_gb300.build() first")
+        lib = ctypes.CDLL(p)
+        i32, sz, vp = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+        dp = ctypes.POINTER(Dims)
+        lib.ink_rel_attn_workspace_size.restype = sz
+        lib.ink_rel_attn_workspace_size.argtypes = [dp, i32, i32]
+        lib.ink_rel_attn_num_splits.restype = i32
+        lib.ink_rel_attn_num_splits.argtypes = [dp, i32, i32, i32, i32]
+        lib.ink_rel_attn_varlen.restype = ctypes.c_int
+        lib.ink_rel_attn_varlen.argtypes = [
+            dp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, i32, i32, i32, vp, i32,
+            vp, vp, vp, sz, vp]
+        lib.ink_status_string.restype = ctypes.c_char_p
+        lib.ink_status_string.argtypes = [ctypes.c_int]
+        lib.ink_rel_attn_read_device_errors.restype = ctypes.c_int
+        lib.ink_rel_attn_read_device_errors.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.ink_attn_version.restype = i32
+        lib.ink_set_timing_events.restype = None
+        lib.ink_set_timing_events.argtypes = [ctypes.c_int, vp, vp]
+        lib.ink_launch_count.restype = ctypes.c_uint64
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def version() -> int:
+    return int(load().ink_attn_version())
+
+
+KERNELS = {"prepass": 1, "decode": 2, "prefill": 3, "combine": 4}
+
+
+def set_timing_events(kernel: str, start=None, stop=None) -> None:
+    """Record torch.cuda.Event `start`/`stop` around the named kernel's launches (None clears)."""
+    load().ink_set_timing_events(KERNELS[kernel], None if start is None else start.cuda_event,
+                                 None if stop is None else stop.cuda_event)
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load().ink_launch_count())
+
+
+def _dims(q, key_cache, block_table) -> Dims:
+    T, H, D = q.shape
+    NB, BS, Hkv, D2 = key_cache.shape
+    B, W = block_table.shape
+    return Dims(T, B, H, Hkv, D, NB, BS, W)
+
+
+def workspace_size(dims: Dims, max_seqlen_q: int, num_splits: int = 0) -> int:
+    n = load().ink_rel_attn_workspace_size(ctypes.byref(dims), int(max_seqlen_q), int(num_splits))
+    if n == 0:
+        raise InkError(1, "ink_rel_attn_workspace_size")
+    return int(n)
+
+
+def num_splits(dims: Dims, max_seqlen_q: int, max_kv_len: int, window_left: int = -1,
+               window_right: int = -1) -> int:
+    return int(load().ink_rel_attn_num_splits(ctypes.byref(dims), int(max_seqlen_q), int(max_kv_len),
+                                              int(window_left), int(window_right)))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device: torch.device, nbytes: int, stream) -> torch.Tensor:
+    """Per (device, stream) workspace, grown on demand (calls on one stream are ordered)."""
+    key = (device.index, int(stream.cuda_stream))
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _check(t: torch.Tensor, name: str, dtype, dim: int, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got shape {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q: int, softmax_scale: float, causal: bool = True,
+                        window_left: int = -1, window_right: int = -1, rel_extent: int = 0,
+                        rel_logits=None, num_splits: int = 0, out=None, lse=None,
+                        return_lse: bool = False, workspace=None, stream=None):
+    """Paged varlen attention with the Inkling relative bias (see include/ink_attn.h).
+
+    Keyword arguments follow ``inkling_fa4_rel_attention`` (fa4_rel_attention.py
+    as quoted by the nxmr.cn article, source lines L101-L163), with the window
+    passed as two integers (-1 = unbounded).  Returns ``out`` (and ``lse``
+    when ``return_lse``).
+    """
+    lib = load()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    _check(q, "q", torch.bfloat16, 3, dev)
+    _check(key_cache, "key_cache", torch.bfloat16, 4, dev)
+    _check(value_cache, "value_cache", torch.bfloat16, 4, dev)
+    if value_cache.shape != key_cache.shape:
+        raise ValueError("value_cache and key_cache shapes differ")
+    _check(block_table, "block_table", torch.int32, 2, dev)
+    _check(cache_seqlens, "cache_seqlens", torch.int32, 1, dev)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, dev)
+    dims = _dims(q, key_cache, block_table)
+    if cache_seqlens.shape[0] != dims.batch or cu_seqlens_q.shape[0] != dims.batch + 1:
+        raise ValueError("cache_seqlens / cu_seqlens_q do not match block_table's batch")
+    rel_ptr = None
+    if rel_extent > 0:
+        if rel_logits is None:
+            raise ValueError("rel_extent > 0 needs rel_logits")
+        _check(rel_logits, "rel_logits", torch.float32, 3, dev)
+        if tuple(rel_logits.shape) != (dims.num_tokens, dims.num_heads, rel_extent):
+            raise ValueError("rel_logits must be (num_tokens, num_heads, rel_extent)")
+        rel_ptr = rel_logits.data_ptr()
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((dims.num_tokens, dims.num_heads), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, 2, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    need = workspace_size(dims, max_seqlen_q, num_splits)
+    if workspace is None:
+        workspace = _workspace(dev, need, stream)
+    rc = lib.ink_rel_attn_varlen(
+        ctypes.byref(dims), q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+        block_table.data_ptr(), cache_seqlens.data_ptr(), cu_seqlens_q.data_ptr(), int(max_seqlen_q),
+        float(softmax_scale), int(bool(causal)), int(window_left), int(window_right), int(rel_extent),
+        rel_ptr, int(num_splits), out.data_ptr(), None if lse is None else lse.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(stream.cuda_stream))
+    if rc != 0:
+        raise InkError(rc, "ink_rel_attn_varlen")
+    return (out, lse) if return_lse else out
+
+
+def read_device_errors(workspace: Optional[torch.Tensor] = None, stream=None, device=None) -> int:
+    """Error word (DEVERR bits) of the last call that used `workspace`; synchronises the stream."""
+    lib = load()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        workspace = _ws_cache.get((dev.index, int(stream.cuda_stream)))
+        if workspace is None:
+            return 0
+    flags = ctypes.c_uint32(0)
+    rc = lib.ink_rel_attn_read_device_errors(workspace.data_ptr(), int(stream.cuda_stream), ctypes.byref(flags))
+    if rc != 0:
+        raise InkError(rc, "ink_rel_attn_read_device_errors")
+    return int(flags.value)

@@ -1,0 +1,421 @@
+// ink_api.cu -- host plan and C ABI (a1): argument validation, the split
+// heuristic re-derived for the GB300 SM count, workspace layout, TMA tensor
+// maps, and the stream-ordered launches (prepass, decode, prefill, combine).
+// Nothing here synchronises the host; nothing here allocates.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "ink_common.cuh"
+
+namespace ink {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA on sm_100-class SMs
+constexpr int kDecSharedBytes = 512;   // mbarriers + item ring of the decode kernel (upper bound)
+constexpr int kPfSharedBytes = 256;    // mbarriers of the prefill kernel (upper bound)
+constexpr int kDecMaxStages = 8;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct TimingHook {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+TimingHook g_hooks[5];
+std::mutex g_hook_mutex;
+std::atomic<unsigned long long> g_launches{0};
+
+// Launch `fn` (returning cudaError_t) between the optional timing events of `kernel`.
+template <typename F>
+cudaError_t timed_launch(int kernel, cudaStream_t stream, F &&fn)
+{
+    TimingHook h;
+    {
+        std::lock_guard<std::mutex> lk(g_hook_mutex);
+        h = g_hooks[kernel];
+    }
+    if (h.start && cudaEventRecord(h.start, stream) != cudaSuccess) return cudaErrorInvalidValue;
+    cudaError_t e = fn();
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e == cudaSuccess && h.stop) e = cudaEventRecord(h.stop, stream);
+    return e;
+}
+
+int sm_count_of_current_device()
+{
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) cache[dev] = n;
+    return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+struct Plan {
+    int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0;
+    int S_dec = 1, S_pf = 1, chunk_dec = 1, chunk_pf = 1;
+    int dec_rows = 0, lq_dec = 0;
+    long long dec_cap = 0, pf_cap = 0, units_cap = 0;
+    bool any_prefill = false, any_decode = false;
+    // workspace offsets
+    size_t off_dec_items = 0, off_pf_items = 0, off_dec_off = 0, off_unit_off = 0;
+    size_t off_pdo = 0, off_pdl = 0, off_ppo = 0, off_ppl = 0, total = 0;
+};
+
+bool dims_ok(const ink_attn_dims *d)
+{
+    return d && d->num_tokens >= 0 && d->batch >= 1 && d->num_heads >= 1 && d->num_kv_heads >= 1 &&
+           d->num_heads % d->num_kv_heads == 0 && d->head_dim >= 1 && d->num_blocks >= 1 && d->block_size >= 1 &&
+           d->max_blocks_per_seq >= 1;
+}
+
+bool dims_supported(const ink_attn_dims *d)
+{
+    const int G = d->num_heads / d->num_kv_heads;
+    return d->head_dim == kHeadDim && d->block_size % kKeyGroup == 0 && G <= kTileRows &&
+           (long long)d->num_blocks * d->block_size < (1ll << 31);
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Upper bound on the visible 16-key groups of a unit whose q rows span
+// `span` consecutive positions.
+long long max_groups(const ink_attn_dims *d, int span, int causal, int wl, int wr)
+{
+    const long long keys = (long long)d->max_blocks_per_seq * d->block_size;
+    long long g = ceil_div(keys, kKeyGroup);
+    if (wl >= 0 && (causal || wr >= 0)) {
+        const long long right = causal ? (wr >= 0 ? std::min(wr, 0) : 0) : wr;
+        const long long w = (long long)wl + span + right;
+        g = std::min(g, ceil_div(w, kKeyGroup) + 1);
+    }
+    return std::max(1ll, g);
+}
+
+// Split counts re-derived for this GPU from the page heuristic's intent:
+// fill every SM several times over, never split below 16 keys, and keep the
+// partial traffic a small fraction of the KV bytes.
+int heuristic_splits_decode(long long batch, long long groups, int sms)
+{
+    const long long target_chunk = 32;  // 512 keys per split
+    long long s = ceil_div(groups, target_chunk);
+    if (batch * s < 4ll * sms) s = ceil_div(4ll * sms, batch);
+    s = std::min<long long>(s, groups);
+    s = std::min<long long>(s, 1024);
+    return (int)std::max(1ll, s);
+}
+
+int heuristic_splits_prefill(long long units, long long groups, int sms)
+{
+    if (units >= 2ll * sms) return 1;
+    long long s = ceil_div(2ll * sms, std::max(1ll, units));
+    s = std::min<long long>(s, ceil_div(groups, 8));  // at least one 128-key tile per split
+    s = std::min<long long>(s, 256);
+    return (int)std::max(1ll, s);
+}
+
+bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int causal, int wl, int wr, int sms,
+               Plan &pl)
+{
+    const int T = d->num_tokens, B = d->batch, H = d->num_heads, Hkv = d->num_kv_heads;
+    pl.G = H / Hkv;
+    pl.tpt = kTileRows / pl.G;
+    pl.fast_pack = (32 % pl.G == 0) ? 1 : 0;
+    pl.decode_kernel = (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
+    const long long msq = std::min<long long>(max_seqlen_q, std::max(T, 1));
+    pl.any_decode = pl.decode_kernel != 0;
+    pl.any_prefill = !pl.decode_kernel || msq * pl.G > kDecodeRows;
+    if (!pl.decode_kernel) pl.any_decode = false;
+    pl.lq_dec = pl.decode_kernel ? (int)std::min<long long>(kDecodeRows / pl.G, msq) : 0;
+    pl.dec_rows = pl.lq_dec * H;
+
+    const long long g_dec = max_groups(d, kDecodeRows / std::max(1, pl.G), causal, wl, wr);
+    const long long g_pf = max_groups(d, pl.tpt, causal, wl, wr);
+    if (num_splits > 0) {
+        pl.S_dec = pl.S_pf = num_splits;
+    } else {
+        pl.S_dec = heuristic_splits_decode(B, g_dec, sms);
+        const long long units = (long long)B * Hkv * ceil_div(msq * pl.G, kTileRows);
+        pl.S_pf = heuristic_splits_prefill(units, g_pf, sms);
+    }
+    pl.chunk_dec = (int)std::max(1ll, ceil_div(g_dec, pl.S_dec));
+    pl.chunk_pf = (int)std::max(1ll, ceil_div(g_pf, pl.S_pf));
+    if (pl.S_pf > 1) pl.chunk_pf = (int)(ceil_div(pl.chunk_pf, 8) * 8);  // whole 128-key tiles
+    const long long sdec_eff = ceil_div(g_dec, pl.chunk_dec);
+    const long long spf_eff = ceil_div(g_pf, pl.chunk_pf);
+    pl.S_pf = (int)std::max(1ll, spf_eff);
+
+    pl.dec_cap = pl.any_decode ? (long long)B * sdec_eff : 0;
+    pl.units_cap = pl.any_prefill ? ceil_div(T, pl.tpt) + B : 0;
+    pl.pf_cap = pl.any_prefill ? pl.units_cap * pl.S_pf * Hkv : 0;
+    if (pl.dec_cap > (1ll << 30) || pl.pf_cap > (1ll << 30)) return false;
+
+    size_t off = sizeof(WsHeader);
+    pl.off_dec_items = off; off = align256(off + sizeof(int2) * (size_t)pl.dec_cap);
+    pl.off_pf_items = off; off = align256(off + sizeof(int4) * (size_t)pl.pf_cap);
+    pl.off_dec_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
+    pl.off_unit_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
+    const bool dec_parts = pl.any_decode && sdec_eff > 1;
+    const bool pf_parts = pl.any_prefill && pl.S_pf > 1;
+    const size_t dec_rows_total = dec_parts ? (size_t)pl.dec_cap * pl.dec_rows : 0;
+    const size_t pf_rows_total = pf_parts ? (size_t)pl.units_cap * pl.S_pf * Hkv * kTileRows : 0;
+    pl.off_pdl = off; off = align256(off + sizeof(float) * dec_rows_total);
+    pl.off_pdo = off; off = align256(off + sizeof(float) * dec_rows_total * kHeadDim);
+    pl.off_ppl = off; off = align256(off + sizeof(float) * pf_rows_total);
+    pl.off_ppo = off; off = align256(off + sizeof(float) * pf_rows_total * kHeadDim);
+    pl.total = off;
+    return true;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool encode(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(map, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace ink
+
+using namespace ink;
+
+extern "C" {
+
+int32_t ink_attn_version(void) { return 100; }
+
+void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event)
+{
+    if ((int)kernel < 1 || (int)kernel > 4) return;
+    std::lock_guard<std::mutex> lk(g_hook_mutex);
+    g_hooks[kernel].start = static_cast<cudaEvent_t>(start_event);
+    g_hooks[kernel].stop = static_cast<cudaEvent_t>(stop_event);
+}
+
+uint64_t ink_launch_count(void) { return (uint64_t)g_launches.load(); }
+
+const char *ink_status_string(ink_status s)
+{
+    switch (s) {
+        case INK_OK: return "ok";
+        case INK_ERR_INVALID_ARG: return "invalid argument";
+        case INK_ERR_UNSUPPORTED: return "unsupported configuration";
+        case INK_ERR_WORKSPACE: return "workspace too small";
+        case INK_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t max_seqlen_q, int32_t num_splits)
+{
+    if (!dims_ok(dims) || max_seqlen_q < 1 || num_splits < 0 || !dims_supported(dims)) return 0;
+    const int sms = sm_count_of_current_device();
+    Plan pl;
+    // no window: the largest split count the heuristic can choose for these dims
+    if (!make_plan(dims, max_seqlen_q, num_splits, 1, -1, -1, sms > 0 ? sms : 152, pl)) return 0;
+    Plan pl2;  // non-causal needs no more than causal; take the max of both to be safe
+    if (make_plan(dims, max_seqlen_q, num_splits, 0, -1, -1, sms > 0 ? sms : 152, pl2))
+        return std::max(pl.total, pl2.total);
+    return pl.total;
+}
+
+int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_seqlen_q, int32_t max_kv_len,
+                                int32_t window_left, int32_t window_right)
+{
+    if (!dims_ok(dims) || max_seqlen_q < 1 || max_kv_len < 0 || !dims_supported(dims)) return 0;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return 0;
+    ink_attn_dims d = *dims;
+    const long long blocks = ceil_div(std::max(1, max_kv_len), d.block_size);
+    d.max_blocks_per_seq = (int)std::min<long long>(d.max_blocks_per_seq, blocks);
+    Plan pl;
+    if (!make_plan(&d, max_seqlen_q, 0, 1, window_left, window_right, sms, pl)) return 0;
+    const long long msq = std::min<long long>(max_seqlen_q, std::max(d.num_tokens, 1));
+    const bool decode_shaped = pl.decode_kernel && msq * pl.G <= kDecodeRows;
+    return decode_shaped ? pl.S_dec : pl.S_pf;
+}
+
+ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const void *key_cache,
+                               const void *value_cache, const int32_t *block_table, const int32_t *cache_seqlens,
+                               const int32_t *cu_seqlens_q, int32_t max_seqlen_q, float softmax_scale, int causal,
+                               int32_t window_left, int32_t window_right, int32_t rel_extent,
+                               const float *rel_logits, int32_t num_splits, void *out, float *lse, void *workspace,
+                               size_t workspace_bytes, ink_stream_t stream_handle)
+{
+    if (!dims_ok(dims)) return INK_ERR_INVALID_ARG;
+    if (!q || !key_cache || !value_cache || !block_table || !cache_seqlens || !cu_seqlens_q || !out || !workspace)
+        return INK_ERR_INVALID_ARG;
+    if (max_seqlen_q < 1 || window_left < -1 || window_right < -1 || rel_extent < 0 || num_splits < 0)
+        return INK_ERR_INVALID_ARG;
+    if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return INK_ERR_INVALID_ARG;
+    if (rel_extent > 0 && !rel_logits) return INK_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(cache_seqlens, 4) || !aligned(cu_seqlens_q, 4) ||
+        (lse && !aligned(lse, 4)) || (rel_logits && !aligned(rel_logits, 4)) || !aligned(workspace, 256))
+        return INK_ERR_INVALID_ARG;
+    if (!dims_supported(dims)) return INK_ERR_UNSUPPORTED;
+    if (dims->num_tokens == 0) return INK_OK;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return INK_ERR_CUDA;
+    Plan pl;
+    if (!make_plan(dims, max_seqlen_q, num_splits, causal ? 1 : 0, window_left, window_right, sms, pl))
+        return INK_ERR_UNSUPPORTED;
+    if (workspace_bytes < pl.total) return INK_ERR_WORKSPACE;
+
+    const int T = dims->num_tokens, H = dims->num_heads, Hkv = dims->num_kv_heads, E = rel_extent;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.T = T; p.B = dims->batch; p.H = H; p.Hkv = Hkv; p.G = pl.G; p.NB = dims->num_blocks;
+    p.BS = dims->block_size; p.MAXBLK = dims->max_blocks_per_seq; p.max_seqlen_q = max_seqlen_q;
+    p.softmax_scale = softmax_scale;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.inv_scale = 1.0f / softmax_scale;
+    p.causal = causal ? 1 : 0; p.wl = window_left; p.wr = window_right; p.E = E;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.kc = static_cast<const __nv_bfloat16 *>(key_cache);
+    p.vc = static_cast<const __nv_bfloat16 *>(value_cache);
+    p.bt = block_table; p.seqk = cache_seqlens; p.cu = cu_seqlens_q;
+    p.rel = E > 0 ? rel_logits : nullptr;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.hdr = reinterpret_cast<WsHeader *>(ws);
+    p.dec_items = reinterpret_cast<int2 *>(ws + pl.off_dec_items);
+    p.dec_items_cap = (int)pl.dec_cap;
+    p.pf_items = reinterpret_cast<int4 *>(ws + pl.off_pf_items);
+    p.pf_items_cap = (int)pl.pf_cap;
+    p.dec_off = reinterpret_cast<int *>(ws + pl.off_dec_off);
+    p.unit_off = reinterpret_cast<int *>(ws + pl.off_unit_off);
+    p.part_dec_lse = reinterpret_cast<float *>(ws + pl.off_pdl);
+    p.part_dec_o = reinterpret_cast<float *>(ws + pl.off_pdo);
+    p.dec_rows = pl.dec_rows;
+    p.part_pf_lse = reinterpret_cast<float *>(ws + pl.off_ppl);
+    p.part_pf_o = reinterpret_cast<float *>(ws + pl.off_ppo);
+    p.units_cap = (int)pl.units_cap;
+    p.S_pf = pl.S_pf;
+    p.decode_kernel = pl.decode_kernel;
+    p.chunk_dec = pl.chunk_dec;
+    p.chunk_pf = pl.chunk_pf;
+    p.tpt = pl.tpt;
+    p.fast_pack = pl.fast_pack;
+
+    // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
+    alignas(64) CUtensorMap tm_k, tm_v, tm_bdec, tm_bpf;
+    memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v);
+    memset(&tm_bdec, 0, sizeof tm_bdec); memset(&tm_bpf, 0, sizeof tm_bpf);
+    {
+        const cuuint64_t gd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv,
+                                  (cuuint64_t)dims->num_blocks * dims->block_size};
+        const cuuint64_t gs[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hkv * kHeadDim * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)kKeyGroup};
+        if (!encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, key_cache, gd, gs, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, value_cache, gd, gs, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return INK_ERR_CUDA;
+    }
+    // bias maps: rel_logits as (E, H, T) fp32, no swizzle; needs 16-byte rows
+    bool bias_dec_tma = false, bias_pf_tma = false;
+    if (E > 0 && E % 4 == 0 && aligned(rel_logits, 16)) {
+        const cuuint64_t gd[3] = {(cuuint64_t)E, (cuuint64_t)H, (cuuint64_t)T};
+        const cuuint64_t gs[2] = {(cuuint64_t)E * 4, (cuuint64_t)E * H * 4};
+        if (H <= 256) {
+            const cuuint32_t box[3] = {20, (cuuint32_t)H, 1};
+            bias_dec_tma = encode(&tm_bdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE);
+        }
+        const cuuint32_t box2[3] = {132, (cuuint32_t)pl.G, 1};
+        bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+
+    // 1. device-side plan
+    if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, stream); }) != cudaSuccess)
+        return INK_ERR_CUDA;
+
+    // 2. decode kernel
+    if (pl.any_decode && pl.dec_cap > 0) {
+        Params pd = p;
+        pd.bias_tma = bias_dec_tma ? 1 : 0;
+        const int kv_bytes = Hkv * 4096;
+        const int bias_slot = (H * 80 + 127) & ~127;
+        const int bias_bytes = (kDecodeRows / pl.G) * bias_slot;
+        const int stage_bytes = (2 * kv_bytes + bias_bytes + 1023) & ~1023;
+        int nst = (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
+        nst = std::min(nst, kDecMaxStages);
+        if (nst < 2) return INK_ERR_UNSUPPORTED;
+        const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
+        const int grid = (int)std::min<long long>(sms, pl.dec_cap);
+        if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
+                return launch_decode(pd, tm_k, tm_v, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, grid, smem,
+                                     stream);
+            }) != cudaSuccess)
+            return INK_ERR_CUDA;
+    }
+
+    // 3. prefill kernel
+    if (pl.any_prefill && pl.pf_cap > 0) {
+        Params pp = p;
+        pp.bias_tma = bias_pf_tma ? 1 : 0;
+        const int bias_slot = ((pl.G * 132 * 4) + 127) & ~127;
+        const size_t smem = 1024 + 32768 + 3 * 32768 + (size_t)pl.tpt * bias_slot + kPfSharedBytes;
+        if (smem > kSmemLimit) return INK_ERR_UNSUPPORTED;
+        const int grid = (int)std::min<long long>(sms, pl.pf_cap);
+        if (timed_launch(INK_KERNEL_PREFILL, stream,
+                         [&] { return launch_prefill(pp, tm_k, tm_v, tm_bpf, grid, smem, stream); }) != cudaSuccess)
+            return INK_ERR_CUDA;
+    }
+
+    // 4. split-KV merge
+    const long long sdec_eff = ceil_div(max_groups(dims, kDecodeRows / std::max(1, pl.G), causal, window_left,
+                                                   window_right),
+                                        pl.chunk_dec);
+    if ((pl.any_decode && sdec_eff > 1) || (pl.any_prefill && pl.S_pf > 1)) {
+        const long long rows = (long long)T * H;
+        const int grid = (int)ceil_div(rows, 8);
+        if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, grid, stream); }) != cudaSuccess)
+            return INK_ERR_CUDA;
+    }
+    return INK_OK;
+}
+
+ink_status ink_rel_attn_read_device_errors(const void *workspace, ink_stream_t stream_handle, uint32_t *flags)
+{
+    if (!workspace || !flags) return INK_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return INK_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return INK_ERR_CUDA;
+    *flags = v;
+    return INK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,300 @@
+// ink_common.cuh -- shared device-side definitions of the GB300 attention path:
+// launch parameters, workspace layout, the work-unit arithmetic every kernel
+// must agree on, and thin inline-PTX wrappers (mbarrier, TMA, tcgen05).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ink_attn.h"
+
+namespace ink {
+
+constexpr int kHeadDim = 128;     // D
+constexpr int kKeyGroup = 16;     // keys per TMA box / per decode stage
+constexpr int kTileKeys = 128;    // keys per prefill KV tile (8 groups)
+constexpr int kTileRows = 128;    // packed (token, head) rows per prefill tile
+constexpr int kDecodeRows = 16;   // packed rows per KV head in the decode kernel
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after ~2 s
+
+// ---------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned).
+//   header | dec_items[int2] | pf_items[int4] | part_lse[f32] | part_o[f32]
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    uint32_t errors;       // INK_DEVERR_* bits
+    uint32_t dec_count;    // decode work items written by the prepass
+    uint32_t pf_count;     // prefill work items written by the prepass
+    uint32_t dec_next;     // dynamic scheduler counter of the decode kernel
+    uint32_t pf_next;      // dynamic scheduler counter of the prefill kernel
+    uint32_t pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
+
+struct Params {
+    // shapes
+    int T, B, H, Hkv, G, NB, BS, MAXBLK, max_seqlen_q;
+    // scalars
+    float softmax_scale, scale_log2, inv_scale;
+    int causal, wl, wr, E;
+    // tensors
+    const __nv_bfloat16 *q, *kc, *vc;
+    const int32_t *bt, *seqk, *cu;
+    const float *rel;
+    __nv_bfloat16 *out;
+    float *lse;
+    // workspace
+    WsHeader *hdr;
+    int2 *dec_items;
+    int dec_items_cap;
+    int4 *pf_items;
+    int pf_items_cap;
+    int *dec_off;      // (B+1) first decode item of each request (prepass)
+    int *unit_off;     // (B+1) first prefill unit (q tile) of each request (prepass)
+    // split partials: one block per decode item, and per (prefill unit, split)
+    float *part_dec_o, *part_dec_lse;  // (dec_items_cap, dec_rows, D), (dec_items_cap, dec_rows)
+    int dec_rows;                      // rows per decode block: (16 / G) * H
+    float *part_pf_o, *part_pf_lse;    // (units_cap * S_pf, Hkv * 128, D), (..., Hkv * 128)
+    int units_cap;
+    int S_pf;                          // splits per prefill unit (1: no partials)
+    // scheduling
+    int decode_kernel;   // 1: decode-shaped requests go to the decode kernel
+    int chunk_dec;       // 16-key groups per split for decode units
+    int chunk_pf;        // 16-key groups per split for prefill units
+    int tpt;             // prefill tokens per 128-row tile (128 / G)
+    int fast_pack;       // prefill: warp-strided token packing (G divides 32)
+    int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
+};
+
+// ---------------------------------------------------------------------------
+// Requests and work units.  A request is decode-shaped when its Lq*G rows fit
+// one mma row block (<= 16) and the decode kernel is enabled; such a request
+// is one unit.  Other requests are cut into q tiles of `tpt` tokens.  Each
+// unit's visible key range is cut into splits of `chunk` 16-key groups.
+// ---------------------------------------------------------------------------
+struct Req {
+    int t0, Lq, Lk;
+    bool ok;
+    uint32_t err;
+};
+
+__device__ __forceinline__ Req load_req(const Params &p, int b)
+{
+    Req r;
+    const int c0 = __ldg(p.cu + b), c1 = __ldg(p.cu + b + 1), lk = __ldg(p.seqk + b);
+    r.t0 = c0;
+    r.Lq = c1 - c0;
+    r.Lk = lk;
+    r.err = 0;
+    if (!(c0 >= 0 && c0 <= c1 && c1 <= p.T)) r.err |= INK_DEVERR_CU_SEQLENS;
+    if (r.Lq > p.max_seqlen_q) r.err |= INK_DEVERR_SEQLEN_Q;
+    if (lk < 0 || (long long)lk > (long long)p.MAXBLK * p.BS) r.err |= INK_DEVERR_SEQLEN_K;
+    r.ok = (r.err == 0);
+    return r;
+}
+
+__device__ __forceinline__ bool is_decode_req(const Params &p, const Req &r)
+{
+    return p.decode_kernel && r.Lq * p.G <= kDecodeRows;
+}
+
+// Inclusive visible key range of the rows whose q_abs lies in [qa0, qa1].
+// Both ends are non-decreasing in q_abs, so the union is [lo(qa0), hi(qa1)].
+__host__ __device__ __forceinline__ void visible_range(int qa0, int qa1, int Lk, int causal, int wl,
+                                                       int wr, int &lo, int &hi)
+{
+    lo = 0;
+    if (wl >= 0) lo = max(0, qa0 - wl);
+    hi = Lk - 1;
+    if (causal) hi = min(hi, qa1);
+    if (wr >= 0) hi = min(hi, qa1 + wr);
+}
+
+struct UnitSplit {
+    int gb, ge;    // 16-key groups [gb, ge) of this split (may be empty)
+    int nact;      // number of splits of the unit (>= 1)
+    int klo, khi;  // unit visible key range (inclusive; khi < klo when empty)
+};
+
+__host__ __device__ __forceinline__ UnitSplit unit_split(int qa0, int qa1, int Lk, int causal, int wl,
+                                                         int wr, int chunk, int s)
+{
+    UnitSplit u;
+    visible_range(qa0, qa1, Lk, causal, wl, wr, u.klo, u.khi);
+    if (u.khi < u.klo) {
+        u.nact = 1;
+        u.gb = u.ge = 0;
+        return u;
+    }
+    const int g0 = u.klo / kKeyGroup, g1 = u.khi / kKeyGroup + 1;
+    u.nact = (g1 - g0 + chunk - 1) / chunk;
+    u.gb = g0 + s * chunk;
+    u.ge = min(g1, u.gb + chunk);
+    if (u.ge < u.gb) u.ge = u.gb;
+    return u;
+}
+
+// Packed row of (token offset k, head j) inside a prefill tile, and back.
+__host__ __device__ __forceinline__ int pf_row_of(int fast_pack, int G, int k, int j)
+{
+    return fast_pack ? 32 * (k & 3) + (k >> 2) * G + j : k * G + j;
+}
+
+__device__ __forceinline__ void report(const Params &p, uint32_t bits)
+{
+    if (bits) atomicOr(&p.hdr->errors, bits);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase parity.  Returns false (and raises the timeout
+// bit, and sets *abort) when the phase did not complete within the limit or
+// another role already gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          const Params &p)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                report(p, INK_DEVERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMA tiled loads into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                                 uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 128-byte swizzle of a byte offset inside a 1024-byte aligned atom: the
+// 16-byte chunk index (bits 4-6) is XOR-ed with the row within the atom
+// (bits 7-9).  This is the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B
+// and the tensor core reads with layout type "128B swizzle".
+__device__ __forceinline__ uint32_t swz128(uint32_t off)
+{
+    return off ^ (((off >> 7) & 7u) << 4);
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Host-side launchers, one per translation unit (ink_api.cu calls these).
+cudaError_t launch_prepass(const Params &p, cudaStream_t stream);
+cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                          const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,
+                          int bias_slot_bytes, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_combine(const Params &p, int grid, cudaStream_t stream);
+
+}  // namespace ink

@@ -1,0 +1,656 @@
+// ink_prefill.cu -- prefill kernel: paged varlen causal GQA attention on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// One work item = (request, q tile, split, KV head): 128 packed rows, i.e.
+// 128/G tokens x the G query heads that share KV head g (GQA packing, a4).
+// Persistent CTAs (one per SM) walk the device-built item list, longest
+// items first.  Warp roles:
+//   warp 0      page-gather producer (a3): per 16-key group one block_table
+//               read and two TMA boxes (d halves, 128-byte swizzle) per
+//               tensor into a 3-slot K/V ring; per bias tile one fp32 TMA box
+//               of rel_logits per token (out-of-range distances read as 0);
+//   warp 1      tensor-memory allocator and single-thread MMA issuer (a5, a9):
+//               S = Q K^T (M128 N128 K16 x 8, smem x smem) into a 3-slot S ring
+//               in TMEM, O += P V with P read from TMEM (M128 N128 K16 x 8);
+//   warps 2-3   Q tile loader (coalesced 16-byte loads, manual swizzle);
+//   warps 4-7   online softmax (a8) and epilogue (a10); thread = TMEM lane = row;
+//   warps 8-11  relative bias and masks (a6, a7): for tiles that need them,
+//               write bias/scale (or -inf) into the S slot before the QK MMA
+//               accumulates onto it, so the softmax warps never touch bias.
+// Row packing is token-strided per warp so that every row of a warp has the
+// same q_abs mod 4, which makes the misalignment of its bias span (relative
+// to a 16-byte TMA box start) a warp-uniform constant.
+#include "ink_common.cuh"
+
+namespace ink {
+
+constexpr int kPfThreads = 12 * 32;
+constexpr int kKvSlots = 3;
+constexpr int kSSlots = 3;
+constexpr int kSlotBytes = 32768;           // one K or V tile: 2 d halves x 128 rows x 128 B
+constexpr int kBiasBox = 132;               // floats per bias row box (128 + 4 for alignment)
+constexpr int kRescaleThreshold = 8;        // log2 units (factor 256)
+constexpr uint32_t kTmemCols = 512;
+
+// Instruction descriptor, kind::f16: D f32, A bf16, B bf16, M 128, N 128.
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// Same with B (V) in MN-major layout.
+constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;   // descriptor version for sm_100-class tensor cores
+    d |= 2ull << 61;   // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+#define INK_TMEM_LD32(taddr, r)                                                                                  \
+    asm volatile(                                                                                                \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17," \
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                       \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),         \
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),   \
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), \
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])  \
+        : "r"(taddr))
+
+#define INK_TMEM_ST32(taddr, r)                                                                                  \
+    asm volatile(                                                                                                \
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"  \
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),                       \
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),       \
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),          \
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),         \
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                      \
+        : "memory")
+
+struct PfShared {
+    uint64_t kv_full[kKvSlots], kv_empty[kKvSlots];
+    uint64_t bias_full, bias_empty;
+    uint64_t q_full, q_empty;
+    uint64_t s_init[kSSlots], s_full[kSSlots], p_full[kSSlots], pv_done[kSSlots];
+    uint64_t o_full;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Everything a role needs to know about one work item; every role computes
+// it from the item with the same code.
+struct PfItem {
+    int b, qt, s, g;
+    int t0, Lq, Lk;
+    int i0, ntok;        // first token of the tile, valid tokens in it
+    int qa_min, qa_max;  // q_abs of the first / last valid token
+    int gb, ge, nact;    // 16-key groups of the split, splits of the unit
+    int ntiles;          // 128-key tiles (8 groups each) of the split
+    int lo_max, hi_min;  // keys visible to every valid row (inside the split)
+};
+
+__device__ __forceinline__ PfItem pf_item(const Params &p, int4 v)
+{
+    PfItem it;
+    it.b = v.x; it.qt = v.y; it.s = v.z; it.g = v.w;
+    const Req r = load_req(p, it.b);
+    it.t0 = r.t0; it.Lq = r.Lq; it.Lk = r.Lk;
+    it.i0 = it.qt * p.tpt;
+    it.ntok = min(p.tpt, it.Lq - it.i0);
+    it.qa_min = it.i0 + it.Lk - it.Lq;
+    it.qa_max = it.qa_min + it.ntok - 1;
+    const UnitSplit u = unit_split(it.qa_min, it.qa_max, it.Lk, p.causal, p.wl, p.wr, p.chunk_pf, it.s);
+    it.gb = u.gb; it.ge = u.ge; it.nact = u.nact;
+    it.ntiles = (it.ge - it.gb + 7) / 8;
+    int lo, hi, t;
+    visible_range(it.qa_max, it.qa_max, it.Lk, p.causal, p.wl, p.wr, lo, t);
+    visible_range(it.qa_min, it.qa_min, it.Lk, p.causal, p.wl, p.wr, t, hi);
+    it.lo_max = max(lo, it.gb * kKeyGroup);
+    it.hi_min = min(hi, it.ge * kKeyGroup - 1);
+    return it;
+}
+
+__device__ __forceinline__ int pf_tile_key0(const PfItem &it, int n) { return (it.gb + 8 * n) * kKeyGroup; }
+
+__device__ __forceinline__ bool pf_tile_bias(const Params &p, const PfItem &it, int n)
+{
+    const int j0 = pf_tile_key0(it, n);
+    const int rd_min = it.qa_min - (j0 + kTileKeys - 1), rd_max = it.qa_max - j0;
+    return p.E > 0 && rd_max >= 0 && rd_min < p.E;
+}
+
+__device__ __forceinline__ bool pf_tile_mask(const PfItem &it, int n)
+{
+    const int j0 = pf_tile_key0(it, n);
+    return j0 < it.lo_max || j0 + kTileKeys - 1 > it.hi_min;
+}
+
+// Row L of the tile -> (token offset k, head j); false when the row is padding.
+__device__ __forceinline__ bool pf_row(const Params &p, int L, int &k, int &j)
+{
+    if (p.fast_pack) {
+        const int q = L >> 5, l = L & 31;
+        k = 4 * (l / p.G) + q;
+        j = l % p.G;
+        return true;
+    }
+    k = L / p.G;
+    j = L % p.G;
+    return k < p.tpt;
+}
+
+__device__ __forceinline__ int pf_bias_slot_bytes(const Params &p)
+{
+    return ((p.G * kBiasBox * 4) + 127) & ~127;
+}
+
+// Item of round r for this CTA: snake order over the cost-sorted list.
+__device__ __forceinline__ int pf_item_index(int r)
+{
+    return r * gridDim.x + ((r & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x);
+}
+
+// Bias of one row for 128 keys starting at j0, read from its TMA box:
+// v[c] = box[O + 127 - c] where O = (q_abs - j0 - 127) mod 4 is a compile-time
+// constant here.  33 aligned 16-byte loads cover the 132-float box.
+template <int O>
+__device__ __forceinline__ void bias_from_box(const float *box, float (&v)[128])
+{
+    const float4 *b4 = reinterpret_cast<const float4 *>(box);
+#pragma unroll
+    for (int m = 0; m < 33; ++m) {
+        const float4 f = b4[m];
+        const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = 4 * m + u;
+            const int c = O + 127 - idx;
+            if (c >= 0 && c < 128) v[c] = e[u];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    ink_prefill_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias)
+{
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_smem = base;                                   // 32 KB
+    uint8_t *kv_smem = base + 32768;                          // 3 x 32 KB
+    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // tpt x slot
+    const int bias_slot = pf_bias_slot_bytes(p);
+    PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + p.tpt * bias_slot);
+    volatile int *abort = &sh.abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = (int)*(volatile uint32_t *)&p.hdr->pf_count;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kKvSlots; ++s) {
+            mbar_init(&sh.kv_full[s], 1);
+            mbar_init(&sh.kv_empty[s], 1);
+        }
+        mbar_init(&sh.bias_full, 1);
+        mbar_init(&sh.bias_empty, 4);
+        mbar_init(&sh.q_full, 2);
+        mbar_init(&sh.q_empty, 1);
+        for (int s = 0; s < kSSlots; ++s) {
+            mbar_init(&sh.s_init[s], 4);
+            mbar_init(&sh.s_full[s], 1);
+            mbar_init(&sh.p_full[s], 4);
+            mbar_init(&sh.pv_done[s], 1);
+        }
+        mbar_init(&sh.o_full, 1);
+        sh.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const uint32_t tmem_o = tmem + kSSlots * 128;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            if (p.bias_tma) prefetch_tmap(&tm_bias);
+        }
+        const uint64_t pol_kv = policy_evict_last();
+        const uint64_t pol_bias = policy_evict_first();
+        uint32_t seq = 0, bseq = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            const int32_t *bt_row = p.bt + (size_t)it.b * p.MAXBLK;
+            // load order: K0, then K_n, V_{n-1} for n >= 1, then V_{last}
+            for (int step = 0; step <= it.ntiles && it.ntiles > 0; ++step) {
+                for (int which = 0; which < 2; ++which) {
+                    int n, isV;
+                    if (step == 0) { if (which) break; n = 0; isV = 0; }
+                    else if (step == it.ntiles) { if (which) break; n = it.ntiles - 1; isV = 1; }
+                    else { n = which ? step - 1 : step; isV = which; }
+                    const int slot = seq % kKvSlots;
+                    if (!mbar_wait(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
+                    const int gfirst = it.gb + 8 * n;
+                    // one page id per lane (lanes 0-7), key coordinate of its 16-key group
+                    int key0 = -kKeyGroup;
+                    if (lane < 8 && gfirst + lane < it.ge) {
+                        const int gi = gfirst + lane;
+                        const int pid = __ldg(bt_row + (gi * kKeyGroup) / p.BS);
+                        if (pid >= 0 && pid < p.NB) key0 = pid * p.BS + (gi * kKeyGroup) % p.BS;
+                        else report(p, INK_DEVERR_PAGE_ID);
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
+                    __syncwarp();
+                    if (lane < 16) {
+                        const int grp = lane & 7, dh = lane >> 3;
+                        const int kc = __shfl_sync(0x0000ffffu, key0, grp);
+                        uint8_t *dst = kv_smem + slot * kSlotBytes + dh * 16384 + grp * 2048;
+                        tma_load_3d_hint(dst, isV ? &tm_v : &tm_k, dh * 64, it.g, kc, &sh.kv_full[slot], pol_kv);
+                    }
+                    __syncwarp();
+                    ++seq;
+                    // bias of tile n travels right after K_n
+                    if (!isV && p.bias_tma && pf_tile_bias(p, it, n)) {
+                        if (!mbar_wait(&sh.bias_empty, (bseq & 1) ^ 1, abort, p)) break;
+                        const int j0 = pf_tile_key0(it, n);
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&sh.bias_full, (uint32_t)it.ntok * p.G * kBiasBox * 4);
+                        __syncwarp();
+                        for (int k = lane; k < it.ntok; k += 32) {
+                            const int qa = it.qa_min + k;
+                            const int start = qa - j0 - (kTileKeys - 1);
+                            const int x0 = start >= 0 ? (start & ~3) : -(((-start) + 3) & ~3);
+                            tma_load_3d_hint(bias_smem + k * bias_slot, &tm_bias, x0, it.g * p.G, it.t0 + it.i0 + k,
+                                             &sh.bias_full, pol_bias);
+                        }
+                        __syncwarp();
+                        ++bseq;
+                    }
+                }
+                if (*abort) break;
+            }
+        }
+        // let copies still in flight land before the CTA can exit
+        if (lane == 0) {
+            for (uint32_t k = (seq > kKvSlots ? seq - kKvSlots : 0); k < seq; ++k)
+                mbar_wait(&sh.kv_full[k % kKvSlots], (k / kKvSlots) & 1, abort, p);
+            if (bseq > 0) mbar_wait(&sh.bias_full, (bseq - 1) & 1, abort, p);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        uint32_t seq = 0, tc = 0, qseq = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            if (it.ntiles == 0) continue;
+            if (!mbar_wait(&sh.q_full, qseq & 1, abort, p)) break;
+            const uint32_t qaddr = smem_u32(q_smem);
+            const uint32_t tc0 = tc;
+            auto zero_tail = [&](int slot, int n) {
+                // keys at or beyond Lk inside loaded groups may hold stale data: zero them
+                const int j0 = pf_tile_key0(it, n);
+                const int loaded = min(8, it.ge - (it.gb + 8 * n)) * kKeyGroup;
+                const int z0 = max(0, it.Lk - j0);
+                if (z0 < loaded) {
+                    uint8_t *t = kv_smem + slot * kSlotBytes;
+                    for (int c = lane; c < (loaded - z0) * 16; c += 32) {  // 16 chunks of 16 B per row
+                        const int row = z0 + c / 16, ch = c % 16;
+                        *reinterpret_cast<uint4 *>(t + (ch >> 3) * 16384 + row * 128 + (ch & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+            };
+            auto issue_pv = [&](int m) {
+                const uint32_t t = tc0 + m;
+                const int ss = t % kSSlots;
+                if (!mbar_wait(&sh.p_full[ss], (t / kSSlots) & 1, abort, p)) return false;
+                const int slot = seq % kKvSlots;
+                if (!mbar_wait(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) return false;
+                zero_tail(slot, m);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t vaddr = smem_u32(kv_smem + slot * kSlotBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = smem_desc(vaddr + kk * 2048, 16384, 1024);
+                        mma_ts(tmem_o, tmem + ss * 128 + kk * 8, bdesc, kIdescPV, (m > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&sh.kv_empty[slot]);
+                    mma_commit(&sh.pv_done[ss]);
+                }
+                __syncwarp();
+                ++seq;
+                return true;
+            };
+            bool ok = true;
+            for (int n = 0; n < it.ntiles && ok; ++n) {
+                const uint32_t t = tc0 + n;
+                const int ss = t % kSSlots;
+                const int slot = seq % kKvSlots;
+                if (!mbar_wait(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
+                const bool init = pf_tile_bias(p, it, n) || pf_tile_mask(it, n);
+                if (init && !mbar_wait(&sh.s_init[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
+                zero_tail(slot, n);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t kaddr = smem_u32(kv_smem + slot * kSlotBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint64_t adesc = smem_desc(qaddr + off, 16, 1024);
+                        const uint64_t bdesc = smem_desc(kaddr + off, 16, 1024);
+                        mma_ss(tmem + ss * 128, adesc, bdesc, kIdescQK, (init || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&sh.s_full[ss]);
+                    mma_commit(&sh.kv_empty[slot]);
+                    if (n == it.ntiles - 1) mma_commit(&sh.q_empty);
+                }
+                __syncwarp();
+                ++seq;
+                if (n >= 1) ok = issue_pv(n - 1);
+            }
+            if (ok) ok = issue_pv(it.ntiles - 1);
+            if (ok && lane == 0) mma_commit(&sh.o_full);
+            __syncwarp();
+            tc += it.ntiles;
+            ++qseq;
+            if (!ok) break;
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- Q loader
+        const int t = threadIdx.x - 64;  // 0..63
+        uint32_t qseq = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            if (it.ntiles == 0) continue;
+            if (!mbar_wait(&sh.q_empty, (qseq & 1) ^ 1, abort, p)) break;
+            for (int c = t; c < kTileRows * 16; c += 64) {
+                const int L = c >> 4, ch = c & 15;
+                int k, j;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (pf_row(p, L, k, j) && k < it.ntok) {
+                    const __nv_bfloat16 *src =
+                        p.q + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * kHeadDim + ch * 8;
+                    v = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+                *reinterpret_cast<uint4 *>(q_smem + (ch >> 3) * 16384 + swz128(L * 128 + (ch & 7) * 16)) = v;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_full);
+            ++qseq;
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int L = (warp - 4) * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
+        const float sl2 = p.scale_log2;
+        const float ln2 = 0.6931471805599453f;
+        uint32_t tc = 0, oseq = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            int k, j;
+            const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
+            float m_used = -INFINITY;  // raw-score units
+            float l = 0.f;
+            bool ok = true;
+            for (int n = 0; n < it.ntiles; ++n) {
+                const uint32_t t = tc + n;
+                const int ss = t % kSSlots;
+                if (!mbar_wait(&sh.s_full[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sv[128];
+                const uint32_t sa = tmem + lane_addr + ss * 128;
+                INK_TMEM_LD32(sa + 0, (sv + 0));
+                INK_TMEM_LD32(sa + 32, (sv + 32));
+                INK_TMEM_LD32(sa + 64, (sv + 64));
+                INK_TMEM_LD32(sa + 96, (sv + 96));
+                tc_wait_ld();
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * sl2 > (float)kRescaleThreshold)) {
+                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2((m_used - mx) * sl2);
+                    l *= alpha;
+                    if (n > 0 && m_used != -INFINITY) {
+                        // O holds tiles 0..n-1 once PV(n-1) is done: rescale it in place
+                        const uint32_t tp = t - 1;
+                        if (!mbar_wait(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            uint32_t ov[32];
+                            INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            INK_TMEM_ST32(tmem_o + lane_addr + cc * 32, ov);
+                        }
+                    }
+                    m_used = mx;
+                }
+                const float moff = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -moff));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -moff));
+                    l += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                INK_TMEM_ST32(sa + 0, (pk + 0));
+                INK_TMEM_ST32(sa + 32, (pk + 32));
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.p_full[ss]);
+            }
+            if (!ok) break;
+            // epilogue
+            if (it.ntiles > 0) {
+                if (!mbar_wait(&sh.o_full, oseq & 1, abort, p)) break;
+                ++oseq;
+                tc_fence_after();
+            }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lse = l > 0.f ? (m_used * sl2 + __log2f(l)) * ln2 : -INFINITY;
+            const size_t row = (size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j;
+            const bool final_out = it.nact == 1;
+            // partial block of (unit, split): rows g * 128 + L
+            size_t prow = 0;
+            if (!final_out)
+                prow = ((size_t)(__ldg(p.unit_off + it.b) + it.qt) * p.S_pf + it.s) * ((size_t)p.Hkv * kTileRows) +
+                       (size_t)it.g * kTileRows + L;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t ov[32];
+                if (it.ntiles > 0) {
+                    INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                }
+                if (row_ok) {
+                    if (final_out) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim + cc * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+                            dst[q4] = w;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(p.part_pf_o + prow * kHeadDim + cc * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(ov[4 * q4]) * inv, __uint_as_float(ov[4 * q4 + 1]) * inv,
+                                                  __uint_as_float(ov[4 * q4 + 2]) * inv, __uint_as_float(ov[4 * q4 + 3]) * inv);
+                    }
+                }
+            }
+            if (row_ok) {
+                if (final_out) {
+                    if (p.lse) p.lse[row] = lse;
+                } else {
+                    p.part_pf_lse[prow] = lse;
+                }
+            }
+            tc_fence_before();
+            tc += it.ntiles;
+        }
+    } else {
+        // ---------------------------------------------------------------- bias + masks
+        const int L = (warp - 8) * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)((warp - 8) * 32) << 16;
+        const float inv_scale = p.inv_scale;
+        uint32_t tc = 0, bseq = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            int k, j;
+            const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
+            const int qa = it.qa_min + k;
+            int lo = 1, hi = 0;
+            if (row_ok) {
+                visible_range(qa, qa, it.Lk, p.causal, p.wl, p.wr, lo, hi);
+                lo = max(lo, it.gb * kKeyGroup);
+                hi = min(hi, it.ge * kKeyGroup - 1);
+            }
+            const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
+            bool ok = true;
+            for (int n = 0; n < it.ntiles; ++n) {
+                const uint32_t t = tc + n;
+                const int ss = t % kSSlots;
+                const bool has_bias = pf_tile_bias(p, it, n);
+                const bool has_mask = pf_tile_mask(it, n);
+                if (!has_bias && !has_mask) continue;
+                const int j0 = pf_tile_key0(it, n);
+                float v[128];
+#pragma unroll
+                for (int c = 0; c < 128; ++c) v[c] = 0.f;
+                if (has_bias) {
+                    if (p.bias_tma) {
+                        if (!mbar_wait(&sh.bias_full, bseq & 1, abort, p)) { ok = false; break; }
+                        if (row_ok) {
+                            const float *box = reinterpret_cast<const float *>(bias_smem + k * bias_slot) + j * kBiasBox;
+                            const int o = (qa - j0 - (kTileKeys - 1)) & 3;
+                            switch (o) {
+                                case 0: bias_from_box<0>(box, v); break;
+                                case 1: bias_from_box<1>(box, v); break;
+                                case 2: bias_from_box<2>(box, v); break;
+                                default: bias_from_box<3>(box, v); break;
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.bias_empty);
+                        ++bseq;
+                    } else if (row_ok) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) {
+                            const int rd = qa - (j0 + c);
+                            v[c] = (rd >= 0 && rd < p.E) ? __ldg(rel_row + rd) : 0.f;
+                        }
+                    }
+                }
+                // the S slot is free once the PV of the tile that used it before is done
+                if (t >= kSSlots) {
+                    const uint32_t tp = t - kSSlots;
+                    if (!mbar_wait(&sh.pv_done[ss], (tp / kSSlots) & 1, abort, p)) { ok = false; break; }
+                }
+                uint32_t w[128];
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = j0 + c;
+                    const bool vis = key >= lo && key <= hi;
+                    w[c] = __float_as_uint(vis ? v[c] * inv_scale : -INFINITY);
+                }
+                tc_fence_after();
+                const uint32_t sa = tmem + lane_addr + ss * 128;
+                INK_TMEM_ST32(sa + 0, (w + 0));
+                INK_TMEM_ST32(sa + 32, (w + 32));
+                INK_TMEM_ST32(sa + 64, (w + 64));
+                INK_TMEM_ST32(sa + 96, (w + 96));
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.s_init[ss]);
+            }
+            if (!ok) break;
+            tc += it.ntiles;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(ink_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ink_prefill_kernel<<<grid, kPfThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias);
+    return cudaGetLastError();
+}
+
+}  // namespace ink

@@ -1,0 +1,201 @@
+// ink_prepass.cu -- device-side plan of one call (a1/a2: validation and work
+// decomposition), so that the host never has to read cu_seqlens_q or
+// cache_seqlens and the whole call stays free of host synchronisation.
+//
+// One CTA of 1024 threads:
+//   1. clears the workspace header (error word, counters);
+//   2. validates every request and classifies it as decode-shaped (one unit)
+//      or prefill-shaped (q tiles of `tpt` tokens);
+//   3. writes the decode work items (request, split) in request order;
+//   4. writes the prefill work items (request, q tile, split, KV head) sorted
+//      by decreasing number of 128-key tiles (a counting sort), so that the
+//      persistent prefill kernel hands out the longest items first.
+#include "ink_common.cuh"
+
+namespace ink {
+
+constexpr int kPrepassThreads = 1024;
+constexpr int kCostBuckets = 1024;
+
+// Exclusive block-wide scan of one int per thread; returns the block total.
+__device__ int block_exclusive_scan(int v, int *out, int *warp_sums)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int total = warp_sums[31];
+    *out = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ void pf_unit_of(const Params &p, const Req &r, int qt, int &qa0, int &qa1)
+{
+    const int i0 = qt * p.tpt, i1 = min(r.Lq, i0 + p.tpt) - 1;
+    qa0 = i0 + r.Lk - r.Lq;
+    qa1 = i1 + r.Lk - r.Lq;
+}
+
+// Cost of a prefill split in 128-key tiles, clamped to the bucket range.
+__device__ __forceinline__ int pf_cost_bucket(const UnitSplit &u)
+{
+    const int groups = u.ge - u.gb;
+    const int tiles = (groups + 7) / 8;
+    return min(tiles, kCostBuckets - 1);
+}
+
+__global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params p)
+{
+    __shared__ int warp_sums[32];
+    __shared__ int bucket_count[kCostBuckets];
+    __shared__ int bucket_base[kCostBuckets];
+    __shared__ int s_carry[2];
+    __shared__ uint32_t s_err;
+
+    int *dec_off = p.dec_off;
+    int *unit_off = p.unit_off;
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        p.hdr->errors = 0;
+        p.hdr->dec_count = 0;
+        p.hdr->pf_count = 0;
+        p.hdr->dec_next = 0;
+        p.hdr->pf_next = 0;
+        s_carry[0] = s_carry[1] = 0;
+        uint32_t e = 0;
+        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.B) != p.T) e |= INK_DEVERR_CU_SEQLENS;
+        s_err = e;
+    }
+    for (int i = tid; i < kCostBuckets; i += blockDim.x) bucket_count[i] = 0;
+    __syncthreads();
+
+    // pass 1: per request, decode split count and prefill q-tile count; scans.
+    uint32_t my_err = 0;
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        const int b = base + tid;
+        int ndec = 0, nq = 0;
+        if (b < p.B) {
+            Req r = load_req(p, b);
+            my_err |= r.err;
+            if (r.ok && r.Lq > 0) {
+                if (is_decode_req(p, r)) {
+                    UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
+                    ndec = u.nact;
+                } else {
+                    nq = (r.Lq + p.tpt - 1) / p.tpt;
+                }
+                if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
+            }
+        }
+        int xd, xq;
+        const int td = block_exclusive_scan(ndec, &xd, warp_sums);
+        const int tq = block_exclusive_scan(nq, &xq, warp_sums);
+        if (b < p.B) {
+            dec_off[b] = s_carry[0] + xd;
+            unit_off[b] = s_carry[1] + xq;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            s_carry[0] += td;
+            s_carry[1] += tq;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        dec_off[p.B] = s_carry[0];
+        unit_off[p.B] = s_carry[1];
+    }
+    if (my_err) atomicOr(&s_err, my_err);
+    __syncthreads();
+    __threadfence_block();
+
+    const int n_dec = min(s_carry[0], p.dec_items_cap);
+    const int n_units = s_carry[1];
+
+    // pass 2: decode items (request, split), request order.
+    for (int b = tid; b < p.B; b += blockDim.x) {
+        const int o0 = dec_off[b], o1 = dec_off[b + 1];
+        for (int s = 0; o0 + s < o1 && o0 + s < n_dec; ++s) p.dec_items[o0 + s] = make_int2(b, s);
+    }
+
+    // pass 3: prefill units -> cost histogram of their splits.
+    for (int u = tid; u < n_units; u += blockDim.x) {
+        int lo = 0, hi = p.B - 1;  // request owning unit u: last b with unit_off[b] <= u
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (unit_off[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo, qt = u - unit_off[b];
+        Req r = load_req(p, b);
+        int qa0, qa1;
+        pf_unit_of(p, r, qt, qa0, qa1);
+        UnitSplit u0 = unit_split(qa0, qa1, r.Lk, p.causal, p.wl, p.wr, p.chunk_pf, 0);
+        for (int s = 0; s < u0.nact; ++s) {
+            UnitSplit us = unit_split(qa0, qa1, r.Lk, p.causal, p.wl, p.wr, p.chunk_pf, s);
+            atomicAdd(&bucket_count[pf_cost_bucket(us)], p.Hkv);
+        }
+    }
+    __syncthreads();
+    // descending-cost bucket bases: bucket k starts after every bucket > k
+    {
+        int x = 0;
+        const int k = kCostBuckets - 1 - tid;  // tid 0 -> highest cost
+        const int c = (k >= 0) ? bucket_count[k] : 0;
+        const int total = block_exclusive_scan(c, &x, warp_sums);
+        if (k >= 0) bucket_base[k] = x;
+        if (tid == 0) {
+            p.hdr->pf_count = (uint32_t)min(total, p.pf_items_cap);
+            p.hdr->dec_count = (uint32_t)n_dec;
+        }
+    }
+    for (int i = tid; i < kCostBuckets; i += blockDim.x) bucket_count[i] = 0;  // reused as cursors
+    __syncthreads();
+    // pass 4: scatter the prefill items, KV heads of one split side by side
+    const int cap = p.pf_items_cap;
+    for (int u = tid; u < n_units; u += blockDim.x) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (unit_off[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo, qt = u - unit_off[b];
+        Req r = load_req(p, b);
+        int qa0, qa1;
+        pf_unit_of(p, r, qt, qa0, qa1);
+        UnitSplit u0 = unit_split(qa0, qa1, r.Lk, p.causal, p.wl, p.wr, p.chunk_pf, 0);
+        for (int s = 0; s < u0.nact; ++s) {
+            UnitSplit us = unit_split(qa0, qa1, r.Lk, p.causal, p.wl, p.wr, p.chunk_pf, s);
+            const int c = pf_cost_bucket(us);
+            const int pos = bucket_base[c] + atomicAdd(&bucket_count[c], p.Hkv);
+            for (int g = 0; g < p.Hkv; ++g)
+                if (pos + g < cap) p.pf_items[pos + g] = make_int4(b, qt, s, g);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) atomicOr(&p.hdr->errors, s_err);
+}
+
+cudaError_t launch_prepass(const Params &p, cudaStream_t stream)
+{
+    ink_prepass_kernel<<<1, kPrepassThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ink
