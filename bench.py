@@ -287,10 +287,14 @@ def run_ours(args, rank, world, local_rank):
         return res
 
     steps, warmup = args.steps, args.warmup
-    head = measure(HEADLINE, steps, warmup, "decode")
+    headline = args.workload
+    head_kernel = "prefill" if headline == "chunked_prefill" else "decode"
+    head = measure(headline, steps, warmup, head_kernel)
     sec = {}
     if not args.headline_only:
-        for name in SECONDARY:
+        for name in [HEADLINE] + SECONDARY:
+            if name == headline:
+                continue
             kern = "prefill" if name == "chunked_prefill" else "decode"
             sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
 
@@ -309,8 +313,16 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    value = world * head["kv_bytes"] / (head["ms_per_step"] * 1e-3) / 1e9
-    e2e = world * head["kv_bytes"] / (head["e2e_ms"] * 1e-3) / 1e9
+    if headline == "chunked_prefill":
+        unit = "TFLOP/s"
+        value = world * head["flops"] / (head["ms_per_step"] * 1e-3) / 1e12
+        e2e = world * head["flops"] / (head["e2e_ms"] * 1e-3) / 1e12
+        roof = roof_prefill(head, headline)
+    else:
+        unit = "GB/s"
+        value = world * head["kv_bytes"] / (head["ms_per_step"] * 1e-3) / 1e9
+        e2e = world * head["kv_bytes"] / (head["e2e_ms"] * 1e-3) / 1e9
+        roof = roof_decode(head, headline)
     workloads_out = {}
     for name, r in sec.items():
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
@@ -332,15 +344,15 @@ def run_ours(args, rank, world, local_rank):
         workloads_out[name] = entry
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(HEADLINE, args.cpu_seconds)
+        cpu = cpu_baseline(headline, args.cpu_seconds)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(head["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads/)",
-        "config": {"workload": HEADLINE, "desc": WORKLOADS[HEADLINE], "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV cache 4.4 GB), no flush"},
-        "roofline": roof_decode(head, HEADLINE),
-        "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": head["h2d_bytes"],
+        "config": {"workload": headline, "desc": WORKLOADS[headline], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": head["h2d_bytes"],
                 "d2h_bytes_per_step": head["d2h_bytes"], "ms_per_step": round(head["e2e_ms"], 4),
                 "note": "q, rel_logits and metadata copied from pinned host memory and out/lse read back "
                         "every step; the paged KV cache is resident state in HBM"},
@@ -399,7 +411,11 @@ def cpu_baseline(name, seconds):
                     break
     except Exception:
         pass
-    return {"value": round(done_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    if name == "chunked_prefill":
+        value, unit = done_flops / dt / 1e12, "TFLOP/s"
+    else:
+        value, unit = done_bytes / dt / 1e9, "GB/s"
+    return {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
             "sample": f"{reqs} of {case.B} requests of {name} (all heads), {dt:.1f} s",
             "seconds": round(dt, 2), "cpu": cpu_name}
 
@@ -412,20 +428,20 @@ def run_reference(args, rank, world):
     times = []
     val = None
     for k in range(args.warmup + args.steps):
-        r = cpu_baseline(HEADLINE, args.cpu_seconds / max(1, args.steps))
+        r = cpu_baseline(args.workload, args.cpu_seconds / max(1, args.steps))
         if k >= args.warmup:
             times.append(r)
     vals = [r["value"] for r in times]
     val = statistics.median(vals)
     last = times[-1]
     line = {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": val, "unit": last["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads/)",
-        "config": {"workload": HEADLINE, "desc": WORKLOADS[HEADLINE], "parallelism": "host cores"},
-        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+        "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "parallelism": "host cores"},
+        "cpu_baseline": {"value": val, "unit": last["unit"], "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
-        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": val, "unit": last["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -438,6 +454,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

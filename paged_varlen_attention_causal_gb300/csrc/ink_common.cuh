@@ -18,6 +18,7 @@ constexpr int kTileKeys = 128;    // keys per prefill KV tile (8 groups)
 constexpr int kTileRows = 128;    // packed (token, head) rows per prefill tile
 constexpr int kDecodeRows = 16;   // packed rows per KV head in the decode kernel
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after ~2 s
+constexpr uint32_t kWaitHintNs = 100000;           // longest single suspension of a wait (100 us)
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned).
@@ -197,23 +198,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait whose suspension is bounded by a hint (ns), so that a caller can
+// look at the clock between attempts.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on a phase parity.  Returns false (and raises the timeout
 // bit, and sets *abort) when the phase did not complete within the limit or
-// another role already gave up.
+// another role already gave up.  The clock is checked after every bounded
+// suspension, so a stuck pipeline ends within about kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           const Params &p)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                report(p, INK_DEVERR_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report(p, INK_DEVERR_TIMEOUT);
+            *abort = 1;
+            return false;
         }
     }
 }

@@ -160,26 +160,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const int stage = n % nstages;
                 if (!mbar_wait(&sh.empty[stage], ((n / nstages) & 1) ^ 1, abort, p)) break;
                 const bool band = p.bias_tma && group_in_band(qa0, qa1, gi, p.E);
+                uint8_t *st = ring + (size_t)stage * stage_bytes;
                 if (lane == 0) {
-                    uint8_t *st = ring + (size_t)stage * stage_bytes;
                     const uint32_t bytes = 2u * kv_bytes + (band ? (uint32_t)it.Lq * H * 20 * 4 : 0u);
                     mbar_arrive_expect_tx(&sh.full[stage], bytes);
-                    // invalid page: an out-of-range key coordinate makes TMA fill zeros
-                    const int key0 = page >= 0 ? page * p.BS + (gi * kKeyGroup) % p.BS : -kKeyGroup;
-                    for (int g = 0; g < Hkv; ++g) {
-                        for (int dh = 0; dh < 2; ++dh) {
-                            const int off = (g * 2 + dh) * 2048;
-                            tma_load_3d_hint(st + off, &tm_k, dh * 64, g, key0, &sh.full[stage], pol_kv);
-                            tma_load_3d_hint(st + kv_bytes + off, &tm_v, dh * 64, g, key0, &sh.full[stage], pol_kv);
-                        }
-                    }
-                    if (band) {
-                        for (int i = 0; i < it.Lq; ++i) {
-                            const int qa = qa0 + i;
-                            const int x0 = floor4(qa - (gi * kKeyGroup + kKeyGroup - 1));
-                            tma_load_3d(st + 2 * kv_bytes + i * bias_slot_bytes, &tm_bias, x0, 0, it.t0 + i,
-                                        &sh.full[stage]);
-                        }
+                }
+                __syncwarp();
+                // invalid page: an out-of-range key coordinate makes TMA fill zeros
+                const int key0 = page >= 0 ? page * p.BS + (gi * kKeyGroup) % p.BS : -kKeyGroup;
+                if (lane < 4 * Hkv) {  // one box per lane: (tensor, KV head, d half)
+                    const int isv = lane / (2 * Hkv), g = (lane >> 1) % Hkv, dh = lane & 1;
+                    const int off = (g * 2 + dh) * 2048 + isv * kv_bytes;
+                    tma_load_3d_hint(st + off, isv ? &tm_v : &tm_k, dh * 64, g, key0, &sh.full[stage], pol_kv);
+                }
+                if (band) {
+                    for (int i = lane; i < it.Lq; i += 32) {
+                        const int qa = qa0 + i;
+                        const int x0 = floor4(qa - (gi * kKeyGroup + kKeyGroup - 1));
+                        tma_load_3d(st + 2 * kv_bytes + i * bias_slot_bytes, &tm_bias, x0, 0, it.t0 + i,
+                                    &sh.full[stage]);
                     }
                 }
                 __syncwarp();

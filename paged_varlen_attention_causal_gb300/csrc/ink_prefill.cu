@@ -323,6 +323,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         uint32_t seq = 0, tc = 0, qseq = 0;
+        uint32_t init_cnt[kSSlots] = {0, 0, 0};  // s_init phases seen per S slot (only tiles with bias/masks)
         for (int r = 0;; ++r) {
             const int idx = pf_item_index(r);
             if (idx >= total || *abort) break;
@@ -376,7 +377,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int slot = seq % kKvSlots;
                 if (!mbar_wait(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
                 const bool init = pf_tile_bias(p, it, n) || pf_tile_mask(it, n);
-                if (init && !mbar_wait(&sh.s_init[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
+                if (init) {
+                    if (!mbar_wait(&sh.s_init[ss], init_cnt[ss] & 1, abort, p)) { ok = false; break; }
+                    ++init_cnt[ss];
+                }
                 zero_tail(slot, n);
                 tc_fence_after();
                 if (lane == 0) {

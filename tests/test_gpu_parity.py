@@ -134,6 +134,18 @@ def test_multi_token_decode(lq):
     parity(case, f"lq={lq}")
 
 
+@pytest.mark.parametrize("E,window", [(256, (-1, -1)), (0, (-1, -1)), (64, (700, 0)), (4096, (-1, -1))])
+def test_multi_item_prefill(E, window):
+    """Several work items per CTA and interior tiles that need neither bias nor masks."""
+    case = build_case(f"multi{E}", [3000, 1, 700], [9000, 5000, 700], H=8, Hkv=2, E=E, seed=31, device="cuda",
+                      window=window)
+    out, lse = gpu_run(case)
+    assert errors_of_last_call() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+    rows = sampled_rows(case, 600, 3)
+    ref_out, ref_lse = oracle_run(case, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what=f"multi-item E={E} window={window}")
+
+
 # --- edge cases -------------------------------------------------------------------------
 
 def test_empty_requests_and_empty_rows():
