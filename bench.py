@@ -190,14 +190,34 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of `x` over all ranks (the step time the job is charged); identity without a group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes the same work; value = all ranks' units / slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
     import torch
 
     import paged_varlen_attention_causal_gb300 as ink
-    from workloads import WORKLOADS, workload
+    from workloads import PROFILE_WORKLOADS, WORKLOADS, workload
 
+    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     ink.build()
@@ -232,6 +252,9 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError(f"{name}: device error flags {flags:#x}")
         kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for a, b in kev:  # torch creates the CUDA events on first record; the library needs real handles
+            a.record(stream)
+            b.record(stream)
         n0 = ink.launch_count()
         barrier()
         torch.cuda.synchronize(dev)
@@ -247,10 +270,7 @@ def run_ours(args, rank, world, local_rank):
         launches = ink.launch_count() - n0
         ms = start.elapsed_time(end) / steps
         kms = sum(a.elapsed_time(b) for a, b in kev) / steps
-        t = torch.tensor([ms], device=dev)
-        if dist is not None:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+        ms_max = max_over_ranks(ms, dev)
         kv, flops, pairs = work_of(case)
         res = {"workload": name, "desc": WORKLOADS[name], "ms_per_step": ms_max, "kernel_ms": kms,
                "kv_bytes": kv, "flops": flops, "launches": launches, "clocks": clk.summary()}
@@ -276,10 +296,7 @@ def run_ours(args, rank, world, local_rank):
             host_lse.copy_(lse, non_blocking=True)
             torch.cuda.synchronize(dev)
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
-        te = torch.tensor([e2e_ms], device=dev)
-        if dist is not None:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        res["e2e_ms"] = float(te.item())
+        res["e2e_ms"] = max_over_ranks(e2e_ms, dev)
         res["h2d_bytes"] = h2d
         res["d2h_bytes"] = d2h
         del case, out, lse, pin
@@ -288,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
 
     steps, warmup = args.steps, args.warmup
     headline = args.workload
-    head_kernel = "prefill" if headline == "chunked_prefill" else "decode"
+    head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
     head = measure(headline, steps, warmup, head_kernel)
     sec = {}
     if not args.headline_only:
@@ -296,7 +313,10 @@ def run_ours(args, rank, world, local_rank):
             if name == headline:
                 continue
             kern = "prefill" if name == "chunked_prefill" else "decode"
-            sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
+            try:
+                sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
+            except Exception as exc:  # report, keep the headline line
+                sec[name] = {"error": f"{type(exc).__name__}: {exc}"}
 
     def roof_decode(r, name):
         bytes_ = r["kv_bytes"]
@@ -313,18 +333,21 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    if headline == "chunked_prefill":
+    if headline.startswith("chunked_prefill"):
         unit = "TFLOP/s"
-        value = world * head["flops"] / (head["ms_per_step"] * 1e-3) / 1e12
-        e2e = world * head["flops"] / (head["e2e_ms"] * 1e-3) / 1e12
+        value = job_throughput(head["flops"], world, head["ms_per_step"]) / 1e12
+        e2e = job_throughput(head["flops"], world, head["e2e_ms"]) / 1e12
         roof = roof_prefill(head, headline)
     else:
         unit = "GB/s"
-        value = world * head["kv_bytes"] / (head["ms_per_step"] * 1e-3) / 1e9
-        e2e = world * head["kv_bytes"] / (head["e2e_ms"] * 1e-3) / 1e9
+        value = job_throughput(head["kv_bytes"], world, head["ms_per_step"]) / 1e9
+        e2e = job_throughput(head["kv_bytes"], world, head["e2e_ms"]) / 1e9
         roof = roof_decode(head, headline)
     workloads_out = {}
     for name, r in sec.items():
+        if "error" in r:
+            workloads_out[name] = r
+            continue
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
                  "gpu_launches": r["launches"], "clocks": r["clocks"]}
         if name == "chunked_prefill":
@@ -411,7 +434,7 @@ def cpu_baseline(name, seconds):
                     break
     except Exception:
         pass
-    if name == "chunked_prefill":
+    if name.startswith("chunked_prefill"):
         value, unit = done_flops / dt / 1e12, "TFLOP/s"
     else:
         value, unit = done_bytes / dt / 1e9, "GB/s"
@@ -423,8 +446,9 @@ def cpu_baseline(name, seconds):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    from workloads import WORKLOADS, workload  # noqa: F401
+    from workloads import PROFILE_WORKLOADS, WORKLOADS  # noqa: F401
 
+    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
     times = []
     val = None
     for k in range(args.warmup + args.steps):
@@ -455,7 +479,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch"])
+                    choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch",
+                             "decode_batch_quarter", "chunked_prefill_quarter"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -29,3 +29,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_runtest_logreport(report):
+    """With INK_TEST_LOG set, append every test's outcome and duration to that file as it finishes."""
+    path = os.environ.get("INK_TEST_LOG")
+    if not path or report.when != "call" and not (report.when == "setup" and report.outcome != "passed"):
+        return
+    with open(path, "a") as f:
+        f.write(f"{report.outcome:8s} {report.duration:8.2f}s {report.nodeid}\n")
+        if report.outcome == "failed":
+            f.write(str(report.longrepr)[-3000:] + "\n")

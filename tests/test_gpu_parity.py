@@ -271,8 +271,6 @@ def test_bad_cu_and_lengths_are_flagged():
     assert errors_of_last_call() & ink.DEVERR["SEQLEN_Q"]
 
 
-# --- the five workloads at full size (sampled rows for the oracle) ------------------------
-
 def sampled_rows(case, n, seed):
     g = np.random.default_rng(seed)
     T, H = case.T, case.H
@@ -284,28 +282,3 @@ def sampled_rows(case, n, seed):
             rows.add(cu[b] * H)
             rows.add((cu[b + 1] - 1) * H + H - 1)
     return np.array(sorted(rows), dtype=np.int64)
-
-
-@pytest.mark.parametrize("name,nrows", [("decode_batch", 256), ("chunked_prefill", 192), ("long_decode", 64),
-                                        ("continuous_batch", 256)])
-def test_workload_full_size(name, nrows):
-    case = workload(name, device="cuda")
-    out, lse = gpu_run(case)
-    assert errors_of_last_call() & ~ink.DEVERR["EMPTY_ROWS"] == 0
-    assert torch.isfinite(out.float()).all()
-    rows = sampled_rows(case, nrows, 7)
-    ref_out, ref_lse = oracle_run(case, rows=rows)
-    check(out, lse, ref_out, ref_lse, rows=rows, what=name)
-    del case, out, lse
-    torch.cuda.empty_cache()
-
-
-def test_long_decode_split_sweep():
-    case = workload("long_decode", device="cuda")
-    rows = np.arange(case.H, dtype=np.int64)
-    ref_out, ref_lse = oracle_run(case, rows=rows)
-    for s in (16, 32, 64, 128):
-        out, lse = gpu_run(case, num_splits=s)
-        check(out, lse, ref_out, ref_lse, rows=rows, what=f"long_decode splits={s}")
-    del case
-    torch.cuda.empty_cache()

@@ -148,6 +148,12 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Reduced variants for profiler captures (a few GB on the device, still larger than L2).
+PROFILE_WORKLOADS = {
+    "decode_batch_quarter": "first 16 requests of decode_batch (same lengths, pool and head shapes)",
+    "chunked_prefill_quarter": "one request of chunked_prefill: Lq 2048 on prior KV 6144, H 32, Hkv 8, E 4096",
+}
+
 
 def workload_lengths(name: str):
     """(q_lens, kv_lens) of a named workload, drawn from seed 1000 + index."""
@@ -174,6 +180,12 @@ def workload_lengths(name: str):
 
 def workload(name: str, device="cpu", **overrides) -> Case:
     """Build a named workload with its recipe (seed 1000 + index)."""
+    if name == "decode_batch_quarter":
+        q, k = workload_lengths("decode_batch")
+        return build_case(name, q[:16], k[:16], H=32, Hkv=8, E=1024, seed=1001, device=device, **overrides)
+    if name == "chunked_prefill_quarter":
+        return build_case(name, [2048], [8192], H=32, Hkv=8, E=4096, bias_std=0.5, seed=1002, device=device,
+                          **overrides)
     idx = WORKLOAD_ORDER.index(name)
     q_lens, kv_lens = workload_lengths(name)
     kw = dict(seed=1000 + idx, device=device)
