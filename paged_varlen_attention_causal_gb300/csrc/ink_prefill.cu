@@ -108,6 +108,9 @@ struct PfShared {
     uint64_t o_full;
     uint32_t tmem_base;
     int abort;
+    // Tiles (CTA-wide sequence numbers) whose PV product has completed: published by the
+    // softmax warpgroup, which observes every tile's pv_done phase in order.
+    uint32_t pv_seen;
 };
 
 // Everything a role needs to know about one work item; every role computes
@@ -156,6 +159,28 @@ __device__ __forceinline__ bool pf_tile_mask(const PfItem &it, int n)
 {
     const int j0 = pf_tile_key0(it, n);
     return j0 < it.lo_max || j0 + kTileKeys - 1 > it.hi_min;
+}
+
+// Bounded wait until a shared counter written with release semantics reaches `target`.
+__device__ __forceinline__ bool wait_counter(uint32_t *ctr, uint32_t target, volatile int *abort, const Params &p)
+{
+    auto load = [&]() {
+        uint32_t v;
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ctr)) : "memory");
+        return v;
+    };
+    if ((int32_t)(load() - target) >= 0) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if ((int32_t)(load() - target) >= 0) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report(p, INK_DEVERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
 }
 
 // Row L of the tile -> (token offset k, head j); false when the row is padding.
@@ -236,6 +261,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         mbar_init(&sh.o_full, 1);
         sh.abort = 0;
+        sh.pv_seen = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -461,16 +487,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 INK_TMEM_LD32(sa + 64, (sv + 64));
                 INK_TMEM_LD32(sa + 96, (sv + 96));
                 tc_wait_ld();
-                float mx = -INFINITY;
+                // row maximum: eight independent chains, then a tree (max is exact in any order)
+                float mxs[8];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                for (int e = 0; e < 8; ++e) mxs[e] = __uint_as_float(sv[e]);
+#pragma unroll
+                for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mxs[e] = fmaxf(mxs[e], __uint_as_float(sv[c + e]));
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                       fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+                // The PV of the previous tile (CTA-wide) is observed exactly once per tile, here or below.
+                bool pv_prev_seen = (t == 0);
+                auto see_prev_pv = [&]() {
+                    if (pv_prev_seen) return true;
+                    const uint32_t tp = t - 1;
+                    if (!mbar_wait(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) return false;
+                    pv_prev_seen = true;
+                    return true;
+                };
                 if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * sl2 > (float)kRescaleThreshold)) {
                     const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2((m_used - mx) * sl2);
                     l *= alpha;
                     if (n > 0 && m_used != -INFINITY) {
                         // O holds tiles 0..n-1 once PV(n-1) is done: rescale it in place
-                        const uint32_t tp = t - 1;
-                        if (!mbar_wait(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) { ok = false; break; }
+                        if (!see_prev_pv()) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
@@ -486,19 +528,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 const float moff = (m_used == -INFINITY) ? 0.f : m_used * sl2;
                 uint32_t pk[64];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -moff));
                     const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -moff));
-                    l += p0 + p1;
+                    ls[c & 3] += p0 + p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 INK_TMEM_ST32(sa + 0, (pk + 0));
                 INK_TMEM_ST32(sa + 32, (pk + 32));
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.p_full[ss]);
+                // keep in step with the PV completions and publish them for the bias warpgroup
+                if (!see_prev_pv()) { ok = false; break; }
+                if (warp == 4 && lane == 0 && t > 0) {
+                    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&sh.pv_seen)), "r"(t)
+                                 : "memory");
+                }
             }
             if (!ok) break;
             // epilogue
@@ -612,11 +662,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         }
                     }
                 }
-                // the S slot is free once the PV of the tile that used it before is done
-                if (t >= kSSlots) {
-                    const uint32_t tp = t - kSSlots;
-                    if (!mbar_wait(&sh.pv_done[ss], (tp / kSSlots) & 1, abort, p)) { ok = false; break; }
-                }
+                // the S slot is free once the PV of the tile that used it before (t - 3) is done,
+                // i.e. once PV completions through tile t - 3 have been published (pv_seen >= t - 2)
+                if (t >= kSSlots && !wait_counter(&sh.pv_seen, t - kSSlots + 1, abort, p)) { ok = false; break; }
                 uint32_t w[128];
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
