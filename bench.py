@@ -309,8 +309,9 @@ def run_ours(args, rank, world, local_rank):
     head = measure(headline, steps, warmup, head_kernel)
     sec = {}
     if not args.headline_only:
+        skip = {x for x in args.skip.split(",") if x}
         for name in [HEADLINE] + SECONDARY:
-            if name == headline:
+            if name == headline or name in skip:
                 continue
             kern = "prefill" if name == "chunked_prefill" else "decode"
             try:
@@ -482,6 +483,7 @@ def main():
                     choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch",
                              "decode_batch_quarter", "chunked_prefill_quarter"])
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--skip", default="", help="comma-separated secondary workloads to leave out")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
