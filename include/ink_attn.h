@@ -151,6 +151,37 @@ INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
                                void *workspace, size_t workspace_bytes,
                                ink_stream_t stream);
 
+/*
+ * Allocation-free variant (this entry point has no counterpart on the source
+ * pages).  For callers that cannot allocate device memory: programs embedded in
+ * a host that owns all device memory itself, such as a serving engine that has
+ * reserved nearly all of HBM for its paged KV-cache pool, or a plugin interface
+ * that passes an operator its tensors but no scratch buffer and no allocator.
+ * Same arguments and results as ink_rel_attn_varlen, without the workspace: the
+ * call runs on a scratch area of INK_STATIC_SCRATCH_BYTES compiled into the
+ * library, which every GPU that loads the library holds until the process exits.
+ *   - Work that needs more scratch than that (see ink_rel_attn_workspace_size)
+ *     returns INK_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the scratch area's device address for
+ *     that device (with it current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call, on every stream, shares the one scratch area of its device, and
+ *     the area keeps the last call's contents (each call clears what must start
+ *     at zero).  Calls that overlap on the GPU race on it: order them, for
+ *     example on one stream.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+#define INK_STATIC_SCRATCH_BYTES (32u << 20)
+INK_API ink_status ink_rel_attn_varlen_static(const ink_attn_dims *dims,
+                                              const void *q, const void *key_cache, const void *value_cache,
+                                              const int32_t *block_table, const int32_t *cache_seqlens,
+                                              const int32_t *cu_seqlens_q, int32_t max_seqlen_q,
+                                              float softmax_scale, int causal,
+                                              int32_t window_left, int32_t window_right,
+                                              int32_t rel_extent, const float *rel_logits,
+                                              int32_t num_splits, void *out, float *lse,
+                                              ink_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 INK_API const char *ink_status_string(ink_status status);
 
