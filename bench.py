@@ -23,6 +23,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -112,41 +113,119 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {"ink_decode_kernel": "ink_decode.cu", "ink_prefill_kernel": "ink_prefill.cu",
+                  "ink_combine_kernel": "ink_combine.cu", "ink_prepass_kernel": "ink_prepass.cu"}
+
+
+def kernel_source_hash(kernel):
+    """Hash of what one kernel is compiled from: its own .cu file and the shared header."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_varlen_attention_causal_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("ink_common.cuh", KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_of(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    """DRAM bytes per launch from the committed ncu summary, if taken on the kernel's current source."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        if t.get("source_hash") != kernel_source_hash():
+            k = json.load(f)["kernels"][kernel]
+        if k.get("source_hash") != kernel_source_hash(kernel):
             return None
-        return t["kernels"][kernel][workload]
+        return k[workload]
     except Exception:
         return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, clock-event reasons)."""
+
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: Optional[str], index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid.encode()), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_sm = self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn) -> Optional[float]:
+        v = self.c.c_uint(0)
+        return float(v.value) if fn(self.h, self.c.c_int(self.SM), self.c.byref(v)) == 0 else None
+
+    def sample(self):
+        v = self.c.c_ulonglong(0)
+        bits = v.value if self.reason_fn(self.h, self.c.byref(v)) == 0 else 0
+        return self._clock(self.lib.nvmlDeviceGetClockInfo), [n for b, n in self.REASONS.items() if bits & b]
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def _device_uuid(index: int) -> Optional[str]:
+    import torch
+    u = getattr(torch.cuda.get_device_properties(index), "uuid", None)
+    if u is None:
+        return None
+    u = str(u)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs.
+
+    NVML is polled every 2 ms from a thread (the timed regions last milliseconds,
+    shorter than nvidia-smi's start-up); nvidia-smi at 100 ms is the fallback.
+    """
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_s: float = 0.002):
         self.gpu = gpu_index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.sm, self.reasons = [], set()
+        self.stop = threading.Event()
+        self.t = None
+        try:
+            self.nvml = _Nvml(_device_uuid(gpu_index), gpu_index)
+        except Exception:
+            self.nvml = None
+
+    def _poll(self):
+        while True:
+            clk, rs = self.nvml.sample()
+            if clk is not None:
+                self.sm.append(clk)
+            self.reasons.update(rs)
+            if self.stop.wait(self.period):
+                return
 
     def __enter__(self):
+        if self.nvml is not None:
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -162,6 +241,9 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.stop.set()
+            self.t.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -170,6 +252,12 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            if not self.sm:
+                return {"sm_mhz": None, "sm_max_mhz": self.nvml.max_sm, "reasons": sorted(self.reasons),
+                        "samples": 0, "source": "nvml"}
+            return {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.nvml.max_sm,
+                    "reasons": sorted(self.reasons), "samples": len(self.sm), "source": "nvml"}
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -185,9 +273,9 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvidia-smi"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------------- ranks

@@ -19,7 +19,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA on sm_100-class SMs
 constexpr int kDecSharedBytes = 512;   // mbarriers + item ring of the decode kernel (upper bound)
-constexpr int kPfSharedBytes = 256;    // mbarriers of the prefill kernel (upper bound)
+constexpr int kPfSharedBytes = 512;    // mbarriers and bookkeeping of the prefill kernel (upper bound)
 constexpr int kDecMaxStages = 8;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -121,8 +121,10 @@ long long max_groups(const ink_attn_dims *d, int span, int causal, int wl, int w
 int heuristic_splits_decode(long long batch, long long groups, int sms)
 {
     const long long target_chunk = 32;  // 512 keys per split
+    const long long s_wave = ceil_div(4ll * sms, batch);  // units that fill every SM four times
     long long s = ceil_div(groups, target_chunk);
-    if (batch * s < 4ll * sms) s = ceil_div(4ll * sms, batch);
+    if (batch * s < 4ll * sms) s = s_wave;
+    s = std::min<long long>(s, std::max<long long>(64, s_wave));  // long rows: whole waves, fewer partials
     s = std::min<long long>(s, groups);
     s = std::min<long long>(s, 1024);
     return (int)std::max(1ll, s);
@@ -386,7 +388,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         Params pp = p;
         pp.bias_tma = bias_pf_tma ? 1 : 0;
         const int bias_slot = ((pl.G * 132 * 4) + 127) & ~127;
-        const size_t smem = 1024 + 32768 + 3 * 32768 + (size_t)pl.tpt * bias_slot + kPfSharedBytes;
+        const size_t smem = 1024 + 2 * 32768 + 2 * (size_t)pl.tpt * bias_slot + kPfSharedBytes;
         if (smem > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);
         if (timed_launch(INK_KERNEL_PREFILL, stream,
@@ -399,9 +401,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
                                                    window_right),
                                         pl.chunk_dec);
     if ((pl.any_decode && sdec_eff > 1) || (pl.any_prefill && pl.S_pf > 1)) {
-        const long long rows = (long long)T * H;
-        const int grid = (int)ceil_div(rows, 8);
-        if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, grid, stream); }) != cudaSuccess)
+        if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, stream); }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
     return INK_OK;

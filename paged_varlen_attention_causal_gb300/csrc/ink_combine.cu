@@ -4,94 +4,159 @@
 //     lse = log sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * O_s.
 // This is the log-sum-exp Phase 2 of the "paged_attention_v2_pytorch.py"
 // page (global max, per-partition weights exp(m_s - gmax) * l_s, weighted sum
-// divided by the weight total) written with lse_s = m_s + ln l_s.  Splits
-// with no visible key carry lse_s = -inf and weigh nothing.
-// One warp per row; lane l owns d values 4l..4l+3.
+// divided by the weight total) written with lse_s = m_s + ln l_s, streamed:
+// each warp keeps a running maximum and rescales its sums when it grows.
+// Splits with no visible key carry lse_s = -inf and weigh nothing.
+//
+// kWarpsPerRow warps share one row (warp w takes splits w, w + kWarpsPerRow, ...)
+// and merge their states through shared memory; lane l owns d values
+// 4l..4l+3.  Loads are issued kBatch splits at a time.
 #include "ink_common.cuh"
 
 namespace ink {
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 256;
+constexpr int kBatch = 4;
 
-__global__ void __launch_bounds__(kCombineWarps * 32) ink_combine_kernel(const Params p)
+struct RowPartials {
+    const float *po, *pl;
+    size_t first, stride;  // partial row of split s = first + s * stride
+    int nact;
+};
+
+// Locate the partials of row (t, h); false when the row needs no merge.
+__device__ __forceinline__ bool row_partials(const Params &p, int t, int h, RowPartials &rp)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * kCombineWarps + warp;
-    if (row >= (long long)p.T * p.H) return;
-    const int t = (int)(row / p.H), h = (int)(row % p.H);
-    // request owning token t: last b with cu[b] <= t and cu[b+1] > t
-    int lo = 0, hi = p.B - 1;
+    int lo = 0, hi = p.B - 1;  // request owning token t: first b with cu[b+1] > t
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         if (__ldg(p.cu + mid + 1) > t) hi = mid; else lo = mid + 1;
     }
     const int b = lo;
     const Req r = load_req(p, b);
-    if (!r.ok || t < r.t0 || t >= r.t0 + r.Lq) return;
+    if (!r.ok || t < r.t0 || t >= r.t0 + r.Lq) return false;
     const int i = t - r.t0;
-
-    const float *po;
-    const float *pl;
-    size_t stride_blk, first;  // partial row of split s = first + s * stride_blk
-    int nact;
     if (is_decode_req(p, r)) {
         const UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
-        nact = u.nact;
-        if (nact <= 1) return;
-        first = (size_t)__ldg(p.dec_off + b) * p.dec_rows + (size_t)i * p.H + h;
-        stride_blk = (size_t)p.dec_rows;
-        po = p.part_dec_o;
-        pl = p.part_dec_lse;
+        rp.nact = u.nact;
+        if (rp.nact <= 1) return false;
+        rp.first = (size_t)__ldg(p.dec_off + b) * p.dec_rows + (size_t)i * p.H + h;
+        rp.stride = (size_t)p.dec_rows;
+        rp.po = p.part_dec_o;
+        rp.pl = p.part_dec_lse;
     } else {
         const int qt = i / p.tpt, k = i % p.tpt;
         const int i0 = qt * p.tpt, i1 = min(r.Lq, i0 + p.tpt) - 1;
         const UnitSplit u = unit_split(i0 + r.Lk - r.Lq, i1 + r.Lk - r.Lq, r.Lk, p.causal, p.wl, p.wr, p.chunk_pf, 0);
-        nact = u.nact;
-        if (nact <= 1) return;
+        rp.nact = u.nact;
+        if (rp.nact <= 1) return false;
         const int g = h / p.G, j = h % p.G;
         const size_t rows = (size_t)p.Hkv * kTileRows;
-        first = (size_t)(__ldg(p.unit_off + b) + qt) * p.S_pf * rows + (size_t)g * kTileRows +
-                pf_row_of(p.fast_pack, p.G, k, j);
-        stride_blk = rows;
-        po = p.part_pf_o;
-        pl = p.part_pf_lse;
+        rp.first = (size_t)(__ldg(p.unit_off + b) + qt) * p.S_pf * rows + (size_t)g * kTileRows +
+                   pf_row_of(p.fast_pack, p.G, k, j);
+        rp.stride = rows;
+        rp.po = p.part_pf_o;
+        rp.pl = p.part_pf_lse;
     }
-    // global maximum of the split log-sum-exps
-    float m = -INFINITY;
-    for (int s = lane; s < nact; s += 32) m = fmaxf(m, pl[first + (size_t)s * stride_blk]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return true;
+}
+
+template <int kWarpsPerRow>
+__global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Params p)
+{
+    constexpr int kRowsPerCta = kCombineThreads / 32 / kWarpsPerRow;
+    __shared__ float s_m[kCombineThreads / 32], s_l[kCombineThreads / 32];
+    __shared__ float4 s_acc[kWarpsPerRow > 1 ? kCombineThreads / 32 : 1][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % kWarpsPerRow;  // this warp's share of the row's splits
+    const long long row = (long long)blockIdx.x * kRowsPerCta + warp / kWarpsPerRow;
+    RowPartials rp;
+    bool active = row < (long long)p.T * p.H;
+    if (active) active = row_partials(p, (int)(row / p.H), (int)(row % p.H), rp);
+    if (kWarpsPerRow == 1 && !active) return;
+
+    float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (m != -INFINITY) {
-        for (int s0 = 0; s0 < nact; s0 += 32) {
-            const int s = s0 + lane;
-            const float w_l = (s < nact) ? __expf(pl[first + (size_t)s * stride_blk] - m) : 0.f;
-            const int n = min(32, nact - s0);
-            for (int q = 0; q < n; ++q) {
-                const float w = __shfl_sync(0xffffffffu, w_l, q);
-                wsum += w;
-                if (w != 0.f) {
-                    const float4 v = *reinterpret_cast<const float4 *>(po + (first + (size_t)(s0 + q) * stride_blk) * kHeadDim + 4 * lane);
-                    acc.x = fmaf(w, v.x, acc.x);
-                    acc.y = fmaf(w, v.y, acc.y);
-                    acc.z = fmaf(w, v.z, acc.z);
-                    acc.w = fmaf(w, v.w, acc.w);
+    if (active) {
+        for (int s0 = sub; s0 < rp.nact; s0 += kWarpsPerRow * kBatch) {
+            float ls[kBatch];
+            float4 os[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {  // issue the batch's loads before using any of them
+                const int s = s0 + u * kWarpsPerRow;
+                ls[u] = -INFINITY;
+                os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (s < rp.nact) {
+                    const size_t pr = rp.first + (size_t)s * rp.stride;
+                    ls[u] = __ldg(rp.pl + pr);
+                    os[u] = __ldg(reinterpret_cast<const float4 *>(rp.po + pr * kHeadDim) + lane);
                 }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (ls[u] == -INFINITY) continue;
+                if (ls[u] > m) {
+                    const float a = __expf(m - ls[u]);  // m = -inf gives 0
+                    acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+                    l *= a;
+                    m = ls[u];
+                }
+                const float w = __expf(ls[u] - m);
+                l += w;
+                acc.x = fmaf(w, os[u].x, acc.x);
+                acc.y = fmaf(w, os[u].y, acc.y);
+                acc.z = fmaf(w, os[u].z, acc.z);
+                acc.w = fmaf(w, os[u].w, acc.w);
             }
         }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    if (kWarpsPerRow > 1) {
+        if (lane == 0) {
+            s_m[warp] = m;
+            s_l[warp] = l;
+        }
+        s_acc[warp][lane] = acc;
+        __syncthreads();
+        if (!active || sub != 0) return;
+        float gm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerRow; ++w) gm = fmaxf(gm, s_m[warp + w]);
+        l = 0.f;
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gm != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarpsPerRow; ++w) {
+                if (s_m[warp + w] == -INFINITY) continue;
+                const float a = __expf(s_m[warp + w] - gm);
+                const float4 v = s_acc[warp + w][lane];
+                l = fmaf(a, s_l[warp + w], l);
+                acc.x = fmaf(a, v.x, acc.x);
+                acc.y = fmaf(a, v.y, acc.y);
+                acc.z = fmaf(a, v.z, acc.z);
+                acc.w = fmaf(a, v.w, acc.w);
+            }
+        }
+        m = gm;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     uint2 outv;
     outv.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     outv.y = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2 *>(p.out + (size_t)row * kHeadDim + 4 * lane) = outv;
-    if (p.lse && lane == 0) p.lse[row] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+    if (p.lse && lane == 0) p.lse[row] = l > 0.f ? m + __logf(l) : -INFINITY;
 }
 
-cudaError_t launch_combine(const Params &p, int grid, cudaStream_t stream)
+// Few rows (long splits) get eight warps each; many rows get one warp each.
+cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream)
 {
-    ink_combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(p);
+    const long long rows = (long long)p.T * p.H;
+    if (rows * 8 <= 4ll * sms * (kCombineThreads / 32)) {
+        const long long grid = rows;
+        ink_combine_kernel<8><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
+    } else {
+        const long long grid = (rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+        ink_combine_kernel<1><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

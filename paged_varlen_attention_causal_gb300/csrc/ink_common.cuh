@@ -233,6 +233,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// The same wait for a whole warp: every lane waits and the lanes agree on the
+// outcome, so that a warp stays converged for the warp-collective instructions
+// (tcgen05.ld/st, mma.sync, shuffles) that follow even when a wait gives up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               const Params &p)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, p));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -310,6 +319,6 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
                           int bias_slot_bytes, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_combine(const Params &p, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
 
 }  // namespace ink

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 next = __shfl_sync(0xffffffffu, next, 0);
             }
             const int slot = iseq & 1;
-            if (!mbar_wait(&sh.item_empty[slot], ((iseq >> 1) & 1) ^ 1, abort, p)) break;
+            if (!mbar_wait_warp(&sh.item_empty[slot], ((iseq >> 1) & 1) ^ 1, abort, p)) break;
             DecItem it;
             it.valid = 0;
             if (cur < total) {
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
                 const int page = __shfl_sync(0xffffffffu, pages, rel);
                 const int stage = n % nstages;
-                if (!mbar_wait(&sh.empty[stage], ((n / nstages) & 1) ^ 1, abort, p)) break;
+                if (!mbar_wait_warp(&sh.empty[stage], ((n / nstages) & 1) ^ 1, abort, p)) break;
                 const bool band = p.bias_tma && group_in_band(qa0, qa1, gi, p.E);
                 uint8_t *st = ring + (size_t)stage * stage_bytes;
                 if (lane == 0) {
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     uint32_t n = 0;
     for (uint32_t iseq = 0;; ++iseq) {
         const int slot = iseq & 1;
-        if (!mbar_wait(&sh.item_full[slot], (iseq >> 1) & 1, abort, p)) break;
+        if (!mbar_wait_warp(&sh.item_full[slot], (iseq >> 1) & 1, abort, p)) break;
         const DecItem it = sh.item[slot];
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.item_empty[slot]);
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
         for (int gi = it.gb; gi < it.ge; ++gi, ++n) {
             const int stage = n % nstages;
-            if (!mbar_wait(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
+            if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
             const uint8_t *st = ring + (size_t)stage * stage_bytes;
             const uint32_t kbase = smem_u32(st) + g * 4096;
             const uint32_t vbase = kbase + kv_bytes;

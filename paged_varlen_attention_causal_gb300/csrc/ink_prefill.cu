@@ -4,16 +4,19 @@
 // One work item = (request, q tile, split, KV head): 128 packed rows, i.e.
 // 128/G tokens x the G query heads that share KV head g (GQA packing, a4).
 // Persistent CTAs (one per SM) walk the device-built item list, longest
-// items first.  Warp roles:
-//   warp 0      page-gather producer (a3): per 16-key group one block_table
-//               read and two TMA boxes (d halves, 128-byte swizzle) per
-//               tensor into a 3-slot K/V ring; per bias tile one fp32 TMA box
-//               of rel_logits per token (out-of-range distances read as 0);
+// items first.  Tensor memory: a 2-slot ring of S tiles (128 x 128 fp32),
+// the O accumulator (128 x 128 fp32) and the Q tile (128 x 128 bf16).
+// Warp roles:
+//   warp 0      page-gather producer (a3): block_table entries are prefetched
+//               32 groups ahead; per 16-key group two TMA boxes (d halves,
+//               128-byte swizzle) per tensor into a 2-slot K/V ring;
 //   warp 1      tensor-memory allocator and single-thread MMA issuer (a5, a9):
-//               S = Q K^T (M128 N128 K16 x 8, smem x smem) into a 3-slot S ring
-//               in TMEM, O += P V with P read from TMEM (M128 N128 K16 x 8);
-//   warps 2-3   Q tile loader (coalesced 16-byte loads, manual swizzle);
-//   warps 4-7   online softmax (a8) and epilogue (a10); thread = TMEM lane = row;
+//               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
+//               O += P V with P read from tensor memory (M128 N128 K16 x 8);
+//   warp 2      bias producer: per bias tile one fp32 TMA box of rel_logits per
+//               token (out-of-range distances read as 0) into a 2-slot ring;
+//   warps 4-7   online softmax (a8), epilogue (a10), and the next item's Q
+//               rows written into tensor memory; thread = TMEM lane = row;
 //   warps 8-11  relative bias and masks (a6, a7): for tiles that need them,
 //               write bias/scale (or -inf) into the S slot before the QK MMA
 //               accumulates onto it, so the softmax warps never touch bias.
@@ -25,12 +28,13 @@
 namespace ink {
 
 constexpr int kPfThreads = 12 * 32;
-constexpr int kKvSlots = 3;
-constexpr int kSSlots = 3;
+constexpr int kKvSlots = 2;
+constexpr int kSSlots = 2;
+constexpr int kBiasSlots = 2;
 constexpr int kSlotBytes = 32768;           // one K or V tile: 2 d halves x 128 rows x 128 B
 constexpr int kBiasBox = 132;               // floats per bias row box (128 + 4 for alignment)
 constexpr int kRescaleThreshold = 8;        // log2 units (factor 256)
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;         // S ring 2 x 128 | O 128 | Q 64 (bf16 pairs)
 
 // Instruction descriptor, kind::f16: D f32, A bf16, B bf16, M 128, N 128.
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -102,10 +106,11 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 
 struct PfShared {
     uint64_t kv_full[kKvSlots], kv_empty[kKvSlots];
-    uint64_t bias_full, bias_empty;
-    uint64_t q_full, q_empty;
+    uint64_t bias_full[kBiasSlots], bias_empty[kBiasSlots];
+    uint64_t q_full;
     uint64_t s_init[kSSlots], s_full[kSSlots], p_full[kSSlots], pv_done[kSSlots];
     uint64_t o_full;
+    int32_t tile_keys[4][8];  // producer's record of recent tiles' key coordinates (reused by V)
     uint32_t tmem_base;
     int abort;
     // Tiles (CTA-wide sequence numbers) whose PV product has completed: published by the
@@ -234,11 +239,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    uint8_t *q_smem = base;                                   // 32 KB
-    uint8_t *kv_smem = base + 32768;                          // 3 x 32 KB
-    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // tpt x slot
+    uint8_t *kv_smem = base;                                  // 2 x 32 KB
+    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // 2 x (tpt x slot)
     const int bias_slot = pf_bias_slot_bytes(p);
-    PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + p.tpt * bias_slot);
+    const int bias_stage = p.tpt * bias_slot;
+    PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + kBiasSlots * bias_stage);
     volatile int *abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -249,10 +254,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 1);
         }
-        mbar_init(&sh.bias_full, 1);
-        mbar_init(&sh.bias_empty, 4);
-        mbar_init(&sh.q_full, 2);
-        mbar_init(&sh.q_empty, 1);
+        for (int s = 0; s < kBiasSlots; ++s) {
+            mbar_init(&sh.bias_full[s], 1);
+            mbar_init(&sh.bias_empty[s], 4);
+        }
+        mbar_init(&sh.q_full, 4);
         for (int s = 0; s < kSSlots; ++s) {
             mbar_init(&sh.s_init[s], 4);
             mbar_init(&sh.s_full[s], 1);
@@ -275,88 +281,116 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const uint32_t tmem_o = tmem + kSSlots * 128;
+    const uint32_t tmem_q = tmem_o + 128;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- producer
+        // ---------------------------------------------------------------- K/V producer
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            if (p.bias_tma) prefetch_tmap(&tm_bias);
         }
         const uint64_t pol_kv = policy_evict_last();
-        const uint64_t pol_bias = policy_evict_first();
-        uint32_t seq = 0, bseq = 0;
-        for (int r = 0;; ++r) {
-            const int idx = pf_item_index(r);
-            if (idx >= total || *abort) break;
-            const PfItem it = pf_item(p, p.pf_items[idx]);
-            const int32_t *bt_row = p.bt + (size_t)it.b * p.MAXBLK;
-            // load order: K0, then K_n, V_{n-1} for n >= 1, then V_{last}
-            for (int step = 0; step <= it.ntiles && it.ntiles > 0; ++step) {
-                for (int which = 0; which < 2; ++which) {
-                    int n, isV;
-                    if (step == 0) { if (which) break; n = 0; isV = 0; }
-                    else if (step == it.ntiles) { if (which) break; n = it.ntiles - 1; isV = 1; }
-                    else { n = which ? step - 1 : step; isV = which; }
-                    const int slot = seq % kKvSlots;
-                    if (!mbar_wait(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
-                    const int gfirst = it.gb + 8 * n;
-                    // one page id per lane (lanes 0-7), key coordinate of its 16-key group
-                    int key0 = -kKeyGroup;
-                    if (lane < 8 && gfirst + lane < it.ge) {
-                        const int gi = gfirst + lane;
-                        const int pid = __ldg(bt_row + (gi * kKeyGroup) / p.BS);
-                        if (pid >= 0 && pid < p.NB) key0 = pid * p.BS + (gi * kKeyGroup) % p.BS;
-                        else report(p, INK_DEVERR_PAGE_ID);
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
-                    __syncwarp();
-                    if (lane < 16) {
-                        const int grp = lane & 7, dh = lane >> 3;
-                        const int kc = __shfl_sync(0x0000ffffu, key0, grp);
-                        uint8_t *dst = kv_smem + slot * kSlotBytes + dh * 16384 + grp * 2048;
-                        tma_load_3d_hint(dst, isV ? &tm_v : &tm_k, dh * 64, it.g, kc, &sh.kv_full[slot], pol_kv);
-                    }
-                    __syncwarp();
-                    ++seq;
-                    // bias of tile n travels right after K_n
-                    if (!isV && p.bias_tma && pf_tile_bias(p, it, n)) {
-                        if (!mbar_wait(&sh.bias_empty, (bseq & 1) ^ 1, abort, p)) break;
-                        const int j0 = pf_tile_key0(it, n);
-                        if (lane == 0)
-                            mbar_arrive_expect_tx(&sh.bias_full, (uint32_t)it.ntok * p.G * kBiasBox * 4);
-                        __syncwarp();
-                        for (int k = lane; k < it.ntok; k += 32) {
-                            const int qa = it.qa_min + k;
-                            const int start = qa - j0 - (kTileKeys - 1);
-                            const int x0 = start >= 0 ? (start & ~3) : -(((-start) + 3) & ~3);
-                            tma_load_3d_hint(bias_smem + k * bias_slot, &tm_bias, x0, it.g * p.G, it.t0 + it.i0 + k,
-                                             &sh.bias_full, pol_bias);
-                        }
-                        __syncwarp();
-                        ++bseq;
-                    }
-                }
-                if (*abort) break;
-            }
-        }
-        // let copies still in flight land before the CTA can exit
-        if (lane == 0) {
-            for (uint32_t k = (seq > kKvSlots ? seq - kKvSlots : 0); k < seq; ++k)
-                mbar_wait(&sh.kv_full[k % kKvSlots], (k / kKvSlots) & 1, abort, p);
-            if (bseq > 0) mbar_wait(&sh.bias_full, (bseq - 1) & 1, abort, p);
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        uint32_t seq = 0, tc = 0, qseq = 0;
-        uint32_t init_cnt[kSSlots] = {0, 0, 0};  // s_init phases seen per S slot (only tiles with bias/masks)
+        uint32_t seq = 0;
         for (int r = 0;; ++r) {
             const int idx = pf_item_index(r);
             if (idx >= total || *abort) break;
             const PfItem it = pf_item(p, p.pf_items[idx]);
             if (it.ntiles == 0) continue;
-            if (!mbar_wait(&sh.q_full, qseq & 1, abort, p)) break;
-            const uint32_t qaddr = smem_u32(q_smem);
+            const int32_t *bt_row = p.bt + (size_t)it.b * p.MAXBLK;
+            // key coordinate of group gb + 32 * chunk + lane (-16, i.e. zero fill, past the split or on a bad page)
+            auto load_keys = [&](int chunk) {
+                const int gi = it.gb + 32 * chunk + lane;
+                int key = -kKeyGroup;
+                if (gi < it.ge) {
+                    const int pid = __ldg(bt_row + (gi * kKeyGroup) / p.BS);
+                    if (pid >= 0 && pid < p.NB) key = pid * p.BS + (gi * kKeyGroup) % p.BS;
+                    else report(p, INK_DEVERR_PAGE_ID);
+                }
+                return key;
+            };
+            int keys_cur = load_keys(0), keys_nxt = load_keys(1), chunk = 0;
+            // load order: K0, then K_n, V_{n-1} for n >= 1, then V_{last}
+            for (int step = 0; step <= it.ntiles; ++step) {
+                for (int which = 0; which < 2; ++which) {
+                    int n, isV;
+                    if (step == 0) { if (which) break; n = 0; isV = 0; }
+                    else if (step == it.ntiles) { if (which) break; n = it.ntiles - 1; isV = 1; }
+                    else { n = which ? step - 1 : step; isV = which; }
+                    int key0;
+                    if (!isV) {
+                        while (chunk < n / 4) {  // advance the prefetch window by 32 groups
+                            keys_cur = keys_nxt;
+                            ++chunk;
+                            keys_nxt = load_keys(chunk + 1);
+                        }
+                        key0 = __shfl_sync(0xffffffffu, keys_cur, (n % 4) * 8 + (lane & 7));
+                        if (lane < 8) sh.tile_keys[n % 4][lane] = key0;
+                    } else {
+                        key0 = sh.tile_keys[n % 4][lane & 7];
+                    }
+                    __syncwarp();
+                    const int slot = seq % kKvSlots;
+                    if (!mbar_wait_warp(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
+                    if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
+                    __syncwarp();
+                    if (lane < 16) {
+                        const int grp = lane & 7, dh = lane >> 3;
+                        uint8_t *dst = kv_smem + slot * kSlotBytes + dh * 16384 + grp * 2048;
+                        tma_load_3d_hint(dst, isV ? &tm_v : &tm_k, dh * 64, it.g, key0, &sh.kv_full[slot], pol_kv);
+                    }
+                    __syncwarp();
+                    ++seq;
+                }
+                if (*abort) break;
+            }
+        }
+        // let copies still in flight land before the CTA can exit
+        if (lane == 0)
+            for (uint32_t k = (seq > kKvSlots ? seq - kKvSlots : 0); k < seq; ++k)
+                mbar_wait(&sh.kv_full[k % kKvSlots], (k / kKvSlots) & 1, abort, p);
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- bias producer
+        if (p.bias_tma) {
+            if (lane == 0) prefetch_tmap(&tm_bias);
+            const uint64_t pol_bias = policy_evict_first();
+            uint32_t bseq = 0;
+            for (int r = 0;; ++r) {
+                const int idx = pf_item_index(r);
+                if (idx >= total || *abort) break;
+                const PfItem it = pf_item(p, p.pf_items[idx]);
+                for (int n = 0; n < it.ntiles; ++n) {
+                    if (!pf_tile_bias(p, it, n)) continue;
+                    const int bs = bseq % kBiasSlots;
+                    if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) break;
+                    const int j0 = pf_tile_key0(it, n);
+                    if (lane == 0) mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)it.ntok * p.G * kBiasBox * 4);
+                    __syncwarp();
+                    for (int k = lane; k < it.ntok; k += 32) {
+                        const int qa = it.qa_min + k;
+                        const int start = qa - j0 - (kTileKeys - 1);
+                        const int x0 = start >= 0 ? (start & ~3) : -(((-start) + 3) & ~3);
+                        tma_load_3d_hint(bias_smem + bs * bias_stage + k * bias_slot, &tm_bias, x0, it.g * p.G,
+                                         it.t0 + it.i0 + k, &sh.bias_full[bs], pol_bias);
+                    }
+                    __syncwarp();
+                    ++bseq;
+                }
+                if (*abort) break;
+            }
+            if (lane == 0)
+                for (uint32_t k = (bseq > kBiasSlots ? bseq - kBiasSlots : 0); k < bseq; ++k)
+                    mbar_wait(&sh.bias_full[k % kBiasSlots], (k / kBiasSlots) & 1, abort, p);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        uint32_t seq = 0, tc = 0, qseq = 0;
+        uint32_t init_cnt[kSSlots] = {0, 0};  // s_init phases seen per S slot (only tiles with bias/masks)
+        for (int r = 0;; ++r) {
+            const int idx = pf_item_index(r);
+            if (idx >= total || *abort) break;
+            const PfItem it = pf_item(p, p.pf_items[idx]);
+            if (it.ntiles == 0) continue;
+            if (!mbar_wait_warp(&sh.q_full, qseq & 1, abort, p)) break;
             const uint32_t tc0 = tc;
             auto zero_tail = [&](int slot, int n) {
                 // keys at or beyond Lk inside loaded groups may hold stale data: zero them
@@ -377,9 +411,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             auto issue_pv = [&](int m) {
                 const uint32_t t = tc0 + m;
                 const int ss = t % kSSlots;
-                if (!mbar_wait(&sh.p_full[ss], (t / kSSlots) & 1, abort, p)) return false;
+                if (!mbar_wait_warp(&sh.p_full[ss], (t / kSSlots) & 1, abort, p)) return false;
                 const int slot = seq % kKvSlots;
-                if (!mbar_wait(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) return false;
+                if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) return false;
                 zero_tail(slot, m);
                 tc_fence_after();
                 if (lane == 0) {
@@ -401,10 +435,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const uint32_t t = tc0 + n;
                 const int ss = t % kSSlots;
                 const int slot = seq % kKvSlots;
-                if (!mbar_wait(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
+                if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
                 const bool init = pf_tile_bias(p, it, n) || pf_tile_mask(it, n);
                 if (init) {
-                    if (!mbar_wait(&sh.s_init[ss], init_cnt[ss] & 1, abort, p)) { ok = false; break; }
+                    if (!mbar_wait_warp(&sh.s_init[ss], init_cnt[ss] & 1, abort, p)) { ok = false; break; }
                     ++init_cnt[ss];
                 }
                 zero_tail(slot, n);
@@ -414,13 +448,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint64_t adesc = smem_desc(qaddr + off, 16, 1024);
                         const uint64_t bdesc = smem_desc(kaddr + off, 16, 1024);
-                        mma_ss(tmem + ss * 128, adesc, bdesc, kIdescQK, (init || kk > 0) ? 1u : 0u);
+                        mma_ts(tmem + ss * 128, tmem_q + kk * 8, bdesc, kIdescQK, (init || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&sh.s_full[ss]);
                     mma_commit(&sh.kv_empty[slot]);
-                    if (n == it.ntiles - 1) mma_commit(&sh.q_empty);
                 }
                 __syncwarp();
                 ++seq;
@@ -433,38 +465,49 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ++qseq;
             if (!ok) break;
         }
-    } else if (warp == 2 || warp == 3) {
-        // ---------------------------------------------------------------- Q loader
-        const int t = threadIdx.x - 64;  // 0..63
-        uint32_t qseq = 0;
-        for (int r = 0;; ++r) {
-            const int idx = pf_item_index(r);
-            if (idx >= total || *abort) break;
-            const PfItem it = pf_item(p, p.pf_items[idx]);
-            if (it.ntiles == 0) continue;
-            if (!mbar_wait(&sh.q_empty, (qseq & 1) ^ 1, abort, p)) break;
-            for (int c = t; c < kTileRows * 16; c += 64) {
-                const int L = c >> 4, ch = c & 15;
-                int k, j;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (pf_row(p, L, k, j) && k < it.ntok) {
-                    const __nv_bfloat16 *src =
-                        p.q + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * kHeadDim + ch * 8;
-                    v = __ldg(reinterpret_cast<const uint4 *>(src));
-                }
-                *reinterpret_cast<uint4 *>(q_smem + (ch >> 3) * 16384 + swz128(L * 128 + (ch & 7) * 16)) = v;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.q_full);
-            ++qseq;
-        }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- softmax + epilogue
+        // ---------------------------------------------------------------- softmax + epilogue + Q
         const int L = (warp - 4) * 32 + lane;
         const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
         const float sl2 = p.scale_log2;
         const float ln2 = 0.6931471805599453f;
+        // Q rows of an item into tensor memory (bf16 pairs along d), then signal the MMA warp.
+        auto write_q = [&](const PfItem &it) {
+            int k, j;
+            const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
+            uint32_t qv[64];
+            if (row_ok) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * kHeadDim);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = __ldg(src + c);
+                    qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) qv[c] = 0u;
+            }
+            INK_TMEM_ST32(tmem_q + lane_addr + 0, (qv + 0));
+            INK_TMEM_ST32(tmem_q + lane_addr + 32, (qv + 32));
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.q_full);
+        };
+        // next item (round > r) that has tiles, or -1
+        auto next_with_tiles = [&](int r, PfItem &nx) {
+            for (int r2 = r + 1;; ++r2) {
+                const int idx = pf_item_index(r2);
+                if (idx >= total) return false;
+                nx = pf_item(p, p.pf_items[idx]);
+                if (nx.ntiles > 0) return true;
+            }
+        };
+        {
+            PfItem first;
+            if (next_with_tiles(-1, first)) write_q(first);
+        }
         uint32_t tc = 0, oseq = 0;
         for (int r = 0;; ++r) {
             const int idx = pf_item_index(r);
@@ -478,7 +521,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int n = 0; n < it.ntiles; ++n) {
                 const uint32_t t = tc + n;
                 const int ss = t % kSSlots;
-                if (!mbar_wait(&sh.s_full[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
+                if (!mbar_wait_warp(&sh.s_full[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sv[128];
                 const uint32_t sa = tmem + lane_addr + ss * 128;
@@ -503,28 +546,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 auto see_prev_pv = [&]() {
                     if (pv_prev_seen) return true;
                     const uint32_t tp = t - 1;
-                    if (!mbar_wait(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) return false;
+                    if (!mbar_wait_warp(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) return false;
                     pv_prev_seen = true;
                     return true;
                 };
+                // The running maximum moves only when it grows past the threshold (or was -inf).
+                float alpha = 1.f;
+                bool scale_o = false;
                 if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * sl2 > (float)kRescaleThreshold)) {
-                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2((m_used - mx) * sl2);
+                    alpha = (m_used == -INFINITY) ? 0.f : fast_exp2((m_used - mx) * sl2);
                     l *= alpha;
-                    if (n > 0 && m_used != -INFINITY) {
-                        // O holds tiles 0..n-1 once PV(n-1) is done: rescale it in place
-                        if (!see_prev_pv()) { ok = false; break; }
-                        tc_fence_after();
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            uint32_t ov[32];
-                            INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
-                            tc_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            INK_TMEM_ST32(tmem_o + lane_addr + cc * 32, ov);
-                        }
-                    }
+                    scale_o = n > 0 && m_used != -INFINITY;
                     m_used = mx;
+                }
+                // The decision is per row, but tcgen05.ld/st are warp-collective: the warp
+                // rescales its 32 O rows together, by 1 in the rows that keep their maximum.
+                if (__any_sync(0xffffffffu, scale_o)) {
+                    // O holds tiles 0..n-1 once PV(n-1) is done: rescale it in place
+                    if (!see_prev_pv()) { ok = false; break; }
+                    tc_fence_after();
+                    const float a = scale_o ? alpha : 1.f;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t ov[32];
+                        INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
+                        INK_TMEM_ST32(tmem_o + lane_addr + cc * 32, ov);
+                    }
                 }
                 const float moff = (m_used == -INFINITY) ? 0.f : m_used * sl2;
                 uint32_t pk[64];
@@ -551,9 +601,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
             }
             if (!ok) break;
+            if (it.ntiles > 0) {
+                // every QK of this item is complete: the next item's Q may replace this one
+                PfItem nx;
+                if (next_with_tiles(r, nx)) write_q(nx);
+            }
             // epilogue
             if (it.ntiles > 0) {
-                if (!mbar_wait(&sh.o_full, oseq & 1, abort, p)) break;
+                if (!mbar_wait_warp(&sh.o_full, oseq & 1, abort, p)) break;
                 ++oseq;
                 tc_fence_after();
             }
@@ -607,7 +662,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_fence_before();
             tc += it.ntiles;
         }
-    } else {
+    } else if (warp >= 8) {
         // ---------------------------------------------------------------- bias + masks
         const int L = (warp - 8) * 32 + lane;
         const uint32_t lane_addr = (uint32_t)((warp - 8) * 32) << 16;
@@ -640,9 +695,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 for (int c = 0; c < 128; ++c) v[c] = 0.f;
                 if (has_bias) {
                     if (p.bias_tma) {
-                        if (!mbar_wait(&sh.bias_full, bseq & 1, abort, p)) { ok = false; break; }
+                        const int bs = bseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_full[bs], (bseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
                         if (row_ok) {
-                            const float *box = reinterpret_cast<const float *>(bias_smem + k * bias_slot) + j * kBiasBox;
+                            const float *box =
+                                reinterpret_cast<const float *>(bias_smem + bs * bias_stage + k * bias_slot) + j * kBiasBox;
                             const int o = (qa - j0 - (kTileKeys - 1)) & 3;
                             switch (o) {
                                 case 0: bias_from_box<0>(box, v); break;
@@ -652,7 +709,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             }
                         }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&sh.bias_empty);
+                        if (lane == 0) mbar_arrive(&sh.bias_empty[bs]);
                         ++bseq;
                     } else if (row_ok) {
 #pragma unroll
@@ -662,9 +719,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         }
                     }
                 }
-                // the S slot is free once the PV of the tile that used it before (t - 3) is done,
-                // i.e. once PV completions through tile t - 3 have been published (pv_seen >= t - 2)
-                if (t >= kSSlots && !wait_counter(&sh.pv_seen, t - kSSlots + 1, abort, p)) { ok = false; break; }
+                // the S slot is free once the PV of the tile that used it before (t - 2) is done,
+                // i.e. once PV completions through tile t - 2 have been published (pv_seen >= t - 1)
+                if (t >= kSSlots && !__all_sync(0xffffffffu, wait_counter(&sh.pv_seen, t - kSSlots + 1, abort, p))) {
+                    ok = false;
+                    break;
+                }
                 uint32_t w[128];
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {

@@ -66,3 +66,27 @@ def test_workload_totals():
             assert abs(flops / 1e12 - 0.8934) < 1e-4
         if name == "long_decode":
             assert kv == (1 << 20) * 8 * 128 * 2 * 2
+
+
+class _FakeNvml:
+    max_sm = 2070.0
+
+    def __init__(self):
+        self.calls = 0
+
+    def sample(self):
+        self.calls += 1
+        return (1965.0 if self.calls % 2 else 2070.0), (["sw_power_cap"] if self.calls == 3 else [])
+
+
+def test_clock_sampler_summarises_polled_samples():
+    import time
+
+    cs = bench.ClockSampler(0)
+    cs.nvml = _FakeNvml()
+    with cs:
+        time.sleep(0.05)
+    s = cs.summary()
+    assert s["samples"] >= 3 and s["source"] == "nvml"
+    assert s["sm_max_mhz"] == 2070.0 and s["sm_mhz"] in (1965.0, 2017.5, 2070.0)
+    assert s["reasons"] == ["sw_power_cap"]

@@ -146,6 +146,24 @@ def test_multi_item_prefill(E, window):
     check(out, lse, ref_out, ref_lse, rows=rows, what=f"multi-item E={E} window={window}")
 
 
+@pytest.mark.parametrize("splits", [0, 1])
+def test_partial_warp_rescale(splits):
+    """Only some rows of a warp move their running maximum late in the key range.
+
+    A +20 bias on the four nearest distances of the odd heads makes the rows of
+    those heads (every other lane of each softmax warp) raise their maximum by far
+    more than the rescale threshold on the diagonal tile, while the even heads keep
+    theirs; the warp must rescale its O rows together.
+    """
+    case = build_case("late_max", [1536], [1536], H=16, Hkv=2, E=64, seed=41, device="cuda")
+    case.rel_logits[:, 1::2, :4] += 20.0
+    out, lse = gpu_run(case, num_splits=splits)
+    assert errors_of_last_call() == 0
+    rows = sampled_rows(case, 600, 5)
+    ref_out, ref_lse = oracle_run(case, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what=f"late maximum, splits={splits}")
+
+
 # --- edge cases -------------------------------------------------------------------------
 
 def test_empty_requests_and_empty_rows():
