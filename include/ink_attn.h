@@ -81,6 +81,7 @@ typedef enum {
 #define INK_DEVERR_SEQLEN_K   0x08u /* cache_seqlens[b] < 0 or > max_blocks_per_seq * block_size */
 #define INK_DEVERR_EMPTY_ROWS 0x10u /* informational: some rows saw no key (out 0, lse -inf), e.g. causal with Lk < Lq */
 #define INK_DEVERR_TIMEOUT    0x100u /* a bounded pipeline wait gave up; outputs of the call are undefined */
+#define INK_DEVERR_SMEM       0x200u /* a kernel found less shared memory than its layout needs and did nothing */
 
 /*
  * Bytes of device workspace one call needs.  `num_splits` as in

@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_HERE, "libinkattn.so")
 
 DEVERR = {
     "PAGE_ID": 0x01, "CU_SEQLENS": 0x02, "SEQLEN_Q": 0x04, "SEQLEN_K": 0x08, "EMPTY_ROWS": 0x10,
-    "TIMEOUT": 0x100,
+    "TIMEOUT": 0x100, "SMEM": 0x200,
 }
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace too small",
            4: "CUDA error"}

@@ -19,7 +19,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA on sm_100-class SMs
 constexpr int kDecSharedBytes = 512;   // mbarriers + item ring of the decode kernel (upper bound)
-constexpr int kPfSharedBytes = 512;    // mbarriers and bookkeeping of the prefill kernel (upper bound)
 constexpr int kDecMaxStages = 8;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -354,7 +353,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
             bias_dec_tma = encode(&tm_bdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box,
                                   CU_TENSOR_MAP_SWIZZLE_NONE);
         }
-        const cuuint32_t box2[3] = {132, (cuuint32_t)pl.G, 1};
+        const cuuint32_t box2[3] = {(cuuint32_t)kPfBiasBox, (cuuint32_t)pl.G, 1};
         bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
                              CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -387,9 +386,10 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     if (pl.any_prefill && pl.pf_cap > 0) {
         Params pp = p;
         pp.bias_tma = bias_pf_tma ? 1 : 0;
-        const int bias_slot = ((pl.G * 132 * 4) + 127) & ~127;
-        const size_t smem = 1024 + 2 * 32768 + 2 * (size_t)pl.tpt * bias_slot + kPfSharedBytes;
-        if (smem > kSmemLimit) return INK_ERR_UNSUPPORTED;
+        // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
+        const size_t layout = 2 * 32768 + 2 * (size_t)pl.tpt * pf_bias_slot_bytes(pl.G) + kPfSharedBytes;
+        if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
+        const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);
         if (timed_launch(INK_KERNEL_PREFILL, stream,
                          [&] { return launch_prefill(pp, tm_k, tm_v, tm_bpf, grid, smem, stream); }) != cudaSuccess)

@@ -17,6 +17,8 @@ constexpr int kKeyGroup = 16;     // keys per TMA box / per decode stage
 constexpr int kTileKeys = 128;    // keys per prefill KV tile (8 groups)
 constexpr int kTileRows = 128;    // packed (token, head) rows per prefill tile
 constexpr int kDecodeRows = 16;   // packed rows per KV head in the decode kernel
+constexpr int kPfBiasBox = 132;   // floats per prefill bias box row (128 keys + 4 for 16-byte alignment)
+constexpr int kPfSharedBytes = 2560;  // prefill barriers and bookkeeping (upper bound)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after ~2 s
 constexpr uint32_t kWaitHintNs = 100000;           // longest single suspension of a wait (100 us)
 
@@ -137,6 +139,10 @@ __host__ __device__ __forceinline__ UnitSplit unit_split(int qa0, int qa1, int L
     return u;
 }
 
+// Bytes per token in a prefill bias stage: one box of G rows of kPfBiasBox floats,
+// rounded up to 128 bytes because a TMA tensor copy must land on a 128-byte boundary.
+__host__ __device__ __forceinline__ int pf_bias_slot_bytes(int G) { return (G * kPfBiasBox * 4 + 127) & ~127; }
+
 // Packed row of (token offset k, head j) inside a prefill tile, and back.
 __host__ __device__ __forceinline__ int pf_row_of(int fast_pack, int G, int k, int j)
 {
@@ -154,6 +160,14 @@ __device__ __forceinline__ void report(const Params &p, uint32_t bits)
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+// Bytes of dynamic shared memory this CTA was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes()
+{
+    uint32_t n;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns()

@@ -2,24 +2,25 @@
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // One work item = (request, q tile, split, KV head): 128 packed rows, i.e.
-// 128/G tokens x the G query heads that share KV head g (GQA packing, a4).
+// 128/G tokens x the G query heads that share KV head g (GQA packing).
 // Persistent CTAs (one per SM) walk the device-built item list, longest
 // items first.  Tensor memory: a 2-slot ring of S tiles (128 x 128 fp32),
 // the O accumulator (128 x 128 fp32) and the Q tile (128 x 128 bf16).
 // Warp roles:
-//   warp 0      page-gather producer (a3): block_table entries are prefetched
-//               32 groups ahead; per 16-key group two TMA boxes (d halves,
+//   warp 0      page-gather producer: block_table entries are prefetched 32
+//               groups ahead; per 16-key group two TMA boxes (d halves,
 //               128-byte swizzle) per tensor into a 2-slot K/V ring;
-//   warp 1      tensor-memory allocator and single-thread MMA issuer (a5, a9):
+//   warp 1      tensor-memory allocator and single-thread MMA issuer:
 //               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
 //               O += P V with P read from tensor memory (M128 N128 K16 x 8);
 //   warp 2      bias producer: per bias tile one fp32 TMA box of rel_logits per
 //               token (out-of-range distances read as 0) into a 2-slot ring;
-//   warps 4-7   online softmax (a8), epilogue (a10), and the next item's Q
-//               rows written into tensor memory; thread = TMEM lane = row;
-//   warps 8-11  relative bias and masks (a6, a7): for tiles that need them,
-//               write bias/scale (or -inf) into the S slot before the QK MMA
-//               accumulates onto it, so the softmax warps never touch bias.
+//   warps 4-11  online softmax in two warpgroups: warps 4-7 take keys 0-63 of
+//               every S tile, warps 8-11 keys 64-127 (thread = TMEM lane = row);
+//               each adds its half of the relative bias from the staged boxes
+//               and applies the masks, and the two halves of a row agree on
+//               the row maximum through shared memory; they also run the
+//               epilogue and write the next item's Q rows into tensor memory.
 // Row packing is token-strided per warp so that every row of a warp has the
 // same q_abs mod 4, which makes the misalignment of its bias span (relative
 // to a 16-byte TMA box start) a warp-uniform constant.
@@ -32,9 +33,9 @@ constexpr int kKvSlots = 2;
 constexpr int kSSlots = 2;
 constexpr int kBiasSlots = 2;
 constexpr int kSlotBytes = 32768;           // one K or V tile: 2 d halves x 128 rows x 128 B
-constexpr int kBiasBox = 132;               // floats per bias row box (128 + 4 for alignment)
 constexpr int kRescaleThreshold = 8;        // log2 units (factor 256)
 constexpr uint32_t kTmemCols = 512;         // S ring 2 x 128 | O 128 | Q 64 (bf16 pairs)
+constexpr int kSoftmaxWarps = 8;            // two warpgroups, one half of the keys each
 
 // Instruction descriptor, kind::f16: D f32, A bf16, B bf16, M 128, N 128.
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -108,15 +109,15 @@ struct PfShared {
     uint64_t kv_full[kKvSlots], kv_empty[kKvSlots];
     uint64_t bias_full[kBiasSlots], bias_empty[kBiasSlots];
     uint64_t q_full;
-    uint64_t s_init[kSSlots], s_full[kSSlots], p_full[kSSlots], pv_done[kSSlots];
+    uint64_t s_full[kSSlots], p_full[kSSlots], pv_done[kSSlots];
     uint64_t o_full;
+    uint64_t xbar[4][2];      // row-half exchange between warps w and w + 4 (per lane quarter, 2 buffers)
     int32_t tile_keys[4][8];  // producer's record of recent tiles' key coordinates (reused by V)
     uint32_t tmem_base;
     int abort;
-    // Tiles (CTA-wide sequence numbers) whose PV product has completed: published by the
-    // softmax warpgroup, which observes every tile's pv_done phase in order.
-    uint32_t pv_seen;
+    float xchg[2][2][kTileRows];  // [buffer][key half][row]: partial row maxima, then row sums
 };
+static_assert(sizeof(PfShared) <= kPfSharedBytes, "prefill bookkeeping exceeds its shared-memory budget");
 
 // Everything a role needs to know about one work item; every role computes
 // it from the item with the same code.
@@ -166,28 +167,6 @@ __device__ __forceinline__ bool pf_tile_mask(const PfItem &it, int n)
     return j0 < it.lo_max || j0 + kTileKeys - 1 > it.hi_min;
 }
 
-// Bounded wait until a shared counter written with release semantics reaches `target`.
-__device__ __forceinline__ bool wait_counter(uint32_t *ctr, uint32_t target, volatile int *abort, const Params &p)
-{
-    auto load = [&]() {
-        uint32_t v;
-        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ctr)) : "memory");
-        return v;
-    };
-    if ((int32_t)(load() - target) >= 0) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        __nanosleep(64);
-        if ((int32_t)(load() - target) >= 0) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            report(p, INK_DEVERR_TIMEOUT);
-            *abort = 1;
-            return false;
-        }
-    }
-}
-
 // Row L of the tile -> (token offset k, head j); false when the row is padding.
 __device__ __forceinline__ bool pf_row(const Params &p, int L, int &k, int &j)
 {
@@ -202,33 +181,28 @@ __device__ __forceinline__ bool pf_row(const Params &p, int L, int &k, int &j)
     return k < p.tpt;
 }
 
-__device__ __forceinline__ int pf_bias_slot_bytes(const Params &p)
-{
-    return ((p.G * kBiasBox * 4) + 127) & ~127;
-}
-
 // Item of round r for this CTA: snake order over the cost-sorted list.
 __device__ __forceinline__ int pf_item_index(int r)
 {
     return r * gridDim.x + ((r & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x);
 }
 
-// Bias of one row for 128 keys starting at j0, read from its TMA box:
-// v[c] = box[O + 127 - c] where O = (q_abs - j0 - 127) mod 4 is a compile-time
-// constant here.  33 aligned 16-byte loads cover the 132-float box.
+// One key half (64 columns) of a row's relative bias, added to its raw scores:
+// s[c] += inv_scale * box[O + 63 - c], where box starts at the half's first
+// 16-byte chunk and O = (q_abs - j0 - 127) mod 4 is a compile-time constant
+// here.  17 aligned 16-byte loads cover the 68 floats the half needs.
 template <int O>
-__device__ __forceinline__ void bias_from_box(const float *box, float (&v)[128])
+__device__ __forceinline__ void bias_add(const float *box, float inv_scale, uint32_t (&s)[64])
 {
     const float4 *b4 = reinterpret_cast<const float4 *>(box);
 #pragma unroll
-    for (int m = 0; m < 33; ++m) {
+    for (int m = 0; m < 17; ++m) {
         const float4 f = b4[m];
         const float e[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int idx = 4 * m + u;
-            const int c = O + 127 - idx;
-            if (c >= 0 && c < 128) v[c] = e[u];
+            const int c = O + 63 - (4 * m + u);
+            if (c >= 0 && c < 64) s[c] = __float_as_uint(fmaf(e[u], inv_scale, __uint_as_float(s[c])));
         }
     }
 }
@@ -240,13 +214,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     uint8_t *kv_smem = base;                                  // 2 x 32 KB
-    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // 2 x (tpt x slot)
-    const int bias_slot = pf_bias_slot_bytes(p);
+    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // 2 x (tpt x G boxes)
+    const int bias_slot = pf_bias_slot_bytes(p.G);
     const int bias_stage = p.tpt * bias_slot;
     PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + kBiasSlots * bias_stage);
     volatile int *abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The host requests at most the per-CTA limit, which leaves less than 1 KB for aligning
+    // the base when G = 1; if the window is too small after alignment, do nothing (CTA-uniform).
+    if ((uintptr_t)(reinterpret_cast<uint8_t *>(&sh + 1) - dsmem) > dynamic_smem_bytes()) {
+        if (threadIdx.x == 0) report(p, INK_DEVERR_SMEM);
+        return;
+    }
     const int total = (int)*(volatile uint32_t *)&p.hdr->pf_count;
 
     if (threadIdx.x == 0) {
@@ -256,18 +236,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int s = 0; s < kBiasSlots; ++s) {
             mbar_init(&sh.bias_full[s], 1);
-            mbar_init(&sh.bias_empty[s], 4);
+            mbar_init(&sh.bias_empty[s], kSoftmaxWarps);
         }
-        mbar_init(&sh.q_full, 4);
+        mbar_init(&sh.q_full, kSoftmaxWarps);
         for (int s = 0; s < kSSlots; ++s) {
-            mbar_init(&sh.s_init[s], 4);
             mbar_init(&sh.s_full[s], 1);
-            mbar_init(&sh.p_full[s], 4);
+            mbar_init(&sh.p_full[s], kSoftmaxWarps);
             mbar_init(&sh.pv_done[s], 1);
         }
         mbar_init(&sh.o_full, 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&sh.xbar[q][0], 2);
+            mbar_init(&sh.xbar[q][1], 2);
+        }
         sh.abort = 0;
-        sh.pv_seen = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -363,14 +345,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int bs = bseq % kBiasSlots;
                     if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) break;
                     const int j0 = pf_tile_key0(it, n);
-                    if (lane == 0) mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)it.ntok * p.G * kBiasBox * 4);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)it.ntok * p.G * kPfBiasBox * 4);
                     __syncwarp();
                     for (int k = lane; k < it.ntok; k += 32) {
                         const int qa = it.qa_min + k;
                         const int start = qa - j0 - (kTileKeys - 1);
                         const int x0 = start >= 0 ? (start & ~3) : -(((-start) + 3) & ~3);
-                        tma_load_3d_hint(bias_smem + bs * bias_stage + k * bias_slot, &tm_bias, x0, it.g * p.G,
-                                         it.t0 + it.i0 + k, &sh.bias_full[bs], pol_bias);
+                        tma_load_3d_hint(bias_smem + bs * bias_stage + k * bias_slot, &tm_bias, x0,
+                                         it.g * p.G, it.t0 + it.i0 + k, &sh.bias_full[bs], pol_bias);
                     }
                     __syncwarp();
                     ++bseq;
@@ -384,7 +367,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         uint32_t seq = 0, tc = 0, qseq = 0;
-        uint32_t init_cnt[kSSlots] = {0, 0};  // s_init phases seen per S slot (only tiles with bias/masks)
         for (int r = 0;; ++r) {
             const int idx = pf_item_index(r);
             if (idx >= total || *abort) break;
@@ -436,20 +418,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int ss = t % kSSlots;
                 const int slot = seq % kKvSlots;
                 if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
-                const bool init = pf_tile_bias(p, it, n) || pf_tile_mask(it, n);
-                if (init) {
-                    if (!mbar_wait_warp(&sh.s_init[ss], init_cnt[ss] & 1, abort, p)) { ok = false; break; }
-                    ++init_cnt[ss];
-                }
                 zero_tail(slot, n);
                 tc_fence_after();
                 if (lane == 0) {
+                    // S slot ss was last read by PV(t - 2), issued earlier by this thread: the
+                    // tensor core runs them in order
                     const uint32_t kaddr = smem_u32(kv_smem + slot * kSlotBytes);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                         const uint64_t bdesc = smem_desc(kaddr + off, 16, 1024);
-                        mma_ts(tmem + ss * 128, tmem_q + kk * 8, bdesc, kIdescQK, (init || kk > 0) ? 1u : 0u);
+                        mma_ts(tmem + ss * 128, tmem_q + kk * 8, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&sh.s_full[ss]);
                     mma_commit(&sh.kv_empty[slot]);
@@ -465,31 +444,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ++qseq;
             if (!ok) break;
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4) {
         // ---------------------------------------------------------------- softmax + epilogue + Q
-        const int L = (warp - 4) * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
+        const int h = (warp >= 8) ? 1 : 0;   // key half: columns 64h .. 64h + 63 of every S tile
+        const int quarter = warp & 3;        // TMEM lanes 32 * quarter .. + 31
+        const int L = quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const float sl2 = p.scale_log2;
+        const float inv_scale = p.inv_scale;
         const float ln2 = 0.6931471805599453f;
-        // Q rows of an item into tensor memory (bf16 pairs along d), then signal the MMA warp.
+        // Q rows of an item into tensor memory (this half's 64 dims as bf16 pairs), then signal the MMA warp.
         auto write_q = [&](const PfItem &it) {
             int k, j;
             const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
-            uint32_t qv[64];
+            uint32_t qv[32];
             if (row_ok) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.q + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * kHeadDim);
+                    p.q + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * kHeadDim + 64 * h);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     const uint4 v = __ldg(src + c);
                     qv[4 * c] = v.x; qv[4 * c + 1] = v.y; qv[4 * c + 2] = v.z; qv[4 * c + 3] = v.w;
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) qv[c] = 0u;
+                for (int c = 0; c < 32; ++c) qv[c] = 0u;
             }
-            INK_TMEM_ST32(tmem_q + lane_addr + 0, (qv + 0));
-            INK_TMEM_ST32(tmem_q + lane_addr + 32, (qv + 32));
+            INK_TMEM_ST32(tmem_q + lane_addr + 32 * h, qv);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -504,52 +485,105 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (nx.ntiles > 0) return true;
             }
         };
+        // The two warps that share this lane quarter (w and w + 4) swap one float per row.
+        // Buffer b is reused two exchanges later, after the partner has read it.
+        uint32_t xseq = 0;
+        auto exchange = [&](float mine, float &theirs) {
+            const int b = xseq & 1;
+            sh.xchg[b][h][L] = mine;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.xbar[quarter][b]);
+            const bool ok = mbar_wait_warp(&sh.xbar[quarter][b], (xseq >> 1) & 1, abort, p);
+            tc_fence_after();
+            theirs = sh.xchg[b][h ^ 1][L];
+            ++xseq;
+            return ok;
+        };
         {
             PfItem first;
             if (next_with_tiles(-1, first)) write_q(first);
         }
-        uint32_t tc = 0, oseq = 0;
+        uint32_t tc = 0, oseq = 0, bseq = 0;
         for (int r = 0;; ++r) {
             const int idx = pf_item_index(r);
             if (idx >= total || *abort) break;
             const PfItem it = pf_item(p, p.pf_items[idx]);
             int k, j;
             const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
+            const int qa = it.qa_min + k;
+            int lo = 1, hi = 0;  // visible keys of this row inside the split (empty for padding rows)
+            if (row_ok) {
+                visible_range(qa, qa, it.Lk, p.causal, p.wl, p.wr, lo, hi);
+                lo = max(lo, it.gb * kKeyGroup);
+                hi = min(hi, it.ge * kKeyGroup - 1);
+            }
+            // misalignment of the bias span inside its box; tiles start at multiples of 16 keys
+            const int bo = (qa - (kTileKeys - 1)) & 3;
+            const float *box_row = reinterpret_cast<const float *>(bias_smem + k * bias_slot) +
+                                   j * kPfBiasBox + 64 * (1 - h);
+            const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
             float m_used = -INFINITY;  // raw-score units
-            float l = 0.f;
+            float l = 0.f;             // this half's share of the row sum
             bool ok = true;
             for (int n = 0; n < it.ntiles; ++n) {
                 const uint32_t t = tc + n;
                 const int ss = t % kSSlots;
+                const int j0 = pf_tile_key0(it, n) + 64 * h;  // first key of this half
                 if (!mbar_wait_warp(&sh.s_full[ss], (t / kSSlots) & 1, abort, p)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sv[128];
-                const uint32_t sa = tmem + lane_addr + ss * 128;
+                uint32_t sv[64];
+                const uint32_t sa = tmem + lane_addr + ss * 128 + 64 * h;
                 INK_TMEM_LD32(sa + 0, (sv + 0));
                 INK_TMEM_LD32(sa + 32, (sv + 32));
-                INK_TMEM_LD32(sa + 64, (sv + 64));
-                INK_TMEM_LD32(sa + 96, (sv + 96));
                 tc_wait_ld();
-                // row maximum: eight independent chains, then a tree (max is exact in any order)
+                if (pf_tile_bias(p, it, n)) {
+                    if (p.bias_tma) {
+                        const int bs = bseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_full[bs], (bseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
+                        if (row_ok) {
+                            const float *box = box_row + bs * (bias_stage / 4);
+                            switch (bo) {
+                                case 0: bias_add<0>(box, inv_scale, sv); break;
+                                case 1: bias_add<1>(box, inv_scale, sv); break;
+                                case 2: bias_add<2>(box, inv_scale, sv); break;
+                                default: bias_add<3>(box, inv_scale, sv); break;
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.bias_empty[bs]);
+                        ++bseq;
+                    } else if (row_ok) {  // rows without 16-byte alignment: direct loads
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const int rd = qa - (j0 + c);
+                            if (rd >= 0 && rd < p.E)
+                                sv[c] = __float_as_uint(fmaf(__ldg(rel_row + rd), inv_scale, __uint_as_float(sv[c])));
+                        }
+                    }
+                }
+                if (pf_tile_mask(it, n)) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = j0 + c;
+                        if (key < lo || key > hi) sv[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // this half's maximum: eight independent chains, then a tree (max is exact in any order)
                 float mxs[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mxs[e] = __uint_as_float(sv[e]);
 #pragma unroll
-                for (int c = 8; c < 128; c += 8) {
+                for (int c = 8; c < 64; c += 8) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) mxs[e] = fmaxf(mxs[e], __uint_as_float(sv[c + e]));
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                       fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-                // The PV of the previous tile (CTA-wide) is observed exactly once per tile, here or below.
-                bool pv_prev_seen = (t == 0);
-                auto see_prev_pv = [&]() {
-                    if (pv_prev_seen) return true;
-                    const uint32_t tp = t - 1;
-                    if (!mbar_wait_warp(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) return false;
-                    pv_prev_seen = true;
-                    return true;
-                };
+                float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+                // Both halves now hold their S values in registers, so either may overwrite the slot.
+                float mx_other;
+                if (!exchange(mx, mx_other)) { ok = false; break; }
+                mx = fmaxf(mx, mx_other);  // the row maximum, identical in both halves
                 // The running maximum moves only when it grows past the threshold (or was -inf).
                 float alpha = 1.f;
                 bool scale_o = false;
@@ -560,45 +594,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     m_used = mx;
                 }
                 // The decision is per row, but tcgen05.ld/st are warp-collective: the warp
-                // rescales its 32 O rows together, by 1 in the rows that keep their maximum.
+                // rescales its 32 rows together (its 64 O columns), by 1 where the maximum stayed.
                 if (__any_sync(0xffffffffu, scale_o)) {
-                    // O holds tiles 0..n-1 once PV(n-1) is done: rescale it in place
-                    if (!see_prev_pv()) { ok = false; break; }
+                    // O holds tiles 0..n-1 once PV(t - 1) is done.  S(t) being complete means every
+                    // MMA issued before QK(t) is, so PV(t - 1) is the only one that may be pending
+                    // and its phase is the only one of this barrier that can be outstanding.
+                    const uint32_t tp = t - 1;
+                    if (!mbar_wait_warp(&sh.pv_done[tp % kSSlots], (tp / kSSlots) & 1, abort, p)) { ok = false; break; }
                     tc_fence_after();
                     const float a = scale_o ? alpha : 1.f;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
+                    for (int cc = 0; cc < 2; ++cc) {
                         uint32_t ov[32];
-                        INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
+                        INK_TMEM_LD32(tmem_o + lane_addr + 64 * h + cc * 32, ov);
                         tc_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * a);
-                        INK_TMEM_ST32(tmem_o + lane_addr + cc * 32, ov);
+                        INK_TMEM_ST32(tmem_o + lane_addr + 64 * h + cc * 32, ov);
                     }
                 }
                 const float moff = (m_used == -INFINITY) ? 0.f : m_used * sl2;
-                uint32_t pk[64];
+                uint32_t pk[32];
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -moff));
                     const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -moff));
                     ls[c & 3] += p0 + p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                INK_TMEM_ST32(sa + 0, (pk + 0));
-                INK_TMEM_ST32(sa + 32, (pk + 32));
+                // P of keys 64h .. 64h + 63 as bf16 pairs: columns 32h .. 32h + 31 of the slot
+                INK_TMEM_ST32(tmem + lane_addr + ss * 128 + 32 * h, pk);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.p_full[ss]);
-                // keep in step with the PV completions and publish them for the bias warpgroup
-                if (!see_prev_pv()) { ok = false; break; }
-                if (warp == 4 && lane == 0 && t > 0) {
-                    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&sh.pv_seen)), "r"(t)
-                                 : "memory");
-                }
             }
             if (!ok) break;
             if (it.ntiles > 0) {
@@ -606,12 +637,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 PfItem nx;
                 if (next_with_tiles(r, nx)) write_q(nx);
             }
-            // epilogue
+            // epilogue: the row sum is the sum of the two halves' shares
             if (it.ntiles > 0) {
                 if (!mbar_wait_warp(&sh.o_full, oseq & 1, abort, p)) break;
                 ++oseq;
                 tc_fence_after();
             }
+            float l_other;
+            if (!exchange(l, l_other)) break;
+            l += l_other;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse = l > 0.f ? (m_used * sl2 + __log2f(l)) * ln2 : -INFINITY;
             const size_t row = (size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j;
@@ -622,10 +656,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 prow = ((size_t)(__ldg(p.unit_off + it.b) + it.qt) * p.S_pf + it.s) * ((size_t)p.Hkv * kTileRows) +
                        (size_t)it.g * kTileRows + L;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int d0 = 64 * h + 32 * cc;  // first of the 32 dims handled here
                 uint32_t ov[32];
                 if (it.ntiles > 0) {
-                    INK_TMEM_LD32(tmem_o + lane_addr + cc * 32, ov);
+                    INK_TMEM_LD32(tmem_o + lane_addr + d0, ov);
                     tc_wait_ld();
                 } else {
 #pragma unroll
@@ -633,7 +668,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 if (row_ok) {
                     if (final_out) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim + cc * 32);
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kHeadDim + d0);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 w;
@@ -644,7 +679,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             dst[q4] = w;
                         }
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(p.part_pf_o + prow * kHeadDim + cc * 32);
+                        float4 *dst = reinterpret_cast<float4 *>(p.part_pf_o + prow * kHeadDim + d0);
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
                             dst[q4] = make_float4(__uint_as_float(ov[4 * q4]) * inv, __uint_as_float(ov[4 * q4 + 1]) * inv,
@@ -652,7 +687,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                 }
             }
-            if (row_ok) {
+            if (row_ok && h == 0) {
                 if (final_out) {
                     if (p.lse) p.lse[row] = lse;
                 } else {
@@ -660,90 +695,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
             }
             tc_fence_before();
-            tc += it.ntiles;
-        }
-    } else if (warp >= 8) {
-        // ---------------------------------------------------------------- bias + masks
-        const int L = (warp - 8) * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)((warp - 8) * 32) << 16;
-        const float inv_scale = p.inv_scale;
-        uint32_t tc = 0, bseq = 0;
-        for (int r = 0;; ++r) {
-            const int idx = pf_item_index(r);
-            if (idx >= total || *abort) break;
-            const PfItem it = pf_item(p, p.pf_items[idx]);
-            int k, j;
-            const bool row_ok = pf_row(p, L, k, j) && k < it.ntok;
-            const int qa = it.qa_min + k;
-            int lo = 1, hi = 0;
-            if (row_ok) {
-                visible_range(qa, qa, it.Lk, p.causal, p.wl, p.wr, lo, hi);
-                lo = max(lo, it.gb * kKeyGroup);
-                hi = min(hi, it.ge * kKeyGroup - 1);
-            }
-            const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
-            bool ok = true;
-            for (int n = 0; n < it.ntiles; ++n) {
-                const uint32_t t = tc + n;
-                const int ss = t % kSSlots;
-                const bool has_bias = pf_tile_bias(p, it, n);
-                const bool has_mask = pf_tile_mask(it, n);
-                if (!has_bias && !has_mask) continue;
-                const int j0 = pf_tile_key0(it, n);
-                float v[128];
-#pragma unroll
-                for (int c = 0; c < 128; ++c) v[c] = 0.f;
-                if (has_bias) {
-                    if (p.bias_tma) {
-                        const int bs = bseq % kBiasSlots;
-                        if (!mbar_wait_warp(&sh.bias_full[bs], (bseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
-                        if (row_ok) {
-                            const float *box =
-                                reinterpret_cast<const float *>(bias_smem + bs * bias_stage + k * bias_slot) + j * kBiasBox;
-                            const int o = (qa - j0 - (kTileKeys - 1)) & 3;
-                            switch (o) {
-                                case 0: bias_from_box<0>(box, v); break;
-                                case 1: bias_from_box<1>(box, v); break;
-                                case 2: bias_from_box<2>(box, v); break;
-                                default: bias_from_box<3>(box, v); break;
-                            }
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sh.bias_empty[bs]);
-                        ++bseq;
-                    } else if (row_ok) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c) {
-                            const int rd = qa - (j0 + c);
-                            v[c] = (rd >= 0 && rd < p.E) ? __ldg(rel_row + rd) : 0.f;
-                        }
-                    }
-                }
-                // the S slot is free once the PV of the tile that used it before (t - 2) is done,
-                // i.e. once PV completions through tile t - 2 have been published (pv_seen >= t - 1)
-                if (t >= kSSlots && !__all_sync(0xffffffffu, wait_counter(&sh.pv_seen, t - kSSlots + 1, abort, p))) {
-                    ok = false;
-                    break;
-                }
-                uint32_t w[128];
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = j0 + c;
-                    const bool vis = key >= lo && key <= hi;
-                    w[c] = __float_as_uint(vis ? v[c] * inv_scale : -INFINITY);
-                }
-                tc_fence_after();
-                const uint32_t sa = tmem + lane_addr + ss * 128;
-                INK_TMEM_ST32(sa + 0, (w + 0));
-                INK_TMEM_ST32(sa + 32, (w + 32));
-                INK_TMEM_ST32(sa + 64, (w + 64));
-                INK_TMEM_ST32(sa + 96, (w + 96));
-                tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.s_init[ss]);
-            }
-            if (!ok) break;
             tc += it.ntiles;
         }
     }
