@@ -74,7 +74,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 struct Plan {
-    int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0;
+    int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0, bias_tok_log2 = 0;
     int S_dec = 1, S_pf = 1, chunk_dec = 1, chunk_pf = 1;
     int dec_rows = 0, lq_dec = 0;
     long long dec_cap = 0, pf_cap = 0, units_cap = 0;
@@ -144,6 +144,15 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     const int T = d->num_tokens, B = d->batch, H = d->num_heads, Hkv = d->num_kv_heads;
     pl.G = H / Hkv;
     pl.tpt = kTileRows / pl.G;
+    // prefill bias boxes: as many tokens per box (up to 8) as the shared-memory budget allows
+    for (int lg = 3; lg >= 0; --lg) {
+        if ((1 << lg) > pl.tpt) continue;
+        const size_t need = 1024 + 2 * 32768 + 2 * (size_t)pf_bias_stage_bytes(pl.G, pl.tpt, 1 << lg) + kPfSharedBytes;
+        if (need <= kSmemLimit || lg == 0) {
+            pl.bias_tok_log2 = lg;
+            break;
+        }
+    }
     pl.fast_pack = (32 % pl.G == 0) ? 1 : 0;
     pl.decode_kernel = (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
     const long long msq = std::min<long long>(max_seqlen_q, std::max(T, 1));
@@ -329,6 +338,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     p.chunk_pf = pl.chunk_pf;
     p.tpt = pl.tpt;
     p.fast_pack = pl.fast_pack;
+    p.bias_tok_log2 = pl.bias_tok_log2;
 
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
     alignas(64) CUtensorMap tm_k, tm_v, tm_bdec, tm_bpf;
@@ -353,7 +363,8 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
             bias_dec_tma = encode(&tm_bdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box,
                                   CU_TENSOR_MAP_SWIZZLE_NONE);
         }
-        const cuuint32_t box2[3] = {(cuuint32_t)kPfBiasBox, (cuuint32_t)pl.G, 1};
+        const cuuint32_t box2[3] = {(cuuint32_t)pf_bias_width(1 << pl.bias_tok_log2), (cuuint32_t)pl.G,
+                                    (cuuint32_t)(1 << pl.bias_tok_log2)};
         bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
                              CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -387,7 +398,8 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         Params pp = p;
         pp.bias_tma = bias_pf_tma ? 1 : 0;
         // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
-        const size_t layout = 2 * 32768 + 2 * (size_t)pl.tpt * pf_bias_slot_bytes(pl.G) + kPfSharedBytes;
+        const size_t layout =
+            2 * 32768 + 2 * (size_t)pf_bias_stage_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2) + kPfSharedBytes;
         if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);

@@ -17,7 +17,6 @@ constexpr int kKeyGroup = 16;     // keys per TMA box / per decode stage
 constexpr int kTileKeys = 128;    // keys per prefill KV tile (8 groups)
 constexpr int kTileRows = 128;    // packed (token, head) rows per prefill tile
 constexpr int kDecodeRows = 16;   // packed rows per KV head in the decode kernel
-constexpr int kPfBiasBox = 132;   // floats per prefill bias box row (128 keys + 4 for 16-byte alignment)
 constexpr int kPfSharedBytes = 2560;  // prefill barriers and bookkeeping (upper bound)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits give up after ~2 s
 constexpr uint32_t kWaitHintNs = 100000;           // longest single suspension of a wait (100 us)
@@ -69,6 +68,7 @@ struct Params {
     int tpt;             // prefill tokens per 128-row tile (128 / G)
     int fast_pack;       // prefill: warp-strided token packing (G divides 32)
     int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
+    int bias_tok_log2;   // prefill: tokens per bias TMA box = 1 << bias_tok_log2
 };
 
 // ---------------------------------------------------------------------------
@@ -139,9 +139,19 @@ __host__ __device__ __forceinline__ UnitSplit unit_split(int qa0, int qa1, int L
     return u;
 }
 
-// Bytes per token in a prefill bias stage: one box of G rows of kPfBiasBox floats,
-// rounded up to 128 bytes because a TMA tensor copy must land on a 128-byte boundary.
-__host__ __device__ __forceinline__ int pf_bias_slot_bytes(int G) { return (G * kPfBiasBox * 4 + 127) & ~127; }
+// Prefill bias staging.  One TMA box holds the rel_logits rows of nb consecutive tokens
+// (all G heads) for one 128-key tile.  The distance span of token k + 1 starts one key
+// later than token k's, so a common start rounded down to 16 bytes and a width of
+// 128 + 3 + (nb - 1) floats, rounded up to 16 bytes, cover every token of the box.
+__host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (131 + nb + 3) & ~3; }
+// Bytes a box transfers, and its shared-memory footprint (a TMA destination is 128-byte aligned).
+__host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb) { return nb * G * pf_bias_width(nb) * 4; }
+__host__ __device__ __forceinline__ int pf_bias_box_stride(int G, int nb) { return (pf_bias_box_bytes(G, nb) + 127) & ~127; }
+// One stage: the boxes of a q tile of tpt tokens.
+__host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int nb)
+{
+    return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb);
+}
 
 // Packed row of (token offset k, head j) inside a prefill tile, and back.
 __host__ __device__ __forceinline__ int pf_row_of(int fast_pack, int G, int k, int j)

@@ -215,8 +215,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     uint8_t *kv_smem = base;                                  // 2 x 32 KB
     uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // 2 x (tpt x G boxes)
-    const int bias_slot = pf_bias_slot_bytes(p.G);
-    const int bias_stage = p.tpt * bias_slot;
+    const int bias_nb = 1 << p.bias_tok_log2;  // tokens per bias box
+    const int bias_w = pf_bias_width(bias_nb);   // floats per box row
+    const int bias_box = pf_bias_box_stride(p.G, bias_nb);
+    const int bias_stage = pf_bias_stage_bytes(p.G, p.tpt, bias_nb);
     PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + kBiasSlots * bias_stage);
     volatile int *abort = &sh.abort;
 
@@ -345,15 +347,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int bs = bseq % kBiasSlots;
                     if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) break;
                     const int j0 = pf_tile_key0(it, n);
+                    const int nbox = (it.ntok + bias_nb - 1) >> p.bias_tok_log2;
                     if (lane == 0)
-                        mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)it.ntok * p.G * kPfBiasBox * 4);
+                        mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)(nbox * pf_bias_box_bytes(p.G, bias_nb)));
                     __syncwarp();
-                    for (int k = lane; k < it.ntok; k += 32) {
-                        const int qa = it.qa_min + k;
-                        const int start = qa - j0 - (kTileKeys - 1);
-                        const int x0 = start >= 0 ? (start & ~3) : -(((-start) + 3) & ~3);
-                        tma_load_3d_hint(bias_smem + bs * bias_stage + k * bias_slot, &tm_bias, x0,
-                                         it.g * p.G, it.t0 + it.i0 + k, &sh.bias_full[bs], pol_bias);
+                    for (int b = lane; b < nbox; b += 32) {
+                        const int k0 = b << p.bias_tok_log2;
+                        // distance span of token k0: from q_abs - (j0 + 127) up; rounded down to 16 bytes
+                        const int x0 = (it.qa_min + k0 - j0 - (kTileKeys - 1)) & ~3;
+                        tma_load_3d_hint(bias_smem + bs * bias_stage + b * bias_box, &tm_bias, x0, it.g * p.G,
+                                         it.t0 + it.i0 + k0, &sh.bias_full[bs], pol_bias);
                     }
                     __syncwarp();
                     ++bseq;
@@ -518,10 +521,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 lo = max(lo, it.gb * kKeyGroup);
                 hi = min(hi, it.ge * kKeyGroup - 1);
             }
-            // misalignment of the bias span inside its box; tiles start at multiples of 16 keys
-            const int bo = (qa - (kTileKeys - 1)) & 3;
-            const float *box_row = reinterpret_cast<const float *>(bias_smem + k * bias_slot) +
-                                   j * kPfBiasBox + 64 * (1 - h);
+            // This row's bias span inside its box: it starts ko floats after the box start
+            // (tiles start at multiples of 16 keys, so ko is the same for every tile); the
+            // 16-byte chunk that holds it is read whole and the remainder bo is a compile-time
+            // shift below.  With warp-strided packing bo is the same for every row of a warp.
+            const int kb = k >> p.bias_tok_log2, ki = k & (bias_nb - 1);
+            const int ko = (qa - (kTileKeys - 1)) - ((it.qa_min + (kb << p.bias_tok_log2) - (kTileKeys - 1)) & ~3);
+            const int bo = ko & 3;
+            const float *box_row = reinterpret_cast<const float *>(bias_smem + kb * bias_box) +
+                                   (ki * p.G + j) * bias_w + 4 * (ko >> 2) + 64 * (1 - h);
             const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
             float m_used = -INFINITY;  // raw-score units
             float l = 0.f;             // this half's share of the row sum
