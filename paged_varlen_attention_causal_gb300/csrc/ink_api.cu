@@ -80,7 +80,7 @@ struct Plan {
     long long dec_cap = 0, pf_cap = 0, units_cap = 0;
     bool any_prefill = false, any_decode = false;
     // workspace offsets
-    size_t off_dec_items = 0, off_pf_items = 0, off_dec_off = 0, off_unit_off = 0;
+    size_t off_dec_items = 0, off_pf_items = 0, off_dec_off = 0, off_unit_off = 0, off_comb_off = 0;
     size_t off_pdo = 0, off_pdl = 0, off_ppo = 0, off_ppl = 0, total = 0;
 };
 
@@ -188,6 +188,7 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     pl.off_pf_items = off; off = align256(off + sizeof(int4) * (size_t)pl.pf_cap);
     pl.off_dec_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     pl.off_unit_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
+    pl.off_comb_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     const bool dec_parts = pl.any_decode && sdec_eff > 1;
     const bool pf_parts = pl.any_prefill && pl.S_pf > 1;
     const size_t dec_rows_total = dec_parts ? (size_t)pl.dec_cap * pl.dec_rows : 0;
@@ -326,6 +327,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     p.pf_items_cap = (int)pl.pf_cap;
     p.dec_off = reinterpret_cast<int *>(ws + pl.off_dec_off);
     p.unit_off = reinterpret_cast<int *>(ws + pl.off_unit_off);
+    p.comb_off = reinterpret_cast<int *>(ws + pl.off_comb_off);
     p.part_dec_lse = reinterpret_cast<float *>(ws + pl.off_pdl);
     p.part_dec_o = reinterpret_cast<float *>(ws + pl.off_pdo);
     p.dec_rows = pl.dec_rows;

@@ -11,6 +11,8 @@
 // kWarpsPerRow warps share one row (warp w takes splits w, w + kWarpsPerRow, ...)
 // and merge their states through shared memory; lane l owns d values
 // 4l..4l+3.  Loads are issued kBatch splits at a time.
+#include <algorithm>
+
 #include "ink_common.cuh"
 
 namespace ink {
@@ -24,15 +26,24 @@ struct RowPartials {
     int nact;
 };
 
-// Locate the partials of row (t, h); false when the row needs no merge.
-__device__ __forceinline__ bool row_partials(const Params &p, int t, int h, RowPartials &rp)
+// Row r of the merge list: token c = r / H of the list (request b, token t) and head h.
+// The prepass lists, per request, every token of a request that was split.
+__device__ __forceinline__ void list_row(const Params &p, long long r, int &b, int &t, int &h)
 {
-    int lo = 0, hi = p.B - 1;  // request owning token t: first b with cu[b+1] > t
+    const int c = (int)(r / p.H);
+    h = (int)(r % p.H);
+    int lo = 0, hi = p.B - 1;  // request owning list token c: last b with comb_off[b] <= c
     while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.cu + mid + 1) > t) hi = mid; else lo = mid + 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.comb_off + mid) <= c) lo = mid; else hi = mid - 1;
     }
-    const int b = lo;
+    b = lo;
+    t = __ldg(p.cu + b) + (c - __ldg(p.comb_off + b));
+}
+
+// Locate the partials of row (t, h) of request b; false when the row needs no merge.
+__device__ __forceinline__ bool row_partials(const Params &p, int b, int t, int h, RowPartials &rp)
+{
     const Req r = load_req(p, b);
     if (!r.ok || t < r.t0 || t >= r.t0 + r.Lq) return false;
     const int i = t - r.t0;
@@ -69,92 +80,104 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
     __shared__ float4 s_acc[kWarpsPerRow > 1 ? kCombineThreads / 32 : 1][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = warp % kWarpsPerRow;  // this warp's share of the row's splits
-    const long long row = (long long)blockIdx.x * kRowsPerCta + warp / kWarpsPerRow;
-    RowPartials rp;
-    bool active = row < (long long)p.T * p.H;
-    if (active) active = row_partials(p, (int)(row / p.H), (int)(row % p.H), rp);
-    if (kWarpsPerRow == 1 && !active) return;
-
-    float m = -INFINITY, l = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) {
-        for (int s0 = sub; s0 < rp.nact; s0 += kWarpsPerRow * kBatch) {
-            float ls[kBatch];
-            float4 os[kBatch];
+    const long long nrows = (long long)*(volatile uint32_t *)&p.hdr->comb_tokens * p.H;
+    // Grid-stride over the merge list; the trip count is the same for all warps of a CTA.
+    for (long long row0 = (long long)blockIdx.x * kRowsPerCta; row0 < nrows; row0 += (long long)gridDim.x * kRowsPerCta) {
+        const long long row = row0 + warp / kWarpsPerRow;
+        RowPartials rp;
+        int b = 0, t = 0, h = 0;
+        bool active = row < nrows;
+        if (active) {
+            list_row(p, row, b, t, h);
+            active = row_partials(p, b, t, h, rp);
+        }
+        float m = -INFINITY, l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active) {
+            for (int s0 = sub; s0 < rp.nact; s0 += kWarpsPerRow * kBatch) {
+                float ls[kBatch];
+                float4 os[kBatch];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {  // issue the batch's loads before using any of them
-                const int s = s0 + u * kWarpsPerRow;
-                ls[u] = -INFINITY;
-                os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (s < rp.nact) {
-                    const size_t pr = rp.first + (size_t)s * rp.stride;
-                    ls[u] = __ldg(rp.pl + pr);
-                    os[u] = __ldg(reinterpret_cast<const float4 *>(rp.po + pr * kHeadDim) + lane);
+                for (int u = 0; u < kBatch; ++u) {  // issue the batch's loads before using any of them
+                    const int s = s0 + u * kWarpsPerRow;
+                    ls[u] = -INFINITY;
+                    os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (s < rp.nact) {
+                        const size_t pr = rp.first + (size_t)s * rp.stride;
+                        ls[u] = __ldg(rp.pl + pr);
+                        os[u] = __ldg(reinterpret_cast<const float4 *>(rp.po + pr * kHeadDim) + lane);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (ls[u] == -INFINITY) continue;
+                    if (ls[u] > m) {
+                        const float a = __expf(m - ls[u]);  // m = -inf gives 0
+                        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+                        l *= a;
+                        m = ls[u];
+                    }
+                    const float w = __expf(ls[u] - m);
+                    l += w;
+                    acc.x = fmaf(w, os[u].x, acc.x);
+                    acc.y = fmaf(w, os[u].y, acc.y);
+                    acc.z = fmaf(w, os[u].z, acc.z);
+                    acc.w = fmaf(w, os[u].w, acc.w);
                 }
             }
+        }
+        if (kWarpsPerRow > 1) {
+            if (lane == 0) {
+                s_m[warp] = m;
+                s_l[warp] = l;
+            }
+            s_acc[warp][lane] = acc;
+            __syncthreads();
+            if (active && sub == 0) {
+                float gm = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                if (ls[u] == -INFINITY) continue;
-                if (ls[u] > m) {
-                    const float a = __expf(m - ls[u]);  // m = -inf gives 0
-                    acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
-                    l *= a;
-                    m = ls[u];
+                for (int w = 0; w < kWarpsPerRow; ++w) gm = fmaxf(gm, s_m[warp + w]);
+                l = 0.f;
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gm != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < kWarpsPerRow; ++w) {
+                        if (s_m[warp + w] == -INFINITY) continue;
+                        const float a = __expf(s_m[warp + w] - gm);
+                        const float4 v = s_acc[warp + w][lane];
+                        l = fmaf(a, s_l[warp + w], l);
+                        acc.x = fmaf(a, v.x, acc.x);
+                        acc.y = fmaf(a, v.y, acc.y);
+                        acc.z = fmaf(a, v.z, acc.z);
+                        acc.w = fmaf(a, v.w, acc.w);
+                    }
                 }
-                const float w = __expf(ls[u] - m);
-                l += w;
-                acc.x = fmaf(w, os[u].x, acc.x);
-                acc.y = fmaf(w, os[u].y, acc.y);
-                acc.z = fmaf(w, os[u].z, acc.z);
-                acc.w = fmaf(w, os[u].w, acc.w);
+                m = gm;
             }
+            __syncthreads();  // s_* are rewritten by the next row
+            if (sub != 0) continue;
         }
+        if (!active) continue;
+        const size_t orow = (size_t)t * p.H + h;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint2 outv;
+        outv.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        outv.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + orow * kHeadDim + 4 * lane) = outv;
+        if (p.lse && lane == 0) p.lse[orow] = l > 0.f ? m + __logf(l) : -INFINITY;
     }
-    if (kWarpsPerRow > 1) {
-        if (lane == 0) {
-            s_m[warp] = m;
-            s_l[warp] = l;
-        }
-        s_acc[warp][lane] = acc;
-        __syncthreads();
-        if (!active || sub != 0) return;
-        float gm = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarpsPerRow; ++w) gm = fmaxf(gm, s_m[warp + w]);
-        l = 0.f;
-        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (gm != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarpsPerRow; ++w) {
-                if (s_m[warp + w] == -INFINITY) continue;
-                const float a = __expf(s_m[warp + w] - gm);
-                const float4 v = s_acc[warp + w][lane];
-                l = fmaf(a, s_l[warp + w], l);
-                acc.x = fmaf(a, v.x, acc.x);
-                acc.y = fmaf(a, v.y, acc.y);
-                acc.z = fmaf(a, v.z, acc.z);
-                acc.w = fmaf(a, v.w, acc.w);
-            }
-        }
-        m = gm;
-    }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint2 outv;
-    outv.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    outv.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(p.out + (size_t)row * kHeadDim + 4 * lane) = outv;
-    if (p.lse && lane == 0) p.lse[row] = l > 0.f ? m + __logf(l) : -INFINITY;
 }
 
-// Few rows (long splits) get eight warps each; many rows get one warp each.
+// Few rows (long splits) get eight warps each; many rows get one warp each.  The grid is
+// sized for every row of the call; CTAs past the merge list the prepass wrote return at once.
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream)
 {
     const long long rows = (long long)p.T * p.H;
     if (rows * 8 <= 4ll * sms * (kCombineThreads / 32)) {
-        const long long grid = rows;
-        ink_combine_kernel<8><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
+        ink_combine_kernel<8><<<(unsigned)rows, kCombineThreads, 0, stream>>>(p);
     } else {
-        const long long grid = (rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+        const long long per = kCombineThreads / 32;
+        const long long grid = std::min<long long>((rows + per - 1) / per, 16ll * sms);
         ink_combine_kernel<1><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
     }
     return cudaGetLastError();

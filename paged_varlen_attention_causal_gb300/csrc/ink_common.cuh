@@ -31,7 +31,8 @@ struct WsHeader {
     uint32_t pf_count;     // prefill work items written by the prepass
     uint32_t dec_next;     // dynamic scheduler counter of the decode kernel
     uint32_t pf_next;      // dynamic scheduler counter of the prefill kernel
-    uint32_t pad[59];
+    uint32_t comb_tokens;  // tokens whose rows the split-KV merge visits (prepass)
+    uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 
@@ -55,6 +56,7 @@ struct Params {
     int pf_items_cap;
     int *dec_off;      // (B+1) first decode item of each request (prepass)
     int *unit_off;     // (B+1) first prefill unit (q tile) of each request (prepass)
+    int *comb_off;     // (B+1) first merge-list token of each request (prepass)
     // split partials: one block per decode item, and per (prefill unit, split)
     float *part_dec_o, *part_dec_lse;  // (dec_items_cap, dec_rows, D), (dec_items_cap, dec_rows)
     int dec_rows;                      // rows per decode block: (16 / G) * H

@@ -65,11 +65,12 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     __shared__ int warp_sums[32];
     __shared__ int bucket_count[kCostBuckets];
     __shared__ int bucket_base[kCostBuckets];
-    __shared__ int s_carry[2];
+    __shared__ int s_carry[3];
     __shared__ uint32_t s_err;
 
     int *dec_off = p.dec_off;
     int *unit_off = p.unit_off;
+    int *comb_off = p.comb_off;
     const int tid = threadIdx.x;
 
     if (tid == 0) {
@@ -78,7 +79,8 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         p.hdr->pf_count = 0;
         p.hdr->dec_next = 0;
         p.hdr->pf_next = 0;
-        s_carry[0] = s_carry[1] = 0;
+        p.hdr->comb_tokens = 0;
+        s_carry[0] = s_carry[1] = s_carry[2] = 0;
         uint32_t e = 0;
         if (__ldg(p.cu) != 0 || __ldg(p.cu + p.B) != p.T) e |= INK_DEVERR_CU_SEQLENS;
         s_err = e;
@@ -86,11 +88,12 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     for (int i = tid; i < kCostBuckets; i += blockDim.x) bucket_count[i] = 0;
     __syncthreads();
 
-    // pass 1: per request, decode split count and prefill q-tile count; scans.
+    // pass 1: per request, decode split count, prefill q-tile count and the tokens whose
+    // rows the split-KV merge must visit (all of a request's tokens once it is split); scans.
     uint32_t my_err = 0;
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + tid;
-        int ndec = 0, nq = 0;
+        int ndec = 0, nq = 0, nc = 0;
         if (b < p.B) {
             Req r = load_req(p, b);
             my_err |= r.err;
@@ -98,29 +101,36 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
                 if (is_decode_req(p, r)) {
                     UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
                     ndec = u.nact;
+                    nc = ndec > 1 ? r.Lq : 0;
                 } else {
                     nq = (r.Lq + p.tpt - 1) / p.tpt;
+                    nc = p.S_pf > 1 ? r.Lq : 0;
                 }
                 if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
             }
         }
-        int xd, xq;
+        int xd, xq, xc;
         const int td = block_exclusive_scan(ndec, &xd, warp_sums);
         const int tq = block_exclusive_scan(nq, &xq, warp_sums);
+        const int tcb = block_exclusive_scan(nc, &xc, warp_sums);
         if (b < p.B) {
             dec_off[b] = s_carry[0] + xd;
             unit_off[b] = s_carry[1] + xq;
+            comb_off[b] = s_carry[2] + xc;
         }
         __syncthreads();
         if (tid == 0) {
             s_carry[0] += td;
             s_carry[1] += tq;
+            s_carry[2] += tcb;
         }
         __syncthreads();
     }
     if (tid == 0) {
         dec_off[p.B] = s_carry[0];
         unit_off[p.B] = s_carry[1];
+        comb_off[p.B] = s_carry[2];
+        p.hdr->comb_tokens = (uint32_t)s_carry[2];
     }
     if (my_err) atomicOr(&s_err, my_err);
     __syncthreads();
@@ -129,10 +139,15 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     const int n_dec = min(s_carry[0], p.dec_items_cap);
     const int n_units = s_carry[1];
 
-    // pass 2: decode items (request, split), request order.
-    for (int b = tid; b < p.B; b += blockDim.x) {
-        const int o0 = dec_off[b], o1 = dec_off[b + 1];
-        for (int s = 0; o0 + s < o1 && o0 + s < n_dec; ++s) p.dec_items[o0 + s] = make_int2(b, s);
+    // pass 2: decode items (request, split), request order; one item per thread, so that a
+    // single long request's splits are written in parallel.
+    for (int i = tid; i < n_dec; i += blockDim.x) {
+        int lo = 0, hi = p.B - 1;  // request owning item i: last b with dec_off[b] <= i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (dec_off[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        p.dec_items[i] = make_int2(lo, i - dec_off[lo]);
     }
 
     // pass 3: prefill units -> cost histogram of their splits.
