@@ -343,8 +343,8 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     p.bias_tok_log2 = pl.bias_tok_log2;
 
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
-    alignas(64) CUtensorMap tm_k, tm_v, tm_bdec, tm_bpf;
-    memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v);
+    alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_bdec, tm_bpf;
+    memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v); memset(&tm_vp, 0, sizeof tm_vp);
     memset(&tm_bdec, 0, sizeof tm_bdec); memset(&tm_bpf, 0, sizeof tm_bpf);
     {
         const cuuint64_t gd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv,
@@ -353,6 +353,13 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         const cuuint32_t box[3] = {64, 1, (cuuint32_t)kKeyGroup};
         if (!encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, key_cache, gd, gs, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, value_cache, gd, gs, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return INK_ERR_CUDA;
+        // prefill V as (64 d, keys, d half, Hkv) with one 64 x 16 x 2 box per page: the box lands as
+        // [d half][16 keys][128 B], so a page needs one copy instead of two
+        const cuuint64_t gd4[4] = {64, (cuuint64_t)dims->num_blocks * dims->block_size, 2, (cuuint64_t)Hkv};
+        const cuuint64_t gs4[3] = {(cuuint64_t)Hkv * kHeadDim * 2, 128, (cuuint64_t)kHeadDim * 2};
+        const cuuint32_t box4[4] = {64, (cuuint32_t)kKeyGroup, 2, 1};
+        if (!encode(&tm_vp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gd4, gs4, box4, CU_TENSOR_MAP_SWIZZLE_128B))
             return INK_ERR_CUDA;
     }
     // bias maps: rel_logits as (E, H, T) fp32, no swizzle; needs 16-byte rows
@@ -406,7 +413,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);
         if (timed_launch(INK_KERNEL_PREFILL, stream,
-                         [&] { return launch_prefill(pp, tm_k, tm_v, tm_bpf, grid, smem, stream); }) != cudaSuccess)
+                         [&] { return launch_prefill(pp, tm_k, tm_vp, tm_bpf, grid, smem, stream); }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
 

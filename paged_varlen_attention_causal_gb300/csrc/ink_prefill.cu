@@ -8,8 +8,9 @@
 // the O accumulator (128 x 128 fp32) and the Q tile (128 x 128 bf16).
 // Warp roles:
 //   warp 0      page-gather producer: block_table entries are prefetched 32
-//               groups ahead; per 16-key group two TMA boxes (d halves,
-//               128-byte swizzle) per tensor into a 2-slot K/V ring;
+//               groups ahead; per 16-key page two TMA boxes of K (d halves,
+//               128-byte swizzle) and one 4-D box of V (both d halves) into
+//               a 2-slot K/V ring;
 //   warp 1      tensor-memory allocator and single-thread MMA issuer:
 //               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
 //               O += P V with P read from tensor memory (M128 N128 K16 x 8);
@@ -317,10 +318,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!mbar_wait_warp(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
                     if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
                     __syncwarp();
-                    if (lane < 16) {
+                    if (!isV && lane < 16) {
+                        // K tile: [d half][128 keys][128 B]; one box per page and d half
                         const int grp = lane & 7, dh = lane >> 3;
                         uint8_t *dst = kv_smem + slot * kSlotBytes + dh * 16384 + grp * 2048;
-                        tma_load_3d_hint(dst, isV ? &tm_v : &tm_k, dh * 64, it.g, key0, &sh.kv_full[slot], pol_kv);
+                        tma_load_3d_hint(dst, &tm_k, dh * 64, it.g, key0, &sh.kv_full[slot], pol_kv);
+                    } else if (isV && lane < 8) {
+                        // V tile: [page][d half][16 keys][128 B]; one box per page covers both halves
+                        uint8_t *dst = kv_smem + slot * kSlotBytes + lane * 4096;
+                        tma_load_4d_hint(dst, &tm_v, 0, key0, 0, it.g, &sh.kv_full[slot], pol_kv);
                     }
                     __syncwarp();
                     ++seq;
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (it.ntiles == 0) continue;
             if (!mbar_wait_warp(&sh.q_full, qseq & 1, abort, p)) break;
             const uint32_t tc0 = tc;
-            auto zero_tail = [&](int slot, int n) {
+            auto zero_tail = [&](int slot, int n, bool v_layout) {
                 // keys at or beyond Lk inside loaded groups may hold stale data: zero them
                 const int j0 = pf_tile_key0(it, n);
                 const int loaded = min(8, it.ge - (it.gb + 8 * n)) * kKeyGroup;
@@ -386,8 +392,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     uint8_t *t = kv_smem + slot * kSlotBytes;
                     for (int c = lane; c < (loaded - z0) * 16; c += 32) {  // 16 chunks of 16 B per row
                         const int row = z0 + c / 16, ch = c % 16;
-                        *reinterpret_cast<uint4 *>(t + (ch >> 3) * 16384 + row * 128 + (ch & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        const int off = v_layout ? (row >> 4) * 4096 + (ch >> 3) * 2048 + (row & 15) * 128
+                                                 : (ch >> 3) * 16384 + row * 128;
+                        *reinterpret_cast<uint4 *>(t + off + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                 }
@@ -399,13 +406,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (!mbar_wait_warp(&sh.p_full[ss], (t / kSSlots) & 1, abort, p)) return false;
                 const int slot = seq % kKvSlots;
                 if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) return false;
-                zero_tail(slot, m);
+                zero_tail(slot, m, true);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t vaddr = smem_u32(kv_smem + slot * kSlotBytes);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bdesc = smem_desc(vaddr + kk * 2048, 16384, 1024);
+                        // keys 16kk .. 16kk + 15 are page kk: d halves 2 KB apart, 8-key groups 1 KB apart
+                        const uint64_t bdesc = smem_desc(vaddr + kk * 4096, 2048, 1024);
                         mma_ts(tmem_o, tmem + ss * 128 + kk * 8, bdesc, kIdescPV, (m > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&sh.kv_empty[slot]);
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int ss = t % kSSlots;
                 const int slot = seq % kKvSlots;
                 if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
-                zero_tail(slot, n);
+                zero_tail(slot, n, false);
                 tc_fence_after();
                 if (lane == 0) {
                     // S slot ss was last read by PV(t - 2), issued earlier by this thread: the
