@@ -98,8 +98,10 @@ def test_random_small_split(seed):
     parity(case, f"random{100 + seed} splits 3", num_splits=3)
 
 
+# G = H / Hkv covers every prefill packing: warp-strided (G divides 32) and plain, and every number of
+# tokens per bias box the host picks (8: G 1-4, 6, 8, 16; 4: G 5, 7, 12, 32; 2: G 64; 1: G 128).
 @pytest.mark.parametrize("H,Hkv", [(8, 8), (16, 8), (8, 1), (16, 1), (32, 1), (64, 2), (12, 4), (48, 16),
-                                   (128, 1), (6, 2)])
+                                   (128, 1), (6, 2), (10, 2), (12, 2), (14, 2), (24, 2), (64, 1)])
 @pytest.mark.parametrize("kind", ["decode", "prefill", "mixed"])
 def test_head_layouts(H, Hkv, kind):
     if kind == "decode":
