@@ -5,10 +5,9 @@
  * The operation is the one `inkling_fa4_rel_attention` performs in vLLM's
  * fa4_rel_attention.py, as quoted and explained by the article
  * "vllm中提取Inkling FA4 Relative Attention算子基础的base优化版本"
- * (nxmr.cn/news/19446): its wrapper signature (source lines L101-L117, the
- * article's layer 3 "参数签名"), the score modification that adds the bias
- * (score_mod_rel_bias, source lines L25-L57) and the split-KV count
- * (inkling_fa4_num_splits, source lines L60-L98).  The split-KV merge
+ * (nxmr.cn/news/19446): its wrapper signature (the article's layer 3
+ * "参数签名"), the score modification that adds the bias (score_mod_rel_bias)
+ * and the split-KV count (inkling_fa4_num_splits).  The split-KV merge
  * follows the log-sum-exp Phase 2 of the "paged_attention_v2_pytorch.py"
  * page (dev.modelhub.org.cn), and the paged/varlen conventions follow the
  * mini-vllm tutorial "Step 15: FlashAttention 封装" (block_table and
@@ -99,7 +98,7 @@ INK_API size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t ma
  * the cap on splits per work unit for decode-shaped calls
  * (max_seqlen_q * H / Hkv <= 16) and for prefill-shaped calls otherwise.
  * It is re-derived for the GB300 SM count from the page's heuristic
- * (inkling_fa4_num_splits, source lines L60-L98): enough units to fill every
+ * (inkling_fa4_num_splits): enough units to fill every
  * SM several times, with at least 16 keys per split.  `max_kv_len` bounds
  * cache_seqlens.  Returns 0 for invalid dims.  Needs a current CUDA device.
  */

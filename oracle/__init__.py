@@ -104,8 +104,8 @@ def attention(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_
     """Exact (fp64) paged varlen attention with the Inkling relative bias.
 
     Follows the score definition of ``score_mod_rel_bias`` (nxmr.cn article
-    on fa4_rel_attention.py, source lines L25-L57) and the wrapper arguments
-    of ``inkling_fa4_rel_attention`` (source lines L101-L163).
+    on fa4_rel_attention.py) and the wrapper arguments of
+    ``inkling_fa4_rel_attention`` (its layer 3 "参数签名").
 
     q: (T, H, D) bf16; key_cache/value_cache: (NB, BS, Hkv, D) bf16;
     block_table: (B, MAXBLK) int32; cache_seqlens: (B,); cu_seqlens_q: (B+1,).

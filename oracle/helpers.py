@@ -11,8 +11,8 @@ from typing import Sequence
 def bucket_max_seqlen_q(max_seqlen_q: int) -> int:
     """Round the scheduling bound on query length up to a power of two.
 
-    ``bucket_max_seqlen_q`` in fa4_rel_attention.py (nxmr.cn article, source
-    lines L14-L16; layer 1 of its walk-through): one shifted left by the
+    ``bucket_max_seqlen_q`` in fa4_rel_attention.py (nxmr.cn article, layer 1
+    of its walk-through): one shifted left by the
     bit length of max(0, n - 1).  The article's example maps 45000 to 65536.
     Pinned by that example and by the closed form at 0, 1 and powers of two.
     """
@@ -23,7 +23,7 @@ def page_num_splits(*, is_local: bool, batch_size: int, max_query_len: int, num_
                     num_kv_heads: int, max_kv_len: int, capability_major: int = 10) -> int:
     """Split-KV count of ``inkling_fa4_num_splits`` as the article prints it.
 
-    nxmr.cn article, source lines L60-L98 and layer 1 steps 1-5.  The page
+    nxmr.cn article, layer 1 steps 1-5.  The page
     lost its comparison operators; the reading taken is the one that keeps
     the cap monotone in the number of KV heads per rank:
       major 9 -> 1; local attention -> 1;

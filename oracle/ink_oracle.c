@@ -13,7 +13,7 @@
  *   For token i < Lq and head h:  t = cu[b]+i,  g = h / (H/Hkv),
  *     q_abs = i + Lk - Lq                 (bottom-right causal alignment:
  *        "seqlen_local_offset = seqlen_k - seqlen_q" in score_mod_rel_bias,
- *        fa4_rel_attention.py, nxmr.cn article, source lines L25-L57)
+ *        fa4_rel_attention.py, nxmr.cn article)
  *   For key j < Lk:
  *     visible(j) = (!causal || j <= q_abs)
  *                  && (wl < 0 || j >= q_abs - wl) && (wr < 0 || j <= q_abs + wr)
@@ -259,8 +259,8 @@ static int run_rows(const oracle_args *a, const int64_t *rows, int64_t n_rows,
 
 /*
  * Paged varlen attention, fp64.  Argument order follows the wrapper
- * signature of inkling_fa4_rel_attention (nxmr.cn article, source lines
- * L101-L117), with the shape integers a C interface needs.
+ * signature of inkling_fa4_rel_attention (nxmr.cn article, layer 3
+ * "参数签名"), with the shape integers a C interface needs.
  *
  *   q           bf16 bits, (T, H, D)
  *   key_cache   bf16 bits, (NB, BS, Hkv, D); value_cache likewise

@@ -167,7 +167,7 @@ def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens
     """Paged varlen attention with the Inkling relative bias (see include/ink_attn.h).
 
     Keyword arguments follow ``inkling_fa4_rel_attention`` (fa4_rel_attention.py
-    as quoted by the nxmr.cn article, source lines L101-L163), with the window
+    as quoted by the nxmr.cn article, its wrapper signature), with the window
     passed as two integers (-1 = unbounded).  Returns ``out`` (and ``lse``
     when ``return_lse``).
     """

@@ -1,4 +1,4 @@
-// ink_api.cu -- host plan and C ABI (a1): argument validation, the split
+// ink_api.cu -- host plan and C ABI: argument validation, the split
 // heuristic re-derived for the GB300 SM count, workspace layout, TMA tensor
 // maps, and the stream-ordered launches (prepass, decode, prefill, combine).
 // Nothing here synchronises the host; nothing here allocates.

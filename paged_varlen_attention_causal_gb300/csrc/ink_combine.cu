@@ -1,4 +1,4 @@
-// ink_combine.cu -- split-KV merge (a11): for every (token, head) row whose
+// ink_combine.cu -- split-KV merge: for every (token, head) row whose
 // work unit was cut into more than one split, merge the per-split normalised
 // outputs O_s and log-sum-exps lse_s:
 //     lse = log sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * O_s.

@@ -1,5 +1,6 @@
-// ink_decode.cu -- decode / streaming kernel (a12 with a3-a11 specialised for
-// requests whose Lq * G packed rows fit one 16-row mma block).
+// ink_decode.cu -- decode / streaming kernel: page gather, bias, masks, online
+// softmax, PV and epilogue specialised for requests whose Lq * G packed rows fit
+// one 16-row mma block.
 //
 // Design (GB300):
 //  * persistent CTAs, one per SM, take (request, split) items from a

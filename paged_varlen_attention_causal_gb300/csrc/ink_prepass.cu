@@ -1,4 +1,4 @@
-// ink_prepass.cu -- device-side plan of one call (a1/a2: validation and work
+// ink_prepass.cu -- device-side plan of one call (validation and work
 // decomposition), so that the host never has to read cu_seqlens_q or
 // cache_seqlens and the whole call stays free of host synchronisation.
 //
