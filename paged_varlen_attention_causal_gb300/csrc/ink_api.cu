@@ -343,8 +343,9 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     p.bias_tok_log2 = pl.bias_tok_log2;
 
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
-    alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_bdec, tm_bpf;
+    alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_kd, tm_vd, tm_bdec, tm_bpf;
     memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v); memset(&tm_vp, 0, sizeof tm_vp);
+    memset(&tm_kd, 0, sizeof tm_kd); memset(&tm_vd, 0, sizeof tm_vd);
     memset(&tm_bdec, 0, sizeof tm_bdec); memset(&tm_bpf, 0, sizeof tm_bpf);
     {
         const cuuint64_t gd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv,
@@ -361,6 +362,14 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         const cuuint32_t box4[4] = {64, (cuuint32_t)kKeyGroup, 2, 1};
         if (!encode(&tm_vp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gd4, gs4, box4, CU_TENSOR_MAP_SWIZZLE_128B))
             return INK_ERR_CUDA;
+        // decode K and V: the same view with a box over every KV head, which lands as
+        // [KV head][d half][16 keys][128 B]: a whole page per copy (Hkv <= 8 for the decode kernel)
+        if (Hkv <= 8) {
+            const cuuint32_t boxd[4] = {64, (cuuint32_t)kKeyGroup, 2, (cuuint32_t)Hkv};
+            if (!encode(&tm_kd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, key_cache, gd4, gs4, boxd, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode(&tm_vd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gd4, gs4, boxd, CU_TENSOR_MAP_SWIZZLE_128B))
+                return INK_ERR_CUDA;
+        }
     }
     // bias maps: rel_logits as (E, H, T) fp32, no swizzle; needs 16-byte rows
     bool bias_dec_tma = false, bias_pf_tma = false;
@@ -396,7 +405,7 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
         const int grid = (int)std::min<long long>(sms, pl.dec_cap);
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
-                return launch_decode(pd, tm_k, tm_v, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, grid, smem,
+                return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, grid, smem,
                                      stream);
             }) != cudaSuccess)
             return INK_ERR_CUDA;

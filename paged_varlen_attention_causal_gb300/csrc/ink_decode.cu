@@ -169,10 +169,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 __syncwarp();
                 // invalid page: an out-of-range key coordinate makes TMA fill zeros
                 const int key0 = page >= 0 ? page * p.BS + (gi * kKeyGroup) % p.BS : -kKeyGroup;
-                if (lane < 4 * Hkv) {  // one box per lane: (tensor, KV head, d half)
-                    const int isv = lane / (2 * Hkv), g = (lane >> 1) % Hkv, dh = lane & 1;
-                    const int off = (g * 2 + dh) * 2048 + isv * kv_bytes;
-                    tma_load_3d_hint(st + off, isv ? &tm_v : &tm_k, dh * 64, g, key0, &sh.full[stage], pol_kv);
+                if (lane < 2) {  // one 4-D box per tensor: every KV head and d half of the page
+                    tma_load_4d_hint(st + lane * kv_bytes, lane ? &tm_v : &tm_k, 0, key0, 0, 0, &sh.full[stage], pol_kv);
                 }
                 if (band) {
                     for (int i = lane; i < it.Lq; i += 32) {
