@@ -303,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
 
     import paged_varlen_attention_causal_gb300 as ink
-    from workloads import PROFILE_WORKLOADS, WORKLOADS, workload
+    from workloads import PROFILE_WORKLOADS, WORKLOADS, build_case, workload
 
     WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
     torch.cuda.set_device(local_rank)
@@ -437,6 +437,44 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         return res
 
+    def measure_append(steps, warmup):
+        """KV append of one serving step: 4 x 8192 new tokens, Hkv 8, into 16-key pages (K and V)."""
+        case = build_case("kv_append", [8192] * 4, [8192] * 4, H=8, Hkv=8, E=0, seed=1100, device=dev)
+        g = torch.Generator(device=dev).manual_seed(1101)
+        key = torch.randn(case.T, case.Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+        value = torch.randn(case.T, case.Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+        # slot of token j of request b: its logical position through the block table (all positions are new)
+        pos = torch.arange(8192, device=dev)
+        slots = torch.cat([case.block_table[b, pos // case.BS].long() * case.BS + pos % case.BS for b in range(4)])
+        for _ in range(warmup):
+            ink.reshape_and_cache(key, value, case.key_cache, case.value_cache, slots)
+        torch.cuda.synchronize(dev)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        stream = torch.cuda.current_stream(dev)
+        for a, b in kev:
+            a.record(stream)
+            b.record(stream)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = ink.launch_count()
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local_rank) as clk:
+            start.record(stream)
+            for k in range(steps):
+                ink.set_timing_events("append", kev[k][0], kev[k][1])
+                ink.reshape_and_cache(key, value, case.key_cache, case.value_cache, slots)
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+        ink.set_timing_events("append", None, None)
+        barrier()
+        ms = max_over_ranks(start.elapsed_time(end) / steps, dev)
+        kms = sum(a.elapsed_time(b) for a, b in kev) / steps
+        nbytes = 2 * 2 * case.T * case.Hkv * 128 * 2  # K and V, read once and written once
+        del case, key, value, slots
+        torch.cuda.empty_cache()
+        return {"ms_per_step": ms, "kernel_ms": kms, "bytes": nbytes, "launches": ink.launch_count() - n0,
+                "clocks": clk.summary()}
+
     steps, warmup = args.steps, args.warmup
     headline = args.workload
     head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
@@ -452,6 +490,11 @@ def run_ours(args, rank, world, local_rank):
                 sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
             except Exception as exc:  # report, keep the headline line
                 sec[name] = {"error": f"{type(exc).__name__}: {exc}"}
+        if "kv_append" not in skip:
+            try:
+                sec["kv_append"] = measure_append(max(3, steps // 2), max(3, warmup))
+            except Exception as exc:
+                sec["kv_append"] = {"error": f"{type(exc).__name__}: {exc}"}
 
     def roof_decode(r, name):
         bytes_ = r["kv_bytes"]
@@ -482,6 +525,17 @@ def run_ours(args, rank, world, local_rank):
     for name, r in sec.items():
         if "error" in r:
             workloads_out[name] = r
+            continue
+        if name == "kv_append":
+            ach = r["bytes"] / (r["kernel_ms"] * 1e-3) / 1e9
+            workloads_out[name] = {
+                "metric": "KV append GB/s (K and V read and written)", "ms_per_step": round(r["ms_per_step"], 4),
+                "value": round(r["bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages", "gpu_launches": r["launches"],
+                "clocks": r["clocks"],
+                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                             "peak_source": peaks["source"], "kernel": "ink_append_kernel"}}
             continue
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
                  "gpu_launches": r["launches"], "clocks": r["clocks"]}

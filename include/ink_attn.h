@@ -182,6 +182,33 @@ INK_API ink_status ink_rel_attn_varlen_static(const ink_attn_dims *dims,
                                               int32_t num_splits, void *out, float *lse,
                                               ink_stream_t stream);
 
+/*
+ * KV append: writes this step's keys and values into the paged cache before
+ * attention reads it ("reshape_and_cache" with the slot mapping of the vLLM V1
+ * attention page, metadata builder step 2 and appendix O).  For every token t
+ * with s = slot_mapping[t] >= 0:
+ *     key_cache[s / block_size][s % block_size][h][:]   = key[t][h][:]
+ *     value_cache[s / block_size][s % block_size][h][:] = value[t][h][:]
+ * for every KV head h; negative slots are padding and are skipped.
+ *
+ *   dims        num_tokens, num_kv_heads, head_dim (128), num_blocks and
+ *               block_size are read; the other fields are ignored.
+ *   key, value  device, bf16 (num_tokens, num_kv_heads, head_dim), 16-byte
+ *               aligned; read only.
+ *   key_cache, value_cache
+ *               device, bf16 (num_blocks, block_size, num_kv_heads,
+ *               head_dim), 16-byte aligned; written at the mapped slots only.
+ *   slot_mapping device int64 (num_tokens).  Slots must be distinct.
+ *   flags       device uint32 or NULL: INK_DEVERR_PAGE_ID is OR-ed in when a
+ *               slot is >= num_blocks * block_size (that token is skipped).
+ *   stream      the call is stream-ordered; it allocates nothing.
+ * Returns INK_ERR_INVALID_ARG for null pointers, bad shapes or misalignment,
+ * INK_ERR_UNSUPPORTED for head_dim != 128, INK_ERR_CUDA on a launch error.
+ */
+INK_API ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, const void *value,
+                                         void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                                         uint32_t *flags, ink_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 INK_API const char *ink_status_string(ink_status status);
 
@@ -207,7 +234,8 @@ typedef enum {
     INK_KERNEL_PREPASS = 1,
     INK_KERNEL_DECODE = 2,
     INK_KERNEL_PREFILL = 3,
-    INK_KERNEL_COMBINE = 4
+    INK_KERNEL_COMBINE = 4,
+    INK_KERNEL_APPEND = 5
 } ink_kernel_id;
 
 INK_API void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event);

@@ -158,6 +158,33 @@ def attention(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_
     return out, lse
 
 
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping):
+    """KV append: the new tokens' keys and values into copies of the paged caches.
+
+    vLLM V1 attention page, metadata builder step 2 and appendix O: token t
+    is stored at slot s = slot_mapping[t], i.e. in page s // block_size at
+    offset s % block_size, all KV heads at once; a negative slot is padding
+    and stores nothing.  Written out one token at a time.  Returns the new
+    (key_cache, value_cache) as numpy arrays of the input dtype's bits; the
+    inputs are not modified.  Pinned in ``tests/test_oracle_pins.py`` (every
+    stored token reads back through the slot's page and offset, nothing else
+    changes, padding changes nothing).
+    """
+    k = _as_u16(key)
+    v = _as_u16(value)
+    kc = _as_u16(key_cache).copy()
+    vc = _as_u16(value_cache).copy()
+    slots = np.asarray(slot_mapping.cpu() if hasattr(slot_mapping, "cpu") else slot_mapping, dtype=np.int64)
+    bs = kc.shape[1]
+    for t in range(k.shape[0]):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        kc[s // bs, s % bs] = k[t]
+        vc[s // bs, s % bs] = v[t]
+    return kc, vc
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """fp64 -> nearest bf16 value (round half to even), returned as float64.
 

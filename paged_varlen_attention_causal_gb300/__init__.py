@@ -22,6 +22,7 @@ import torch
 __all__ = [
     "LibraryNotBuilt", "InkError", "Dims", "build", "load", "ink_rel_attn_varlen", "workspace_size",
     "num_splits", "read_device_errors", "version", "DEVERR", "set_timing_events", "launch_count",
+    "reshape_and_cache",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,6 +91,8 @@ def load(path: Optional[str] = None):
         lib.ink_set_timing_events.restype = None
         lib.ink_set_timing_events.argtypes = [ctypes.c_int, vp, vp]
         lib.ink_launch_count.restype = ctypes.c_uint64
+        lib.ink_reshape_and_cache.restype = ctypes.c_int
+        lib.ink_reshape_and_cache.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -99,7 +102,7 @@ def version() -> int:
     return int(load().ink_attn_version())
 
 
-KERNELS = {"prepass": 1, "decode": 2, "prefill": 3, "combine": 4}
+KERNELS = {"prepass": 1, "decode": 2, "prefill": 3, "combine": 4, "append": 5}
 
 
 def set_timing_events(kernel: str, start=None, stop=None) -> None:
@@ -218,6 +221,40 @@ def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens
     if rc != 0:
         raise InkError(rc, "ink_rel_attn_varlen")
     return (out, lse) if return_lse else out
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *, flags=None, stream=None) -> None:
+    """Write this step's keys and values into the paged cache at ``slot_mapping`` (see include/ink_attn.h).
+
+    key/value: bf16 (T, Hkv, 128); caches: bf16 (num_blocks, block_size, Hkv, 128), written in place;
+    slot_mapping: int64 (T,), negative = padding; flags: optional int32 (1,) device tensor that receives
+    DEVERR["PAGE_ID"] for slots past the cache.
+    """
+    lib = load()
+    dev = key.device
+    if dev.type != "cuda":
+        raise ValueError("key must be a CUDA tensor")
+    _check(key, "key", torch.bfloat16, 3, dev)
+    _check(value, "value", torch.bfloat16, 3, dev)
+    _check(key_cache, "key_cache", torch.bfloat16, 4, dev)
+    _check(value_cache, "value_cache", torch.bfloat16, 4, dev)
+    _check(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    if value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("key/value or key_cache/value_cache shapes differ")
+    T, Hkv, D = key.shape
+    NB, BS, Hkv2, D2 = key_cache.shape
+    if (Hkv, D) != (Hkv2, D2) or slot_mapping.shape[0] != T:
+        raise ValueError("key, key_cache and slot_mapping shapes do not match")
+    if flags is not None:
+        _check(flags, "flags", torch.int32, 1, dev)
+    dims = Dims(T, 1, Hkv, Hkv, D, NB, BS, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ink_reshape_and_cache(ctypes.byref(dims), key.data_ptr(), value.data_ptr(), key_cache.data_ptr(),
+                                   value_cache.data_ptr(), slot_mapping.data_ptr(),
+                                   None if flags is None else flags.data_ptr(), int(stream.cuda_stream))
+    if rc != 0:
+        raise InkError(rc, "ink_reshape_and_cache")
 
 
 def read_device_errors(workspace: Optional[torch.Tensor] = None, stream=None, device=None) -> int:

@@ -26,7 +26,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct TimingHook {
     cudaEvent_t start = nullptr, stop = nullptr;
 };
-TimingHook g_hooks[5];
+TimingHook g_hooks[6];
 std::mutex g_hook_mutex;
 std::atomic<unsigned long long> g_launches{0};
 
@@ -225,7 +225,7 @@ int32_t ink_attn_version(void) { return 100; }
 
 void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event)
 {
-    if ((int)kernel < 1 || (int)kernel > 4) return;
+    if ((int)kernel < 1 || (int)kernel > 5) return;
     std::lock_guard<std::mutex> lk(g_hook_mutex);
     g_hooks[kernel].start = static_cast<cudaEvent_t>(start_event);
     g_hooks[kernel].stop = static_cast<cudaEvent_t>(stop_event);
@@ -434,6 +434,29 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
         if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, stream); }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
+    return INK_OK;
+}
+
+ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, const void *value, void *key_cache,
+                                 void *value_cache, const int64_t *slot_mapping, uint32_t *flags,
+                                 ink_stream_t stream_handle)
+{
+    if (!dims || dims->num_tokens < 0 || dims->num_kv_heads < 1 || dims->head_dim < 1 || dims->num_blocks < 1 ||
+        dims->block_size < 1)
+        return INK_ERR_INVALID_ARG;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return INK_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(slot_mapping, 8) || (flags && !aligned(flags, 4)))
+        return INK_ERR_INVALID_ARG;
+    if (dims->head_dim != kHeadDim) return INK_ERR_UNSUPPORTED;
+    if (dims->num_tokens == 0) return INK_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return INK_ERR_CUDA;
+    if (timed_launch(INK_KERNEL_APPEND, stream, [&] {
+            return launch_append(dims, key, value, key_cache, value_cache, slot_mapping, flags, sms, stream);
+        }) != cudaSuccess)
+        return INK_ERR_CUDA;
     return INK_OK;
 }
 

@@ -356,5 +356,8 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
+cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
+                          void *value_cache, const int64_t *slot_mapping, uint32_t *flags, int sms,
+                          cudaStream_t stream);
 
 }  // namespace ink

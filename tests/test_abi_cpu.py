@@ -95,3 +95,21 @@ def test_empty_batch_is_a_no_op(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ink.LibraryNotBuilt):
         ink.load(str(tmp_path / "missing.so"))
+
+
+def test_append_host_validation(lib):
+    """ink_reshape_and_cache rejects bad arguments before touching the GPU."""
+    import ctypes
+
+    f = lib.ink_reshape_and_cache
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(ink.Dims)] + [ctypes.c_void_p] * 7
+    good = 0x10000
+    dims = ink.Dims(8, 1, 4, 4, 128, 16, 16, 1)
+    assert f(ctypes.byref(dims), None, good, good, good, good, None, None) == 1          # null key
+    assert f(ctypes.byref(dims), good, good, good, good, good + 4, None, None) == 1      # misaligned slots
+    assert f(ctypes.byref(dims), good + 8, good, good, good, good, None, None) == 1      # misaligned key
+    bad = ink.Dims(8, 1, 4, 4, 64, 16, 16, 1)
+    assert f(ctypes.byref(bad), good, good, good, good, good, None, None) == 2           # head_dim 64
+    empty = ink.Dims(0, 1, 4, 4, 128, 16, 16, 1)
+    assert f(ctypes.byref(empty), good, good, good, good, good, None, None) == 0         # nothing to do

@@ -104,6 +104,50 @@ def test_slot_mapping_brute_force():
     assert got == want
 
 
+@pytest.mark.parametrize("bs", [1, 4, 16])
+def test_reshape_and_cache_reads_back_through_the_block_table(bs):
+    """The append stores every new token where attention later finds it, and nothing else.
+
+    Read back through the definition (request i's logical position p lives in page
+    block_table[i][p // bs] at offset p % bs), not through the slot arithmetic.
+    """
+    g = torch.Generator().manual_seed(11 + bs)
+    H = 3
+    seq_lens, query_lens = [13, 1, 29, 7], [5, 1, 29, 0]
+    pages = [(n + bs - 1) // bs for n in seq_lens]
+    pool = sum(pages) + 5
+    perm = torch.randperm(pool, generator=g).tolist()
+    block_table, o = [], 0
+    for n in pages:
+        block_table.append(perm[o:o + n] + [-1] * (max(pages) - n))
+        o += n
+    slots = oracle.slot_mapping(block_table, seq_lens, query_lens, bs)
+    T = len(slots)
+    # two padding tokens (slot -1) in the middle of the step
+    slots = slots[:3] + [-1, -1] + slots[3:]
+    T += 2
+    key = torch.randn(T, H, 128, generator=g).to(torch.bfloat16)
+    value = torch.randn(T, H, 128, generator=g).to(torch.bfloat16)
+    kc0 = torch.randn(pool, bs, H, 128, generator=g).to(torch.bfloat16)
+    vc0 = torch.randn(pool, bs, H, 128, generator=g).to(torch.bfloat16)
+    kc, vc = oracle.reshape_and_cache(key, value, kc0, vc0, slots)
+    ku, vu = key.view(torch.int16).numpy().view(np.uint16), value.view(torch.int16).numpy().view(np.uint16)
+    k0, v0 = kc0.view(torch.int16).numpy().view(np.uint16), vc0.view(torch.int16).numpy().view(np.uint16)
+    written = np.zeros((pool, bs), dtype=bool)
+    t = 0
+    for i, (n, ql) in enumerate(zip(seq_lens, query_lens)):
+        for j in range(ql):
+            if t == 3:
+                t += 2  # the padding tokens
+            p = n - ql + j
+            page, off = block_table[i][p // bs], p % bs
+            assert np.array_equal(kc[page, off], ku[t]) and np.array_equal(vc[page, off], vu[t])
+            written[page, off] = True
+            t += 1
+    assert written.sum() == T - 2
+    assert np.array_equal(kc[~written], k0[~written]) and np.array_equal(vc[~written], v0[~written])
+
+
 # --- attention core against the independent dense formulation ---------------
 
 @pytest.mark.parametrize("seed", range(240))
