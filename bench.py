@@ -114,7 +114,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"ink_decode_kernel": "ink_decode.cu", "ink_prefill_kernel": "ink_prefill.cu",
-                  "ink_combine_kernel": "ink_combine.cu", "ink_prepass_kernel": "ink_prepass.cu"}
+                  "ink_combine_kernel": "ink_combine.cu", "ink_prepass_kernel": "ink_prepass.cu",
+                  "ink_append_kernel": "ink_append.cu"}
 
 
 def kernel_source_hash(kernel):
@@ -475,6 +476,63 @@ def run_ours(args, rank, world, local_rank):
         return {"ms_per_step": ms, "kernel_ms": kms, "bytes": nbytes, "launches": ink.launch_count() - n0,
                 "clocks": clk.summary()}
 
+    def measure_graph(steps, warmup):
+        """A small decode step (8 requests, Lk 4096, H 32, Hkv 8, E 1024) called through the API every step
+        and replayed from one captured CUDA graph: the host cost per step that the graph removes."""
+        case = build_case("graph_decode", [1] * 8, [4096] * 8, H=32, Hkv=8, E=1024, seed=1200, device=dev)
+        out = torch.empty_like(case.q)
+        lse = torch.empty(case.T, case.H, dtype=torch.float32, device=dev)
+        dims = ink.Dims(case.T, case.B, case.H, case.Hkv, 128, case.num_blocks, case.BS,
+                        case.block_table.shape[1])
+        ws = torch.empty(ink.workspace_size(dims, case.max_seqlen_q, 0), dtype=torch.uint8, device=dev)
+
+        def run():
+            ink.ink_rel_attn_varlen(
+                case.q, case.key_cache, case.value_cache, block_table=case.block_table,
+                cache_seqlens=case.cache_seqlens, cu_seqlens_q=case.cu_seqlens_q, max_seqlen_q=case.max_seqlen_q,
+                softmax_scale=case.softmax_scale, rel_extent=case.E, rel_logits=case.rel_logits, out=out, lse=lse,
+                workspace=ws)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        torch.cuda.synchronize(dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def timed(fn):
+            for _ in range(warmup):
+                fn()
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            torch.cuda.synchronize(dev)
+            start.record(stream)
+            for _ in range(steps):
+                fn()
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+            return start.elapsed_time(end) / steps
+
+        n0 = ink.launch_count()
+        eager_ms = timed(run)
+        per_step = (ink.launch_count() - n0) / (steps + warmup)
+        want = out.clone()
+        with ClockSampler(local_rank) as clk:
+            graph_ms = timed(graph.replay)
+        if not torch.equal(out, want):
+            raise RuntimeError("graph replay and direct call differ")
+        kv, _, _ = work_of(case)
+        del case, out, lse, ws, graph
+        torch.cuda.empty_cache()
+        return {"eager_ms": max_over_ranks(eager_ms, dev), "graph_ms": max_over_ranks(graph_ms, dev),
+                "kv_bytes": kv, "launches_per_step": per_step, "clocks": clk.summary()}
+
     steps, warmup = args.steps, args.warmup
     headline = args.workload
     head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
@@ -495,6 +553,11 @@ def run_ours(args, rank, world, local_rank):
                 sec["kv_append"] = measure_append(max(3, steps // 2), max(3, warmup))
             except Exception as exc:
                 sec["kv_append"] = {"error": f"{type(exc).__name__}: {exc}"}
+        if "graph_decode" not in skip:
+            try:
+                sec["graph_decode"] = measure_graph(max(50, steps * 10), max(5, warmup))
+            except Exception as exc:
+                sec["graph_decode"] = {"error": f"{type(exc).__name__}: {exc}"}
 
     def roof_decode(r, name):
         bytes_ = r["kv_bytes"]
@@ -534,8 +597,18 @@ def run_ours(args, rank, world, local_rank):
                 "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages", "gpu_launches": r["launches"],
                 "clocks": r["clocks"],
                 "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                             "frac": round(ach / peaks["hbm_gbs"], 4),
+                             "traffic": traffic_of("ink_append_kernel", "kv_append"),
                              "peak_source": peaks["source"], "kernel": "ink_append_kernel"}}
+            continue
+        if name == "graph_decode":
+            workloads_out[name] = {
+                "metric": "decode step time, direct API call vs CUDA graph replay (ms)",
+                "desc": "8 decodes, Lk 4096, H 32, Hkv 8, E 1024 (KV 134 MB, not flushed)",
+                "eager_ms": round(r["eager_ms"], 4), "graph_ms": round(r["graph_ms"], 4),
+                "graph_speedup": round(r["eager_ms"] / r["graph_ms"], 3),
+                "graph_kv_gbs": round(r["kv_bytes"] / (r["graph_ms"] * 1e-3) / 1e9, 1),
+                "gpu_launches_per_step": r["launches_per_step"], "clocks": r["clocks"]}
             continue
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
                  "gpu_launches": r["launches"], "clocks": r["clocks"]}

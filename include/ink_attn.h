@@ -72,8 +72,10 @@ typedef enum {
 /* Device-side data errors, OR-ed into the workspace's error word by the
  * kernels (they never trap); read with ink_rel_attn_read_device_errors.
  * A request that raises CU_SEQLENS, SEQLEN_Q or SEQLEN_K is skipped: its
- * rows of out and lse are left as they were.  With PAGE_ID the keys of the
- * bad page read as zeros. */
+ * rows of out and lse are left as they were.  When the valid requests' token
+ * ranges overlap (an inner cu_seqlens_q entry that steps back) so far that
+ * they need more query tiles than T tokens can, CU_SEQLENS is raised and the
+ * whole call is skipped.  With PAGE_ID the keys of the bad page read as zeros. */
 #define INK_DEVERR_PAGE_ID    0x01u /* block_table entry needed for a visible key is outside [0, num_blocks) */
 #define INK_DEVERR_CU_SEQLENS 0x02u /* cu_seqlens_q not non-decreasing within [0, T], or cu[0] != 0, cu[B] != T */
 #define INK_DEVERR_SEQLEN_Q   0x04u /* a request has more query tokens than max_seqlen_q */

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     __shared__ int bucket_base[kCostBuckets];
     __shared__ int s_carry[3];
     __shared__ uint32_t s_err;
+    __shared__ int s_overflow;
 
     int *dec_off = p.dec_off;
     int *unit_off = p.unit_off;
@@ -130,14 +131,20 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         dec_off[p.B] = s_carry[0];
         unit_off[p.B] = s_carry[1];
         comb_off[p.B] = s_carry[2];
-        p.hdr->comb_tokens = (uint32_t)s_carry[2];
+        // Requests whose token ranges overlap (a cu_seqlens_q entry that steps back between valid
+        // neighbours) can need more q tiles than T tokens allow, and the prefill partials are sized
+        // for T: such a batch is flagged and runs nothing.
+        s_overflow = s_carry[1] > p.units_cap;
+        if (s_overflow) s_err |= INK_DEVERR_CU_SEQLENS;
+        p.hdr->comb_tokens = s_overflow ? 0u : (uint32_t)s_carry[2];
     }
+    __syncthreads();
     if (my_err) atomicOr(&s_err, my_err);
     __syncthreads();
     __threadfence_block();
 
-    const int n_dec = min(s_carry[0], p.dec_items_cap);
-    const int n_units = s_carry[1];
+    const int n_dec = s_overflow ? 0 : min(s_carry[0], p.dec_items_cap);
+    const int n_units = s_overflow ? 0 : s_carry[1];
 
     // pass 2: decode items (request, split), request order; one item per thread, so that a
     // single long request's splits are written in parallel.

@@ -291,6 +291,21 @@ def test_bad_cu_and_lengths_are_flagged():
     assert errors_of_last_call() & ink.DEVERR["SEQLEN_Q"]
 
 
+@pytest.mark.parametrize("splits", [1, 4])
+def test_overlapping_requests_beyond_the_tile_budget_run_nothing(splits):
+    """cu = [0, 100, 0, 100, 120]: requests 0 and 2 are valid but cover the same 100 tokens, so the
+    valid requests need 9 q tiles of 32 tokens where T = 120 allows 8 (ceil(T / 32) + B): flagged,
+    and every output row is left as it was."""
+    case = build_case("overlap", [100, 0, 0, 20], [300, 10, 400, 50], H=8, Hkv=2, E=16, seed=6,
+                      device="cuda", max_seqlen_q=100)
+    case.cu_seqlens_q.copy_(torch.tensor([0, 100, 0, 100, 120], dtype=torch.int32))
+    out = torch.full_like(case.q, 3.0)
+    lse = torch.full((case.T, case.H), 7.0, dtype=torch.float32, device="cuda")
+    gpu_run(case, num_splits=splits, out=out, lse=lse)
+    assert errors_of_last_call() & ink.DEVERR["CU_SEQLENS"]
+    assert bool((out == 3.0).all()) and bool((lse == 7.0).all())
+
+
 def sampled_rows(case, n, seed):
     g = np.random.default_rng(seed)
     T, H = case.T, case.H
