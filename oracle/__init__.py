@@ -60,6 +60,15 @@ def _load():
                 f64, ctypes.c_int, i32, i32, i32, vp,
                 vp, i64, i64, vp, vp,
             ]
+            lib.ink_oracle_attn_fp8kv.restype = ctypes.c_int
+            lib.ink_oracle_attn_fp8kv.argtypes = [
+                i32, i32, i32, i32, i32, i32, i32, i32,
+                vp, vp, vp, f64, f64, vp, vp, vp,
+                f64, ctypes.c_int, i32, i32, i32, vp,
+                vp, i64, i64, vp, vp,
+            ]
+            lib.ink_oracle_e4m3_decode.restype = None
+            lib.ink_oracle_e4m3_decode.argtypes = [vp, i64, vp]
             lib.ink_oracle_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -95,6 +104,30 @@ def _as(x, dtype) -> np.ndarray:
     if hasattr(x, "detach"):
         x = x.detach().cpu().numpy()
     return np.ascontiguousarray(np.asarray(x, dtype=dtype))
+
+
+def _as_u8(x) -> np.ndarray:
+    """uint8 tensor / array (E4M3 bytes) -> contiguous uint8 array."""
+    if hasattr(x, "detach"):
+        import torch
+
+        x = x.detach().cpu().contiguous()
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    a = np.ascontiguousarray(np.asarray(x))
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected E4M3 bytes as uint8, got {a.dtype}")
+    return a
+
+
+def e4m3_to_float64(codes) -> np.ndarray:
+    """Values of OCP FP8 E4M3 bytes (NaN for the two NaN codes), decoded by the oracle's C routine."""
+    a = _as_u8(codes)
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().ink_oracle_e4m3_decode(a.ctypes.data_as(ctypes.c_void_p), int(a.size),
+                                   out.ctypes.data_as(ctypes.c_void_p))
+    return out
 
 
 def attention(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, *,
@@ -200,3 +233,58 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     out = rounded.astype(np.uint32).view(np.float32).astype(np.float64)
     out[nan] = np.nan
     return out
+
+
+def attention_fp8kv(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, *,
+                    k_scale: float, v_scale: float, softmax_scale: float, causal: bool = True,
+                    window_left: int = -1, window_right: int = -1, rel_extent: int = 0, rel_logits=None,
+                    rows=None, chunk_keys: int = 0):
+    """``attention`` over an FP8 KV cache: key_cache / value_cache are (NB, BS, Hkv, D) E4M3 bytes and
+    K = k_scale * E4M3(byte), V = v_scale * E4M3(byte).
+
+    The scales enter as the PagedAttention V2 page's paged_attention_v2_pytorch applies k_scale and
+    v_scale to the gathered K and V rows; the cache format is OCP FP8 E4M3, the FP8 KV cache of the
+    vLLM V1 attention page's TurboQuant backend (section 12.1), dequantized when the cache is read.
+    Pinned in ``tests/test_oracle_pins.py``: the decoder against every one of the 256 codes of an
+    independent E4M3 implementation, and the attention against ``attention`` on bf16 caches holding
+    the same values.
+    """
+    lib = _load()
+    qa = _as_u16(q)
+    ka = _as_u8(key_cache)
+    va = _as_u8(value_cache)
+    T, H, D = qa.shape
+    NB, BS, Hkv, D2 = ka.shape
+    if D2 != D or va.shape != ka.shape:
+        raise ValueError("cache shapes do not match q")
+    bt = _as(block_table, np.int32)
+    B, MAXBLK = bt.shape
+    sk = _as(cache_seqlens, np.int32)
+    cu = _as(cu_seqlens_q, np.int32)
+    if sk.shape != (B,) or cu.shape != (B + 1,):
+        raise ValueError("cache_seqlens / cu_seqlens_q shapes do not match block_table")
+    rel = None
+    if rel_extent > 0:
+        rel = _as(rel_logits, np.float32)
+        if rel.shape != (T, H, rel_extent):
+            raise ValueError("rel_logits must be (T, H, rel_extent)")
+    if rows is None:
+        rows_a, n_rows = None, T * H
+    else:
+        rows_a = _as(rows, np.int64).reshape(-1)
+        n_rows = rows_a.size
+    out = np.empty((max(n_rows, 0), D), dtype=np.float64)
+    lse = np.empty((max(n_rows, 0),), dtype=np.float64)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.ink_oracle_attn_fp8kv(
+        T, B, H, Hkv, D, NB, BS, MAXBLK,
+        ptr(qa), ptr(ka), ptr(va), float(k_scale), float(v_scale), ptr(bt), ptr(sk), ptr(cu),
+        float(softmax_scale), int(bool(causal)), int(window_left), int(window_right),
+        int(rel_extent), ptr(rel),
+        ptr(rows_a), int(n_rows), int(chunk_keys), ptr(out), ptr(lse),
+    )
+    if rc != 0:
+        raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
+    if rows is None:
+        return out.reshape(T, H, D), lse.reshape(T, H)
+    return out, lse

@@ -38,6 +38,14 @@
  * (That rule is exact only when o_c is normalised by its own l_c; see the
  * reading recorded for it in the design notes.)
  *
+ * FP8 KV cache (ink_oracle_attn_fp8kv): the caches hold one byte per element
+ * in the OCP 8-bit floating-point format E4M3, and an element's value is its
+ * decoded E4M3 value times the tensor's scale (k_scale for K, v_scale for V),
+ * as the PagedAttention V2 page's paged_attention_v2_pytorch multiplies the
+ * gathered K and V rows by k_scale and v_scale, and as the vLLM V1 attention
+ * page's TurboQuant backend dequantizes an FP8 cache when it decodes
+ * (section 12.1).  Everything else is the definition above.
+ *
  * bf16 inputs are passed as their 16-bit patterns and widened exactly.
  */
 #include <math.h>
@@ -54,6 +62,9 @@
 typedef struct {
     int32_t T, B, H, Hkv, D, NB, BS, MAXBLK;
     const uint16_t *q, *kc, *vc;
+    const uint8_t *kc8, *vc8;       /* E4M3 caches when kv_fp8, else unused */
+    int kv_fp8;
+    double k_scale, v_scale;
     const int32_t *bt, *seqk, *cu;
     double scale;
     int causal;
@@ -67,6 +78,26 @@ static double bf16_bits_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits.  Exponent field 0 holds zero and the subnormals m/8 * 2^-6;
+ * exponent 15 with mantissa 7 is NaN; there are no infinities (the largest
+ * finite value is 1.75 * 2^8 = 448). */
+static double e4m3_bits_to_double(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Element idx of the K (value == 0) or V (value == 1) cache as a real number. */
+static double cache_elem(const oracle_args *a, int value, int64_t idx)
+{
+    if (a->kv_fp8)
+        return (value ? a->v_scale : a->k_scale) * e4m3_bits_to_double((value ? a->vc8 : a->kc8)[idx]);
+    return bf16_bits_to_double((value ? a->vc : a->kc)[idx]);
 }
 
 /* Request owning token t (cu is non-decreasing, checked by the caller). */
@@ -118,11 +149,11 @@ static int64_t row_stats(const oracle_args *a, int64_t t, int32_t h,
         if (key_visible(a, q_abs, j)) {
             const int32_t page = a->bt[(int64_t)b * a->MAXBLK + j / a->BS];
             if (page < 0 || page >= a->NB) return -1;
-            const uint16_t *krow =
-                a->kc + (((int64_t)page * a->BS + j % a->BS) * a->Hkv + g) * a->D;
+            const int64_t krow =
+                (((int64_t)page * a->BS + j % a->BS) * a->Hkv + g) * a->D;
             double dot = 0.0;
             for (int32_t d = 0; d < a->D; ++d)
-                dot += bf16_bits_to_double(qrow[d]) * bf16_bits_to_double(krow[d]);
+                dot += bf16_bits_to_double(qrow[d]) * cache_elem(a, 0, krow + d);
             sj = a->scale * dot;
             const int64_t rd = q_abs - j;
             if (rd >= 0 && rd < a->E)
@@ -140,10 +171,10 @@ static int64_t row_stats(const oracle_args *a, int64_t t, int32_t h,
             if (sj == -INFINITY) continue;
             const double p = exp(sj - m);
             const int32_t page = a->bt[(int64_t)b * a->MAXBLK + j / a->BS];
-            const uint16_t *vrow =
-                a->vc + (((int64_t)page * a->BS + j % a->BS) * a->Hkv + g) * a->D;
+            const int64_t vrow =
+                (((int64_t)page * a->BS + j % a->BS) * a->Hkv + g) * a->D;
             l += p;
-            for (int32_t d = 0; d < a->D; ++d) acc[d] += p * bf16_bits_to_double(vrow[d]);
+            for (int32_t d = 0; d < a->D; ++d) acc[d] += p * cache_elem(a, 1, vrow + d);
         }
     }
     *m_out = m;
@@ -285,6 +316,7 @@ int ink_oracle_attn(int32_t T, int32_t B, int32_t H, int32_t Hkv, int32_t D,
     oracle_args a;
     a.T = T; a.B = B; a.H = H; a.Hkv = Hkv; a.D = D; a.NB = NB; a.BS = BS; a.MAXBLK = MAXBLK;
     a.q = q; a.kc = key_cache; a.vc = value_cache;
+    a.kc8 = NULL; a.vc8 = NULL; a.kv_fp8 = 0; a.k_scale = 1.0; a.v_scale = 1.0;
     a.bt = block_table; a.seqk = cache_seqlens; a.cu = cu_seqlens_q;
     a.scale = softmax_scale; a.causal = causal; a.wl = window_left; a.wr = window_right;
     a.E = rel_extent; a.rel = rel_logits;
@@ -293,6 +325,42 @@ int ink_oracle_attn(int32_t T, int32_t B, int32_t H, int32_t Hkv, int32_t D,
         return ORACLE_ERR_ARG;
     if (rows == NULL && n_rows != (int64_t)T * H) return ORACLE_ERR_ARG;
     return run_rows(&a, rows, n_rows, chunk_keys, out, lse);
+}
+
+/*
+ * The same attention over an FP8 (E4M3) KV cache: key_cache / value_cache
+ * hold one byte per element, (NB, BS, Hkv, D), and K = k_scale * E4M3(byte),
+ * V = v_scale * E4M3(byte).  Other arguments and results as ink_oracle_attn.
+ */
+int ink_oracle_attn_fp8kv(int32_t T, int32_t B, int32_t H, int32_t Hkv, int32_t D,
+                          int32_t NB, int32_t BS, int32_t MAXBLK,
+                          const uint16_t *q, const uint8_t *key_cache, const uint8_t *value_cache,
+                          double k_scale, double v_scale,
+                          const int32_t *block_table, const int32_t *cache_seqlens,
+                          const int32_t *cu_seqlens_q,
+                          double softmax_scale, int causal, int32_t window_left, int32_t window_right,
+                          int32_t rel_extent, const float *rel_logits,
+                          const int64_t *rows, int64_t n_rows, int64_t chunk_keys,
+                          double *out, double *lse)
+{
+    oracle_args a;
+    a.T = T; a.B = B; a.H = H; a.Hkv = Hkv; a.D = D; a.NB = NB; a.BS = BS; a.MAXBLK = MAXBLK;
+    a.q = q; a.kc = NULL; a.vc = NULL;
+    a.kc8 = key_cache; a.vc8 = value_cache; a.kv_fp8 = 1; a.k_scale = k_scale; a.v_scale = v_scale;
+    a.bt = block_table; a.seqk = cache_seqlens; a.cu = cu_seqlens_q;
+    a.scale = softmax_scale; a.causal = causal; a.wl = window_left; a.wr = window_right;
+    a.E = rel_extent; a.rel = rel_logits;
+    if (!q || !key_cache || !value_cache || !block_table || !cache_seqlens || !cu_seqlens_q ||
+        !out || !lse || window_left < -1 || window_right < -1)
+        return ORACLE_ERR_ARG;
+    if (rows == NULL && n_rows != (int64_t)T * H) return ORACLE_ERR_ARG;
+    return run_rows(&a, rows, n_rows, chunk_keys, out, lse);
+}
+
+/* E4M3 bytes to their values (for the decoder's own pins). */
+void ink_oracle_e4m3_decode(const uint8_t *bits, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_bits_to_double(bits[i]);
 }
 
 /* Number of threads the OpenMP runtime will use (for reporting). */

@@ -24,7 +24,12 @@ MUTANTS = {
     "right window edge": ("if (a->wr >= 0 && j > q_abs + a->wr) return 0;", "if (a->wr >= 0 && j >= q_abs + a->wr) return 0;"),
     "causal excludes diagonal": ("if (a->causal && j > q_abs) return 0;", "if (a->causal && j >= q_abs) return 0;"),
     "lse without log": ("lse[r] = m + log(l);", "lse[r] = m + l;"),
-    "values from key cache": ("a->vc + (((int64_t)page", "a->kc + (((int64_t)page"),
+    "values from key cache": ("cache_elem(a, 1, vrow + d)", "cache_elem(a, 0, vrow + d)"),
+    "e4m3 exponent bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3 subnormal scale": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3 sign dropped": ("return sign ? -v : v;", "return v;"),
+    "fp8 scales swapped": ("(value ? a->v_scale : a->k_scale)", "(value ? a->k_scale : a->v_scale)"),
+    "fp8 value scale ignored": ("(value ? a->v_scale : a->k_scale)", "(value ? 1.0 : a->k_scale)"),
     "bias scaled": ("sj += (double)a->rel[", "sj += a->scale * (double)a->rel["),
     "row within page reversed": ("(((int64_t)page * a->BS + j % a->BS) * a->Hkv + g) * a->D;\n            double dot",
                                  "(((int64_t)page * a->BS + (a->BS - 1 - j % a->BS)) * a->Hkv + g) * a->D;\n            double dot"),
@@ -36,7 +41,8 @@ MUTANTS = {
                           "a->bt[(int64_t)b * a->MAXBLK + j % a->BS];\n            if (page < 0"),
 }
 
-PIN_SUBSET = "dense or closed or split or zero_query or single_key or constant or diagonal or unread or sdpa"
+PIN_SUBSET = ("dense or closed or split or zero_query or single_key or constant or diagonal or unread or sdpa "
+              "or fp8")
 
 
 def _build(tmp_path, name, text):

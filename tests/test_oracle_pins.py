@@ -425,6 +425,68 @@ def test_non_monotone_cu_is_reported():
         _run(case)
 
 
+# --- FP8 (E4M3) KV cache ------------------------------------------------------
+
+def test_fp8_decoder_matches_an_independent_e4m3_for_every_code():
+    """All 256 codes against torch's float8_e4m3fn (an independent implementation of the OCP format),
+    plus the format's landmarks: 1, -1, the largest finite value 448, the smallest subnormal 2^-9, the
+    smallest normal 2^-6, +-0, and NaN for S.1111.111."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    mine = oracle.e4m3_to_float64(codes)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.flatnonzero(nan).tolist() == [0x7F, 0xFF]
+    assert np.array_equal(mine[~nan], ref[~nan])
+    got = oracle.e4m3_to_float64(np.array([0x38, 0xB8, 0x7E, 0x01, 0x08, 0x00, 0x80], dtype=np.uint8))
+    assert got.tolist() == [1.0, -1.0, 448.0, 2.0 ** -9, 2.0 ** -6, 0.0, -0.0]
+    assert math.copysign(1.0, got[-1]) == -1.0
+
+
+def _fp8_case(seed, **over):
+    case = random_case(seed, D=32, **over)
+    g = torch.Generator().manual_seed(7000 + seed)
+    shape = case.key_cache.shape
+    k8 = (torch.randn(shape, generator=g) * 6).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (torch.randn(shape, generator=g) * 6).to(torch.float8_e4m3fn).view(torch.uint8)
+    return case, k8, v8
+
+
+def _fp8_run(case, k8, v8, ks, vs, **over):
+    kw = case.oracle_kwargs()
+    kw.update(over)
+    return oracle.attention_fp8kv(case.q, k8, v8, case.block_table, case.cache_seqlens, case.cu_seqlens_q,
+                                  k_scale=ks, v_scale=vs, **kw)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fp8_cache_equals_bf16_cache_of_the_same_values(seed):
+    """With power-of-two scales every k_scale * E4M3 value is exact in bf16, so the FP8-cache attention
+    must equal the (dense-pinned) bf16-cache attention on those values, to the last bit of fp64."""
+    case, k8, v8 = _fp8_case(seed)
+    ks, vs = 2.0 ** -3, 2.0 ** 2
+    kb = torch.from_numpy(oracle.e4m3_to_float64(k8) * ks).to(torch.bfloat16)
+    vb = torch.from_numpy(oracle.e4m3_to_float64(v8) * vs).to(torch.bfloat16)
+    assert np.array_equal(kb.double().numpy(), oracle.e4m3_to_float64(k8) * ks)  # exact in bf16
+    out, lse = _fp8_run(case, k8, v8, ks, vs)
+    bout, blse = oracle.attention(case.q, kb, vb, case.block_table, case.cache_seqlens, case.cu_seqlens_q,
+                                  **case.oracle_kwargs())
+    _close(out, bout, 0.0)
+    _close(lse, blse, 0.0)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fp8_scales_are_a_logit_scale_and_an_output_scale(seed):
+    """K = k_scale * E4M3 multiplies every q.k by k_scale (the same as softmax_scale * k_scale with unit
+    scales); V = v_scale * E4M3 multiplies the output by v_scale and leaves the log-sum-exp alone."""
+    case, k8, v8 = _fp8_case(100 + seed)
+    ks, vs = 0.37, 1.9
+    out, lse = _fp8_run(case, k8, v8, ks, vs)
+    uout, ulse = _fp8_run(case, k8, v8, 1.0, 1.0, softmax_scale=case.softmax_scale * ks)
+    _close(out, vs * uout, 1e-12)
+    _close(lse, ulse, 1e-12)
+
+
 def test_round_to_bf16_matches_torch():
     x = np.random.default_rng(0).normal(size=10000) * 10.0 ** np.random.default_rng(1).integers(-6, 6, 10000)
     want = torch.from_numpy(x).float().to(torch.bfloat16).double().numpy()

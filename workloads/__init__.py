@@ -226,3 +226,12 @@ def random_case(seed: int, *, B: Optional[int] = None, device="cpu", D: int = 12
               device=device)
     kw.update(over)
     return build_case(f"random{seed}", q_lens, kv_lens, **kw)
+
+
+def fp8_kv(case: Case, k_scale: float, v_scale: float):
+    """E4M3 bytes for an FP8 KV cache holding about the case's bf16 K and V: each element divided by its
+    tensor's scale and rounded to E4M3 (torch's float8_e4m3fn cast; values clamped to the format's 448).
+    Returns (key_cache, value_cache) as uint8 tensors of the case's cache shape on its device."""
+    def q8(x, s):
+        return (x.float() / s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q8(case.key_cache, k_scale), q8(case.value_cache, v_scale)
