@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged rel-bias attn: decode KV-read GB/s & prefill TFLOP/s (% of roofline)"
 HEADLINE = "decode_batch"
 SECONDARY = ["chunked_prefill", "long_decode", "continuous_batch"]
+FP8_SCALES = (0.0625, 0.05)  # k_scale, v_scale of the E4M3 caches the bench builds
 D = 128
 
 
@@ -304,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
 
     import paged_varlen_attention_causal_gb300 as ink
-    from workloads import PROFILE_WORKLOADS, WORKLOADS, build_case, workload
+    from workloads import PROFILE_WORKLOADS, WORKLOADS, build_case, fp8_kv, workload
 
     WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
     torch.cuda.set_device(local_rank)
@@ -320,16 +321,26 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    def call(case, out, lse, splits=0, stream=None):
-        return ink.ink_rel_attn_varlen(
-            case.q, case.key_cache, case.value_cache, block_table=case.block_table,
-            cache_seqlens=case.cache_seqlens, cu_seqlens_q=case.cu_seqlens_q, max_seqlen_q=case.max_seqlen_q,
-            softmax_scale=case.softmax_scale, causal=case.causal, window_left=case.window_left,
-            window_right=case.window_right, rel_extent=case.E, rel_logits=case.rel_logits, num_splits=splits,
-            out=out, lse=lse)
+    def attend(case, q, block_table, cache_seqlens, cu_seqlens_q, rel_logits, out, lse, splits=0):
+        """One call of the public API; an E4M3 cache (uint8) goes through the FP8 entry point."""
+        kw = dict(block_table=block_table, cache_seqlens=cache_seqlens, cu_seqlens_q=cu_seqlens_q,
+                  max_seqlen_q=case.max_seqlen_q, softmax_scale=case.softmax_scale, causal=case.causal,
+                  window_left=case.window_left, window_right=case.window_right, rel_extent=case.E,
+                  rel_logits=rel_logits, num_splits=splits, out=out, lse=lse)
+        if case.key_cache.dtype == torch.uint8:
+            return ink.ink_rel_attn_varlen_fp8kv(q, case.key_cache, case.value_cache, k_scale=FP8_SCALES[0],
+                                                 v_scale=FP8_SCALES[1], **kw)
+        return ink.ink_rel_attn_varlen(q, case.key_cache, case.value_cache, **kw)
 
-    def measure(name, steps, warmup, main_kernel):
+    def call(case, out, lse, splits=0):
+        return attend(case, case.q, case.block_table, case.cache_seqlens, case.cu_seqlens_q, case.rel_logits, out,
+                      lse, splits)
+
+    def measure(name, steps, warmup, main_kernel, fp8=False):
         case = workload(name, device=dev)
+        if fp8:  # the same workload over an E4M3 copy of its KV cache
+            case.key_cache, case.value_cache = fp8_kv(case, *FP8_SCALES)
+            torch.cuda.empty_cache()
         out = torch.empty_like(case.q)
         lse = torch.empty(case.T, case.H, dtype=torch.float32, device=dev)
         stream = torch.cuda.current_stream(dev)
@@ -361,6 +372,8 @@ def run_ours(args, rank, world, local_rank):
         kms = sum(a.elapsed_time(b) for a, b in kev) / steps
         ms_max = max_over_ranks(ms, dev)
         kv, flops, pairs = work_of(case)
+        if fp8:
+            kv //= 2  # one byte per K / V element
         res = {"workload": name, "desc": WORKLOADS[name], "ms_per_step": ms_max, "kernel_ms": kms,
                "kv_bytes": kv, "flops": flops, "launches": launches, "clocks": clk.summary()}
         # end-to-end through the public API with host buffers: every step uploads its inputs from pinned
@@ -406,12 +419,8 @@ def run_ours(args, rank, world, local_rank):
                 if k >= 2:
                     stream.wait_event(down_done[b])  # its output buffers are read back already
                 c = dev_in[b]
-                ink.ink_rel_attn_varlen(
-                    c["q"], case.key_cache, case.value_cache, block_table=c["block_table"],
-                    cache_seqlens=c["cache_seqlens"], cu_seqlens_q=c["cu_seqlens_q"],
-                    max_seqlen_q=case.max_seqlen_q, softmax_scale=case.softmax_scale, causal=case.causal,
-                    window_left=case.window_left, window_right=case.window_right, rel_extent=case.E,
-                    rel_logits=c.get("rel_logits"), out=dev_out[b][0], lse=dev_out[b][1])
+                attend(case, c["q"], c["block_table"], c["cache_seqlens"], c["cu_seqlens_q"], c.get("rel_logits"),
+                       dev_out[b][0], dev_out[b][1])
                 comp_done[b].record(stream)
                 s_down.wait_event(comp_done[b])
                 with torch.cuda.stream(s_down):
@@ -536,7 +545,9 @@ def run_ours(args, rank, world, local_rank):
     steps, warmup = args.steps, args.warmup
     headline = args.workload
     head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
-    head = measure(headline, steps, warmup, head_kernel)
+    if args.kv_fp8 and head_kernel != "decode":
+        raise SystemExit("--kv-fp8 applies to decode-shaped workloads only")
+    head = measure(headline, steps, warmup, head_kernel, fp8=args.kv_fp8)
     sec = {}
     if not args.headline_only:
         skip = {x for x in args.skip.split(",") if x}
@@ -553,6 +564,12 @@ def run_ours(args, rank, world, local_rank):
                 sec["kv_append"] = measure_append(max(3, steps // 2), max(3, warmup))
             except Exception as exc:
                 sec["kv_append"] = {"error": f"{type(exc).__name__}: {exc}"}
+        if "decode_batch_fp8" not in skip:
+            try:
+                sec["decode_batch_fp8"] = measure("decode_batch", max(3, steps // 2), max(3, warmup), "decode",
+                                                  fp8=True)
+            except Exception as exc:
+                sec["decode_batch_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
         if "graph_decode" not in skip:
             try:
                 sec["graph_decode"] = measure_graph(max(50, steps * 10), max(5, warmup))
@@ -584,6 +601,8 @@ def run_ours(args, rank, world, local_rank):
         value = job_throughput(head["kv_bytes"], world, head["ms_per_step"]) / 1e9
         e2e = job_throughput(head["kv_bytes"], world, head["e2e_ms"]) / 1e9
         roof = roof_decode(head, headline)
+        if args.kv_fp8:
+            roof.update({"traffic": None, "kernel": "ink_decode_kernel (E4M3 cache)"})
     workloads_out = {}
     for name, r in sec.items():
         if "error" in r:
@@ -600,6 +619,15 @@ def run_ours(args, rank, world, local_rank):
                              "frac": round(ach / peaks["hbm_gbs"], 4),
                              "traffic": traffic_of("ink_append_kernel", "kv_append"),
                              "peak_source": peaks["source"], "kernel": "ink_append_kernel"}}
+            continue
+        if name == "decode_batch_fp8":
+            rf = roof_decode(r, name)
+            rf.update({"traffic": None, "kernel": "ink_decode_kernel (E4M3 cache)"})
+            workloads_out[name] = {
+                "metric": "decode KV-read GB/s (E4M3 cache bytes)", "ms_per_step": round(r["ms_per_step"], 4),
+                "e2e_ms": round(r["e2e_ms"], 4), "value": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "desc": WORKLOADS["decode_batch"] + "; KV cache in E4M3 (1 byte per element)",
+                "gpu_launches": r["launches"], "clocks": r["clocks"], "roofline": rf}
             continue
         if name == "graph_decode":
             workloads_out[name] = {
@@ -635,6 +663,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": warmup, "ms_per_step": round(head["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads/)",
         "config": {"workload": headline, "desc": WORKLOADS[headline], "parallelism": f"replicas x{world}",
+                   "kv_cache": "e4m3" if args.kv_fp8 else "bf16",
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": roof,
         "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": head["h2d_bytes"],
@@ -745,6 +774,8 @@ def main():
                     choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch",
                              "decode_batch_quarter", "chunked_prefill_quarter"])
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="run the (decode-shaped) headline workload over an E4M3 copy of its KV cache")
     ap.add_argument("--skip", default="", help="comma-separated secondary workloads to leave out")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

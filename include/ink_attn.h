@@ -154,6 +154,36 @@ INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
                                ink_stream_t stream);
 
 /*
+ * The same attention over an FP8 KV cache (decode path).  The FP8 cache is
+ * the TurboQuant backend's (vLLM V1 attention page, section 12.1: an FP8
+ * cache dequantized when decoding), with per-tensor k_scale / v_scale applied
+ * to the gathered K and V rows as paged_attention_v2_pytorch does on the
+ * PagedAttention V2 page.
+ *   key_cache, value_cache  OCP FP8 E4M3 bytes, (num_blocks, block_size,
+ *                 Hkv, D), contiguous, 16-byte aligned; the values attended
+ *                 over are k_scale * E4M3(byte) and v_scale * E4M3(byte).
+ *   k_scale, v_scale  finite and > 0, else INK_ERR_INVALID_ARG.
+ * Decode-shaped calls only: max_seqlen_q * (H / Hkv) <= 16 and Hkv in
+ * {1, 2, 4, 8}; any other call returns INK_ERR_UNSUPPORTED before anything
+ * is launched.  The products run in fp16 with fp32 accumulation: every E4M3
+ * value is exact in fp16, and q is converted from bf16 to fp16 (exact for
+ * magnitudes in [2^-14, 65504]; smaller ones lose bits, larger ones
+ * overflow).  All other arguments, the workspace (same size query), results
+ * and errors are those of ink_rel_attn_varlen.
+ */
+INK_API ink_status ink_rel_attn_varlen_fp8kv(const ink_attn_dims *dims,
+                                             const void *q, const void *key_cache, const void *value_cache,
+                                             float k_scale, float v_scale,
+                                             const int32_t *block_table, const int32_t *cache_seqlens,
+                                             const int32_t *cu_seqlens_q, int32_t max_seqlen_q,
+                                             float softmax_scale, int causal,
+                                             int32_t window_left, int32_t window_right,
+                                             int32_t rel_extent, const float *rel_logits,
+                                             int32_t num_splits, void *out, float *lse,
+                                             void *workspace, size_t workspace_bytes,
+                                             ink_stream_t stream);
+
+/*
  * Allocation-free variant (this entry point has no counterpart on the source
  * pages).  For callers that cannot allocate device memory: programs embedded in
  * a host that owns all device memory itself, such as a serving engine that has

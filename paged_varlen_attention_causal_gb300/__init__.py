@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "LibraryNotBuilt", "InkError", "Dims", "build", "load", "ink_rel_attn_varlen", "workspace_size",
     "num_splits", "read_device_errors", "version", "DEVERR", "set_timing_events", "launch_count",
-    "reshape_and_cache",
+    "reshape_and_cache", "ink_rel_attn_varlen_fp8kv",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +83,10 @@ def load(path: Optional[str] = None):
         lib.ink_rel_attn_varlen.argtypes = [
             dp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, i32, i32, i32, vp, i32,
             vp, vp, vp, sz, vp]
+        lib.ink_rel_attn_varlen_fp8kv.restype = ctypes.c_int
+        lib.ink_rel_attn_varlen_fp8kv.argtypes = [
+            dp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, i32,
+            i32, i32, vp, i32, vp, vp, vp, sz, vp]
         lib.ink_status_string.restype = ctypes.c_char_p
         lib.ink_status_string.argtypes = [ctypes.c_int]
         lib.ink_rel_attn_read_device_errors.restype = ctypes.c_int
@@ -162,25 +166,15 @@ def _check(t: torch.Tensor, name: str, dtype, dim: int, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens, cu_seqlens_q,
-                        max_seqlen_q: int, softmax_scale: float, causal: bool = True,
-                        window_left: int = -1, window_right: int = -1, rel_extent: int = 0,
-                        rel_logits=None, num_splits: int = 0, out=None, lse=None,
-                        return_lse: bool = False, workspace=None, stream=None):
-    """Paged varlen attention with the Inkling relative bias (see include/ink_attn.h).
-
-    Keyword arguments follow ``inkling_fa4_rel_attention`` (fa4_rel_attention.py
-    as quoted by the nxmr.cn article, its wrapper signature), with the window
-    passed as two integers (-1 = unbounded).  Returns ``out`` (and ``lse``
-    when ``return_lse``).
-    """
-    lib = load()
+def _prepare(q, key_cache, value_cache, cache_dtype, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+             rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream):
+    """Checks and marshals the arguments both attention entry points share."""
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("q must be a CUDA tensor")
     _check(q, "q", torch.bfloat16, 3, dev)
-    _check(key_cache, "key_cache", torch.bfloat16, 4, dev)
-    _check(value_cache, "value_cache", torch.bfloat16, 4, dev)
+    _check(key_cache, "key_cache", cache_dtype, 4, dev)
+    _check(value_cache, "value_cache", cache_dtype, 4, dev)
     if value_cache.shape != key_cache.shape:
         raise ValueError("value_cache and key_cache shapes differ")
     _check(block_table, "block_table", torch.int32, 2, dev)
@@ -212,6 +206,25 @@ def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens
     need = workspace_size(dims, max_seqlen_q, num_splits)
     if workspace is None:
         workspace = _workspace(dev, need, stream)
+    return dims, rel_ptr, out, lse, workspace, stream
+
+
+def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens, cu_seqlens_q,
+                        max_seqlen_q: int, softmax_scale: float, causal: bool = True,
+                        window_left: int = -1, window_right: int = -1, rel_extent: int = 0,
+                        rel_logits=None, num_splits: int = 0, out=None, lse=None,
+                        return_lse: bool = False, workspace=None, stream=None):
+    """Paged varlen attention with the Inkling relative bias (see include/ink_attn.h).
+
+    Keyword arguments follow ``inkling_fa4_rel_attention`` (fa4_rel_attention.py
+    as quoted by the nxmr.cn article, its wrapper signature), with the window
+    passed as two integers (-1 = unbounded).  Returns ``out`` (and ``lse``
+    when ``return_lse``).
+    """
+    lib = load()
+    dims, rel_ptr, out, lse, workspace, stream = _prepare(
+        q, key_cache, value_cache, torch.bfloat16, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream)
     rc = lib.ink_rel_attn_varlen(
         ctypes.byref(dims), q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
         block_table.data_ptr(), cache_seqlens.data_ptr(), cu_seqlens_q.data_ptr(), int(max_seqlen_q),
@@ -220,6 +233,35 @@ def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(stream.cuda_stream))
     if rc != 0:
         raise InkError(rc, "ink_rel_attn_varlen")
+    return (out, lse) if return_lse else out
+
+
+def ink_rel_attn_varlen_fp8kv(q, key_cache, value_cache, *, k_scale: float, v_scale: float, block_table,
+                              cache_seqlens, cu_seqlens_q, max_seqlen_q: int, softmax_scale: float,
+                              causal: bool = True, window_left: int = -1, window_right: int = -1,
+                              rel_extent: int = 0, rel_logits=None, num_splits: int = 0, out=None, lse=None,
+                              return_lse: bool = False, workspace=None, stream=None):
+    """``ink_rel_attn_varlen`` over an FP8 KV cache (decode-shaped calls; see include/ink_attn.h).
+
+    key_cache / value_cache: E4M3 bytes as uint8 (or float8_e4m3fn) tensors of shape
+    (num_blocks, block_size, Hkv, 128); the values attended over are k_scale * E4M3 and v_scale * E4M3.
+    """
+    lib = load()
+    if key_cache.dtype == torch.float8_e4m3fn:
+        key_cache = key_cache.view(torch.uint8)
+    if value_cache.dtype == torch.float8_e4m3fn:
+        value_cache = value_cache.view(torch.uint8)
+    dims, rel_ptr, out, lse, workspace, stream = _prepare(
+        q, key_cache, value_cache, torch.uint8, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream)
+    rc = lib.ink_rel_attn_varlen_fp8kv(
+        ctypes.byref(dims), q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), float(k_scale),
+        float(v_scale), block_table.data_ptr(), cache_seqlens.data_ptr(), cu_seqlens_q.data_ptr(),
+        int(max_seqlen_q), float(softmax_scale), int(bool(causal)), int(window_left), int(window_right),
+        int(rel_extent), rel_ptr, int(num_splits), out.data_ptr(), None if lse is None else lse.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(stream.cuda_stream))
+    if rc != 0:
+        raise InkError(rc, "ink_rel_attn_varlen_fp8kv")
     return (out, lse) if return_lse else out
 
 

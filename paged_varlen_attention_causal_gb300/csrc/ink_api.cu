@@ -214,6 +214,19 @@ bool encode(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Element format of the K/V caches.
+struct KvFormat {
+    int fp8;          // 0: bf16; 1: E4M3 bytes (decode-shaped calls only)
+    float k_scale, v_scale;
+};
+
+ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_cache, const void *value_cache,
+                     const KvFormat &kv, const int32_t *block_table, const int32_t *cache_seqlens,
+                     const int32_t *cu_seqlens_q, int32_t max_seqlen_q, float softmax_scale, int causal,
+                     int32_t window_left, int32_t window_right, int32_t rel_extent, const float *rel_logits,
+                     int32_t num_splits, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                     ink_stream_t stream_handle);
+
 }  // namespace
 }  // namespace ink
 
@@ -281,6 +294,38 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
                                const float *rel_logits, int32_t num_splits, void *out, float *lse, void *workspace,
                                size_t workspace_bytes, ink_stream_t stream_handle)
 {
+    return attn_impl(dims, q, key_cache, value_cache, KvFormat{0, 1.f, 1.f}, block_table, cache_seqlens,
+                     cu_seqlens_q, max_seqlen_q, softmax_scale, causal, window_left, window_right, rel_extent,
+                     rel_logits, num_splits, out, lse, workspace, workspace_bytes, stream_handle);
+}
+
+ink_status ink_rel_attn_varlen_fp8kv(const ink_attn_dims *dims, const void *q, const void *key_cache,
+                                     const void *value_cache, float k_scale, float v_scale,
+                                     const int32_t *block_table, const int32_t *cache_seqlens,
+                                     const int32_t *cu_seqlens_q, int32_t max_seqlen_q, float softmax_scale,
+                                     int causal, int32_t window_left, int32_t window_right, int32_t rel_extent,
+                                     const float *rel_logits, int32_t num_splits, void *out, float *lse,
+                                     void *workspace, size_t workspace_bytes, ink_stream_t stream_handle)
+{
+    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return INK_ERR_INVALID_ARG;
+    return attn_impl(dims, q, key_cache, value_cache, KvFormat{1, k_scale, v_scale}, block_table, cache_seqlens,
+                     cu_seqlens_q, max_seqlen_q, softmax_scale, causal, window_left, window_right, rel_extent,
+                     rel_logits, num_splits, out, lse, workspace, workspace_bytes, stream_handle);
+}
+
+}  // extern "C"
+
+namespace ink {
+namespace {
+
+ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_cache, const void *value_cache,
+                     const KvFormat &kv, const int32_t *block_table, const int32_t *cache_seqlens,
+                     const int32_t *cu_seqlens_q, int32_t max_seqlen_q, float softmax_scale, int causal,
+                     int32_t window_left, int32_t window_right, int32_t rel_extent, const float *rel_logits,
+                     int32_t num_splits, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                     ink_stream_t stream_handle)
+{
     if (!dims_ok(dims)) return INK_ERR_INVALID_ARG;
     if (!q || !key_cache || !value_cache || !block_table || !cache_seqlens || !cu_seqlens_q || !out || !workspace)
         return INK_ERR_INVALID_ARG;
@@ -301,6 +346,8 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     Plan pl;
     if (!make_plan(dims, max_seqlen_q, num_splits, causal ? 1 : 0, window_left, window_right, sms, pl))
         return INK_ERR_UNSUPPORTED;
+    // an FP8 cache is read by the decode kernel only: every request must be decode-shaped
+    if (kv.fp8 && (!pl.decode_kernel || pl.any_prefill)) return INK_ERR_UNSUPPORTED;
     if (workspace_bytes < pl.total) return INK_ERR_WORKSPACE;
 
     const int T = dims->num_tokens, H = dims->num_heads, Hkv = dims->num_kv_heads, E = rel_extent;
@@ -347,7 +394,17 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v); memset(&tm_vp, 0, sizeof tm_vp);
     memset(&tm_kd, 0, sizeof tm_kd); memset(&tm_vd, 0, sizeof tm_vd);
     memset(&tm_bdec, 0, sizeof tm_bdec); memset(&tm_bpf, 0, sizeof tm_bpf);
-    {
+    if (kv.fp8) {
+        // E4M3 K and V as (128 d bytes, keys, 1, Hkv): one 128 x 16 x 1 x Hkv box per page lands as
+        // [KV head][16 keys][128 B], 128-byte swizzle
+        const cuuint64_t gd8[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)dims->num_blocks * dims->block_size, 1,
+                                   (cuuint64_t)Hkv};
+        const cuuint64_t gs8[3] = {(cuuint64_t)Hkv * kHeadDim, (cuuint64_t)kHeadDim, (cuuint64_t)kHeadDim};
+        const cuuint32_t box8[4] = {(cuuint32_t)kHeadDim, (cuuint32_t)kKeyGroup, 1, (cuuint32_t)Hkv};
+        if (!encode(&tm_kd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, key_cache, gd8, gs8, box8, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&tm_vd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, value_cache, gd8, gs8, box8, CU_TENSOR_MAP_SWIZZLE_128B))
+            return INK_ERR_CUDA;
+    } else {
         const cuuint64_t gd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv,
                                   (cuuint64_t)dims->num_blocks * dims->block_size};
         const cuuint64_t gs[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hkv * kHeadDim * 2};
@@ -395,18 +452,19 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     if (pl.any_decode && pl.dec_cap > 0) {
         Params pd = p;
         pd.bias_tma = bias_dec_tma ? 1 : 0;
-        const int kv_bytes = Hkv * 4096;
+        const int kv_bytes = Hkv * (kv.fp8 ? 2048 : 4096);  // one 16-key page of K (or V), all KV heads
+        const int scratch = kv.fp8 ? kDecFp8ScratchBytes : 0;
         const int bias_slot = (H * 80 + 127) & ~127;
         const int bias_bytes = (kDecodeRows / pl.G) * bias_slot;
         const int stage_bytes = (2 * kv_bytes + bias_bytes + 1023) & ~1023;
-        int nst = (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
+        int nst = (int)((kSmemLimit - 1024 - scratch - kDecSharedBytes) / stage_bytes);
         nst = std::min(nst, kDecMaxStages);
         if (nst < 2) return INK_ERR_UNSUPPORTED;
-        const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
+        const size_t smem = 1024 + (size_t)nst * stage_bytes + scratch + kDecSharedBytes;
         const int grid = (int)std::min<long long>(sms, pl.dec_cap);
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
-                return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, grid, smem,
-                                     stream);
+                return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, kv.fp8,
+                                     kv.k_scale, kv.v_scale, grid, smem, stream);
             }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
@@ -436,6 +494,11 @@ ink_status ink_rel_attn_varlen(const ink_attn_dims *dims, const void *q, const v
     }
     return INK_OK;
 }
+
+}  // namespace
+}  // namespace ink
+
+extern "C" {
 
 ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, const void *value, void *key_cache,
                                  void *value_cache, const int64_t *slot_mapping, uint32_t *flags,

@@ -20,6 +20,20 @@
 //  * online softmax in the log2 domain with the bias added after the scale
 //    (score = scale * q.k + bias); the result is written directly when the
 //    unit has one split, else as an fp32 partial plus its log-sum-exp.
+//
+// FP8 KV cache (kFp8): pages hold E4M3 bytes, one 2 KB [16 keys][128 B] block
+// per KV head and tensor, and K = k_scale * E4M3, V = v_scale * E4M3.  Every
+// E4M3 value is exact in fp16, so the products run as f16 mma.sync with fp32
+// accumulation (q converted from bf16 to fp16 once per item, p in fp16):
+//  * QK^T: ldmatrix reads the E4M3 key rows as they landed; a thread's
+//    register holds 4 consecutive bytes (d = 16 kk + 4 c .. + 3 of k-step kk),
+//    converted in registers to the two f16 pairs of its B fragment.  q's A
+//    fragment uses the same order of d within each k-step, so the dot product
+//    is unchanged.  Keys keep the bf16 path's order;
+//  * PV: each warp converts its d-slice of the V page to fp16 in a private
+//    4 KB buffer laid out like a bf16 page, and the bf16 path's transposed
+//    ldmatrix reads it;
+//  * k_scale joins the softmax scale and v_scale the final normalisation.
 #include "ink_common.cuh"
 
 namespace ink {
@@ -70,6 +84,69 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit pairs held in the mma fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// Two E4M3 bytes (low byte first) to an f16 pair (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    uint32_t r;
+    const uint16_t h = (uint16_t)(two & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A bf16 pair to an f16 pair (exact for magnitudes in [2^-14, 65504]).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
+{
+    return pack_f16x2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// FP8: this lane's share of a warp's V d-slice, E4M3 -> fp16, from the head's E4M3 block at vsrc into the
+// warp's fp16 page at vdst (offsets precomputed per lane; the second chunk's offset has bit 4 flipped).
+template <int kVIt, int kPairs>
+__device__ __forceinline__ void convert_v_slice(uint32_t vsrc, uint32_t vdst, const uint32_t (&v_src)[kVIt],
+                                                const uint32_t (&v_dst)[kVIt], int lane)
+{
+#pragma unroll
+    for (int i = 0; i < kVIt; ++i) {
+        if (kPairs % 32 == 0 || lane + 32 * i < kPairs) {
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(vsrc + v_src[i]));
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(vdst + v_dst[i]), "r"(e4m3x2_to_f16x2(w0)),
+                         "r"(e4m3x2_to_f16x2(w0 >> 16)), "r"(e4m3x2_to_f16x2(w1)), "r"(e4m3x2_to_f16x2(w1 >> 16))
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"((vdst + v_dst[i]) ^ 16u),
+                         "r"(e4m3x2_to_f16x2(w2)), "r"(e4m3x2_to_f16x2(w2 >> 16)), "r"(e4m3x2_to_f16x2(w3)),
+                         "r"(e4m3x2_to_f16x2(w3 >> 16))
+                         : "memory");
+        }
+    }
+}
+
 // Rows of the bias band touched by group gi for query positions [qa0, qa1].
 __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
 {
@@ -78,15 +155,19 @@ __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
     return E > 0 && rd_max >= 0 && rd_min < E;
 }
 
-template <int kDSlices>  // d-slices per KV head = 8 / Hkv
+static_assert(kDecFp8ScratchBytes == kDecComputeWarps * 4096, "one fp16 V page per compute warp");
+
+template <int kDSlices, bool kFp8>  // d-slices per KV head = 8 / Hkv; E4M3 K/V pages
 __global__ void __launch_bounds__(kDecThreads, 1)
     ink_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
-                      int nstages, int stage_bytes, int kv_bytes, int bias_slot_bytes)
+                      int nstages, int stage_bytes, int kv_bytes, int bias_slot_bytes, float k_scale,
+                      float v_scale)
 {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    DecShared &sh = *reinterpret_cast<DecShared *>(ring + (size_t)nstages * stage_bytes);
+    uint8_t *vscratch = ring + (size_t)nstages * stage_bytes;  // kFp8 only
+    DecShared &sh = *reinterpret_cast<DecShared *>(vscratch + (kFp8 ? kDecFp8ScratchBytes : 0));
     volatile int *abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,6 +281,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const float log2e = 1.4426950408889634f;
     const int rA = lane >> 2, rB = rA + 8;      // the two rows this thread holds
     const int cq = (lane & 3) * 2;              // column pair within an 8-wide tile
+    const int c4 = (lane & 3) * 4;              // FP8: first of the 4 d values of a k-step a thread holds
+    const float scale_log2 = kFp8 ? p.scale_log2 * k_scale : p.scale_log2;
+    // FP8: the (key, 16-d chunk) pairs of this warp's d-slice that this lane converts on every page, as
+    // byte offsets into the head's E4M3 V block and into the warp's fp16 page (chunk pair c8, c8 + 1:
+    // the second offset is the first with bit 4 flipped)
+    constexpr int kVCh = kDW / 16;
+    constexpr int kVIt = (kKeyGroup * kVCh + 31) / 32;
+    uint32_t v_src[kVIt], v_dst[kVIt];
+#pragma unroll
+    for (int i = 0; i < kVIt; ++i) {
+        const int idx = lane + 32 * i;  // 8 consecutive lanes: 8 keys of one chunk (no bank conflicts)
+        const int key = idx & (kKeyGroup - 1), d = d0 + 16 * ((idx >> 4) % kVCh);
+        v_src[i] = key * 128 + (((d >> 4) ^ (key & 7)) << 4);
+        v_dst[i] = (d >> 6) * 2048 + key * 128 + ((((d & 63) >> 3) ^ (key & 7)) << 4);
+    }
 
     uint32_t n = 0;
     for (uint32_t iseq = 0;; ++iseq) {
@@ -212,6 +308,237 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
         const int rows = it.Lq * G;
         const int qa0 = it.Lk - it.Lq, qa1 = it.Lk - 1;
+
+        if (rows <= 8) {
+            // ---- at most 8 packed rows: S^T = K Q^T and O^T += V^T P^T, so the 16 keys of a page fill
+            // the mma's M and the rows its N = 8 (half the mma and softmax work of the 16-row block).
+            // Fragments: this thread's S^T / O^T accumulators hold rows 2t and 2t + 1 at keys (or d)
+            // gq and gq + 8; its Q^T and P^T fragments hold row gq.
+            const int gq = lane >> 2, t = lane & 3;
+            const int r0 = 2 * t, r1 = 2 * t + 1;
+            const bool v0 = r0 < rows, v1 = r1 < rows, vq = gq < rows;
+            const int tok0 = r0 / G, tok1 = r1 / G, tokq = gq / G;
+            const int h0 = g * G + r0 % G, h1 = g * G + r1 % G, hq = g * G + gq % G;
+            const int qa_0 = qa0 + tok0, qa_1 = qa0 + tok1;
+            int lo0, hi0, lo1, hi1, nlo, nhi, tmp;
+            visible_range(qa_0, qa_0, it.Lk, p.causal, p.wl, p.wr, lo0, hi0);
+            visible_range(qa_1, qa_1, it.Lk, p.causal, p.wl, p.wr, lo1, hi1);
+            if (!v0) { lo0 = 1; hi0 = 0; }
+            if (!v1) { lo1 = 1; hi1 = 0; }
+            visible_range(qa1, qa1, it.Lk, p.causal, p.wl, p.wr, nlo, tmp);
+            visible_range(qa0, qa0, it.Lk, p.causal, p.wl, p.wr, tmp, nhi);
+
+            // Q^T fragments (B operand) of row gq, 8 k-steps over d
+            uint32_t qb[8][2];
+            {
+                const uint32_t *q_row =
+                    reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokq) * H + hq) * kHeadDim);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    if constexpr (kFp8) {  // d = 16 kk + 4t + {0,1} and + {2,3}: the E4M3 rows' order
+                        const uint2 u = vq ? __ldg(reinterpret_cast<const uint2 *>(q_row + 8 * kk + 2 * t))
+                                           : make_uint2(0u, 0u);
+                        qb[kk][0] = bf16x2_to_f16x2(u.x);
+                        qb[kk][1] = bf16x2_to_f16x2(u.y);
+                    } else {
+                        qb[kk][0] = vq ? __ldg(q_row + 8 * kk + t) : 0u;
+                        qb[kk][1] = vq ? __ldg(q_row + 8 * kk + t + 4) : 0u;
+                    }
+                }
+            }
+            constexpr int kMT = kDW / 16;  // m-tiles (16 d) of this warp's slice in the PV product
+            float o[kMT][4];
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+            const float *rel0 = p.rel ? p.rel + ((size_t)(it.t0 + tok0) * H + h0) * p.E : nullptr;
+            const float *rel1 = p.rel ? p.rel + ((size_t)(it.t0 + tok1) * H + h1) * p.E : nullptr;
+            const int lkey = (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix row of this lane (K)
+
+            for (int gi = it.gb; gi < it.ge; ++gi, ++n) {
+                const int stage = n % nstages;
+                if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
+                const uint8_t *st = ring + (size_t)stage * stage_bytes;
+                const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
+                uint32_t vbase = kbase + kv_bytes;
+                if constexpr (kFp8) {
+                    const uint32_t vsrc = vbase;
+                    vbase = smem_u32(vscratch) + warp * 4096;
+                    convert_v_slice<kVIt, kKeyGroup * kVCh>(vsrc, vbase, v_src, v_dst, lane);
+                    __syncwarp();
+                }
+
+                // S^T = K Q^T (16 keys x 8 rows); even and odd k-steps in two accumulators (shorter chains)
+                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int kp = 0; kp < 4; ++kp) {  // k-steps 2kp, 2kp + 1: E4M3 chunks 2kp + (lane >> 4)
+                        const int chunk = 2 * kp + (lane >> 4);
+                        uint32_t r[4];
+                        ldsm_x4(kbase + lkey * 128 + ((chunk ^ (lkey & 7)) << 4), r[0], r[1], r[2], r[3]);
+                        const uint32_t a0[4] = {e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[1]),
+                                                e4m3x2_to_f16x2(r[0] >> 16), e4m3x2_to_f16x2(r[1] >> 16)};
+                        mma_f16(sc, a0, qb[2 * kp][0], qb[2 * kp][1]);
+                        const uint32_t a1[4] = {e4m3x2_to_f16x2(r[2]), e4m3x2_to_f16x2(r[3]),
+                                                e4m3x2_to_f16x2(r[2] >> 16), e4m3x2_to_f16x2(r[3] >> 16)};
+                        mma_f16(sd, a1, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int chunk = ((kk & 3) << 1) + (lane >> 4);
+                        uint32_t a[4];
+                        ldsm_x4(kbase + (kk >> 2) * 2048 + lkey * 128 + ((chunk ^ (lkey & 7)) << 4), a[0], a[1],
+                                a[2], a[3]);
+                        mma_bf16((kk & 1) ? sd : sc, a, qb[kk][0], qb[kk][1]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+                // sc[e]: row (e & 1 ? r1 : r0), key gq + 8 * (e >> 1)
+                const int kbase_key = gi * kKeyGroup;
+                const bool band = group_in_band(qa0, qa1, gi, p.E);
+                const bool need_mask = (kbase_key < nlo) || (kbase_key + kKeyGroup - 1 > nhi);
+                const float *bsm = reinterpret_cast<const float *>(st + 2 * kv_bytes);
+                float x[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool second = e & 1;
+                    const int key = kbase_key + gq + 8 * (e >> 1);
+                    float v = sc[e] * scale_log2;
+                    if (band) {
+                        const int qa = second ? qa_1 : qa_0;
+                        const int rd = qa - key;
+                        float bias = 0.f;
+                        if (p.bias_tma) {
+                            const int x0 = floor4(qa - (kbase_key + kKeyGroup - 1));
+                            if (second ? v1 : v0)
+                                bias = bsm[((second ? tok1 : tok0) * bias_slot_bytes) / 4 + (second ? h1 : h0) * 20 +
+                                           (rd - x0)];
+                        } else if (rd >= 0 && rd < p.E && (second ? v1 : v0)) {
+                            bias = __ldg((second ? rel1 : rel0) + rd);
+                        }
+                        v = fmaf(bias, log2e, v);
+                    }
+                    if (need_mask) {
+                        const int lo = second ? lo1 : lo0, hi = second ? hi1 : hi0;
+                        if (key < lo || key > hi) v = -INFINITY;
+                    }
+                    x[e] = v;
+                }
+                // row maxima over the page: this thread's two keys, then the 8 lanes with the same t
+                float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+                    t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+                }
+                if (t0 > m0) {
+                    const float alpha = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - t0);
+                    m0 = t0;
+                    l0 *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < kMT; ++mt) { o[mt][0] *= alpha; o[mt][2] *= alpha; }
+                }
+                if (t1 > m1) {
+                    const float alpha = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - t1);
+                    m1 = t1;
+                    l1 *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < kMT; ++mt) { o[mt][1] *= alpha; o[mt][3] *= alpha; }
+                }
+                const float sub0 = (m0 == -INFINITY) ? 0.f : m0;
+                const float sub1 = (m1 == -INFINITY) ? 0.f : m1;
+                const float p0 = fast_exp2(x[0] - sub0), p1 = fast_exp2(x[1] - sub1);
+                const float p2 = fast_exp2(x[2] - sub0), p3 = fast_exp2(x[3] - sub1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // P^T fragments (B operand of PV): the two 8-key blocks of P, transposed in registers
+                const uint32_t pb0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+                const uint32_t pb1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+
+                // O^T += V^T P^T over this warp's d-slice, one m-tile of 16 d at a time
+                {
+                    const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
+                    const int vkey = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+                    for (int mt = 0; mt < kMT; ++mt) {
+                        const int d = d0 + 16 * mt;
+                        const int chunk = ((d & 63) >> 3) + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldsm_x4_t(vbase + (d >> 6) * 2048 + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), a[0], a[1],
+                                  a[2], a[3]);
+                        if (tail < kKeyGroup) {  // zero V entries of keys past the cache length
+                            const int k0 = 2 * t, k1 = 2 * t + 8;
+                            if (k0 >= tail) { a[0] &= 0xffff0000u; a[1] &= 0xffff0000u; }
+                            if (k0 + 1 >= tail) { a[0] &= 0x0000ffffu; a[1] &= 0x0000ffffu; }
+                            if (k1 >= tail) { a[2] &= 0xffff0000u; a[3] &= 0xffff0000u; }
+                            if (k1 + 1 >= tail) { a[2] &= 0x0000ffffu; a[3] &= 0x0000ffffu; }
+                        }
+                        if constexpr (kFp8) mma_f16(o[mt], a, pb0, pb1);
+                        else mma_bf16(o[mt], a, pb0, pb1);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.empty[stage]);
+            }
+            if (*abort) break;
+
+            // epilogue: row sums over the 8 lanes that share t, then rows r0 / r1 at d = d0 + 16 mt + gq (+ 8)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
+            const float ln2 = 0.6931471805599453f;
+            float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+            if constexpr (kFp8) {
+                inv0 *= v_scale;
+                inv1 *= v_scale;
+            }
+            const float lse0 = l0 > 0.f ? (m0 + __log2f(l0)) * ln2 : -INFINITY;
+            const float lse1 = l1 > 0.f ? (m1 + __log2f(l1)) * ln2 : -INFINITY;
+            const size_t row0 = (size_t)(it.t0 + tok0) * H + h0, row1 = (size_t)(it.t0 + tok1) * H + h1;
+            if (it.nact == 1) {
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const int d = d0 + 16 * mt + gq;
+                    if (v0) {
+                        p.out[row0 * kHeadDim + d] = __float2bfloat16_rn(o[mt][0] * inv0);
+                        p.out[row0 * kHeadDim + d + 8] = __float2bfloat16_rn(o[mt][2] * inv0);
+                    }
+                    if (v1) {
+                        p.out[row1 * kHeadDim + d] = __float2bfloat16_rn(o[mt][1] * inv1);
+                        p.out[row1 * kHeadDim + d + 8] = __float2bfloat16_rn(o[mt][3] * inv1);
+                    }
+                }
+                if (p.lse && dsl == 0 && gq == 0) {
+                    if (v0) p.lse[row0] = lse0;
+                    if (v1) p.lse[row1] = lse1;
+                }
+            } else {
+                const size_t blk = (size_t)it.index * p.dec_rows;
+                const size_t pr0 = blk + (size_t)tok0 * H + h0, pr1 = blk + (size_t)tok1 * H + h1;
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const int d = d0 + 16 * mt + gq;
+                    if (v0) {
+                        p.part_dec_o[pr0 * kHeadDim + d] = o[mt][0] * inv0;
+                        p.part_dec_o[pr0 * kHeadDim + d + 8] = o[mt][2] * inv0;
+                    }
+                    if (v1) {
+                        p.part_dec_o[pr1 * kHeadDim + d] = o[mt][1] * inv1;
+                        p.part_dec_o[pr1 * kHeadDim + d + 8] = o[mt][3] * inv1;
+                    }
+                }
+                if (dsl == 0 && gq == 0) {
+                    if (v0) p.part_dec_lse[pr0] = lse0;
+                    if (v1) p.part_dec_lse[pr1] = lse1;
+                }
+            }
+            continue;
+        }
+
         // per-row geometry
         int tokA = rA / G, tokB = rB / G;
         const bool vA = rA < rows, vB = rB < rows;
@@ -231,13 +558,27 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         {
             const uint32_t *qa_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokA) * H + hA) * kHeadDim);
             const uint32_t *qb_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokB) * H + hB) * kHeadDim);
+            if constexpr (kFp8) {
+                // fp16, d = 16 kk + c4 + {0,1} in a0 / a1 and + {2,3} in a2 / a3 (the key rows' order)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int c = (kk * 16 + cq) >> 1;
-                qf[kk][0] = vA ? __ldg(qa_row + c) : 0u;
-                qf[kk][1] = vB ? __ldg(qb_row + c) : 0u;
-                qf[kk][2] = vA ? __ldg(qa_row + c + 4) : 0u;
-                qf[kk][3] = vB ? __ldg(qb_row + c + 4) : 0u;
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int c = (kk * 16 + c4) >> 1;
+                    const uint2 ua = vA ? __ldg(reinterpret_cast<const uint2 *>(qa_row + c)) : make_uint2(0u, 0u);
+                    const uint2 ub = vB ? __ldg(reinterpret_cast<const uint2 *>(qb_row + c)) : make_uint2(0u, 0u);
+                    qf[kk][0] = bf16x2_to_f16x2(ua.x);
+                    qf[kk][1] = bf16x2_to_f16x2(ub.x);
+                    qf[kk][2] = bf16x2_to_f16x2(ua.y);
+                    qf[kk][3] = bf16x2_to_f16x2(ub.y);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int c = (kk * 16 + cq) >> 1;
+                    qf[kk][0] = vA ? __ldg(qa_row + c) : 0u;
+                    qf[kk][1] = vB ? __ldg(qb_row + c) : 0u;
+                    qf[kk][2] = vA ? __ldg(qa_row + c + 4) : 0u;
+                    qf[kk][3] = vB ? __ldg(qb_row + c + 4) : 0u;
+                }
             }
         }
         float o[kNT][4];
@@ -251,14 +592,38 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const int stage = n % nstages;
             if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
             const uint8_t *st = ring + (size_t)stage * stage_bytes;
-            const uint32_t kbase = smem_u32(st) + g * 4096;
-            const uint32_t vbase = kbase + kv_bytes;
+            const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
+            uint32_t vbase = kbase + kv_bytes;
+
+            if constexpr (kFp8) {
+                // this warp's d-slice of the V page, E4M3 -> fp16, into its own buffer in the bf16 page
+                // layout ([d half][16 keys][128 B], 16-byte chunks swizzled by key & 7)
+                const uint32_t vsrc = vbase;
+                vbase = smem_u32(vscratch) + warp * 4096;
+                convert_v_slice<kVIt, kKeyGroup * kVCh>(vsrc, vbase, v_src, v_dst, lane);
+                __syncwarp();
+            }
 
             // S = Q K^T for 16 keys (2 n-tiles)
             float s[2][4];
 #pragma unroll
             for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-            {
+            if constexpr (kFp8) {
+                const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int key = rr + 8 * j;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int chunk = 4 * h + mi;  // matrix mi = 16-d chunk 4h + mi = k-step
+                        uint32_t r[4];
+                        ldsm_x4(kbase + key * 128 + ((chunk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            mma_f16(s[j], qf[4 * h + i], e4m3x2_to_f16x2(r[i]), e4m3x2_to_f16x2(r[i] >> 16));
+                    }
+                }
+            } else {
                 const int mi = lane >> 3, rr = lane & 7;
                 const int key = rr + 8 * (mi >> 1);
 #pragma unroll
@@ -284,7 +649,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const int key = kbase_key + j * 8 + cq + (e & 1);
                     const bool rowB = e >= 2;
-                    float v = s[j][e] * p.scale_log2;
+                    float v = s[j][e] * scale_log2;
                     if (band) {
                         const int qa = rowB ? qaB : qaA;
                         const int rd = qa - key;
@@ -341,10 +706,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 lB += pr[j][2] + pr[j][3];
             }
             uint32_t pa[4];
-            pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
-            pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
-            pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
-            pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            if constexpr (kFp8) {
+                pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
+                pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
+                pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
+                pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
+            } else {
+                pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+                pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+                pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+                pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+            }
 
             // O += P V over this warp's d-slice
             {
@@ -366,8 +738,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                         if (k1 >= tail) { b1 &= 0xffff0000u; b3 &= 0xffff0000u; }
                         if (k1 + 1 >= tail) { b1 &= 0x0000ffffu; b3 &= 0x0000ffffu; }
                     }
-                    mma_bf16(o[2 * jj], pa, b0, b1);
-                    mma_bf16(o[2 * jj + 1], pa, b2, b3);
+                    if constexpr (kFp8) {
+                        mma_f16(o[2 * jj], pa, b0, b1);
+                        mma_f16(o[2 * jj + 1], pa, b2, b3);
+                    } else {
+                        mma_bf16(o[2 * jj], pa, b0, b1);
+                        mma_bf16(o[2 * jj + 1], pa, b2, b3);
+                    }
                 }
             }
             __syncwarp();
@@ -381,8 +758,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         lB += __shfl_xor_sync(0xffffffffu, lB, 1);
         lB += __shfl_xor_sync(0xffffffffu, lB, 2);
         const float ln2 = 0.6931471805599453f;
-        const float invA = lA > 0.f ? 1.f / lA : 0.f;
-        const float invB = lB > 0.f ? 1.f / lB : 0.f;
+        float invA = lA > 0.f ? 1.f / lA : 0.f;
+        float invB = lB > 0.f ? 1.f / lB : 0.f;
+        if constexpr (kFp8) {
+            invA *= v_scale;
+            invB *= v_scale;
+        }
         const float lseA = lA > 0.f ? (mA + __log2f(lA)) * ln2 : -INFINITY;
         const float lseB = lB > 0.f ? (mB + __log2f(lB)) * ln2 : -INFINITY;
         const size_t rowA = (size_t)(it.t0 + tokA) * H + hA;
@@ -418,20 +799,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,
-                          int bias_slot_bytes, int grid, size_t smem, cudaStream_t stream)
+                          int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int grid, size_t smem,
+                          cudaStream_t stream)
 {
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kernel<<<grid, kDecThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias, nstages, stage_bytes, kv_bytes,
-                                                    bias_slot_bytes);
+                                                    bias_slot_bytes, k_scale, v_scale);
         return cudaGetLastError();
     };
+    if (kv_fp8) {
+        switch (8 / p.Hkv) {
+            case 1: return go(ink_decode_kernel<1, true>);
+            case 2: return go(ink_decode_kernel<2, true>);
+            case 4: return go(ink_decode_kernel<4, true>);
+            default: return go(ink_decode_kernel<8, true>);
+        }
+    }
     switch (8 / p.Hkv) {
-        case 1: return go(ink_decode_kernel<1>);
-        case 2: return go(ink_decode_kernel<2>);
-        case 4: return go(ink_decode_kernel<4>);
-        default: return go(ink_decode_kernel<8>);
+        case 1: return go(ink_decode_kernel<1, false>);
+        case 2: return go(ink_decode_kernel<2, false>);
+        case 4: return go(ink_decode_kernel<4, false>);
+        default: return go(ink_decode_kernel<8, false>);
     }
 }
 

@@ -113,3 +113,28 @@ def test_append_host_validation(lib):
     assert f(ctypes.byref(bad), good, good, good, good, good, None, None) == 2           # head_dim 64
     empty = ink.Dims(0, 1, 4, 4, 128, 16, 16, 1)
     assert f(ctypes.byref(empty), good, good, good, good, good, None, None) == 0         # nothing to do
+
+
+def test_fp8_entry_host_validation(lib):
+    """ink_rel_attn_varlen_fp8kv rejects bad scales, pointers and shapes before touching the GPU."""
+    import ctypes
+
+    f = lib.ink_rel_attn_varlen_fp8kv
+    f.restype = ctypes.c_int
+    vp, i32, fl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    f.argtypes = [ctypes.POINTER(ink.Dims), vp, vp, vp, fl, fl, vp, vp, vp, i32, fl, ctypes.c_int, i32, i32, i32,
+                  vp, i32, vp, vp, vp, ctypes.c_size_t, vp]
+    good = 0x10000
+    dims = ink.Dims(4, 2, 8, 2, 128, 16, 16, 4)
+
+    def call(ks=0.5, vs=0.5, q=good, d=dims, scale=0.1):
+        return f(ctypes.byref(d), q, good, good, ks, vs, good, good, good, 2, scale, 1, -1, -1, 0, None, 0,
+                 good, None, good, 1 << 20, None)
+
+    for ks, vs in [(0.0, 1.0), (1.0, 0.0), (-2.0, 1.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+        assert call(ks, vs) == 1
+    assert call(q=None) == 1                                   # null q
+    assert call(q=good + 2) == 1                               # misaligned q
+    assert call(scale=0.0) == 1                                # softmax_scale must be > 0
+    assert call(d=ink.Dims(4, 2, 8, 2, 64, 16, 16, 4)) == 2    # head_dim 64
+    assert call(d=ink.Dims(0, 2, 8, 2, 128, 16, 16, 4)) == 0   # nothing to do
