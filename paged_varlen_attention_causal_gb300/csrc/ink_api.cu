@@ -453,14 +453,13 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         Params pd = p;
         pd.bias_tma = bias_dec_tma ? 1 : 0;
         const int kv_bytes = Hkv * (kv.fp8 ? 2048 : 4096);  // one 16-key page of K (or V), all KV heads
-        const int scratch = kv.fp8 ? kDecFp8ScratchBytes : 0;
         const int bias_slot = (H * 80 + 127) & ~127;
         const int bias_bytes = (kDecodeRows / pl.G) * bias_slot;
         const int stage_bytes = (2 * kv_bytes + bias_bytes + 1023) & ~1023;
-        int nst = (int)((kSmemLimit - 1024 - scratch - kDecSharedBytes) / stage_bytes);
+        int nst = (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
         nst = std::min(nst, kDecMaxStages);
         if (nst < 2) return INK_ERR_UNSUPPORTED;
-        const size_t smem = 1024 + (size_t)nst * stage_bytes + scratch + kDecSharedBytes;
+        const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
         const int grid = (int)std::min<long long>(sms, pl.dec_cap);
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
                 return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, kv.fp8,

@@ -350,9 +350,6 @@ __device__ __forceinline__ float fast_exp2(float x)
 
 // Host-side launchers, one per translation unit (ink_api.cu calls these).
 cudaError_t launch_prepass(const Params &p, cudaStream_t stream);
-// Decode kernel with an FP8 cache: one fp16 V page (4 KB) per compute warp after the ring.
-constexpr int kDecFp8ScratchBytes = 8 * 4096;
-
 // kv_fp8: K/V pages are E4M3 bytes dequantized with k_scale / v_scale (decode kernel only).
 cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,

@@ -123,28 +123,17 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u)
     return pack_f16x2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// FP8: this lane's share of a warp's V d-slice, E4M3 -> fp16, from the head's E4M3 block at vsrc into the
-// warp's fp16 page at vdst (offsets precomputed per lane; the second chunk's offset has bit 4 flipped).
-template <int kVIt, int kPairs>
-__device__ __forceinline__ void convert_v_slice(uint32_t vsrc, uint32_t vdst, const uint32_t (&v_src)[kVIt],
-                                                const uint32_t (&v_dst)[kVIt], int lane)
+// E4M3 bytes 0 and 2 (even) or 1 and 3 (odd) of a word as an f16 pair.  ldmatrix.trans over E4M3 rows read as
+// 16-bit pairs gives a thread keys k, k + 1 at two adjacent d (bytes: [k][d], [k][d+1], [k+1][d], [k+1][d+1]);
+// the even bytes are the (k, k + 1) pair at d, the odd bytes the pair at d + 1.
+__device__ __forceinline__ uint32_t e4m3_even_f16x2(uint32_t w) { return e4m3x2_to_f16x2(__byte_perm(w, 0u, 0x0020)); }
+__device__ __forceinline__ uint32_t e4m3_odd_f16x2(uint32_t w) { return e4m3x2_to_f16x2(__byte_perm(w, 0u, 0x0031)); }
+
+// Zero the halves of a key-pair register (keys k, k + 1) whose keys are at or past `tail`.
+__device__ __forceinline__ void mask_key_pair(uint32_t &x, int k, int tail)
 {
-#pragma unroll
-    for (int i = 0; i < kVIt; ++i) {
-        if (kPairs % 32 == 0 || lane + 32 * i < kPairs) {
-            uint32_t w0, w1, w2, w3;
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                         : "r"(vsrc + v_src[i]));
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(vdst + v_dst[i]), "r"(e4m3x2_to_f16x2(w0)),
-                         "r"(e4m3x2_to_f16x2(w0 >> 16)), "r"(e4m3x2_to_f16x2(w1)), "r"(e4m3x2_to_f16x2(w1 >> 16))
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"((vdst + v_dst[i]) ^ 16u),
-                         "r"(e4m3x2_to_f16x2(w2)), "r"(e4m3x2_to_f16x2(w2 >> 16)), "r"(e4m3x2_to_f16x2(w3)),
-                         "r"(e4m3x2_to_f16x2(w3 >> 16))
-                         : "memory");
-        }
-    }
+    if (k >= tail) x &= 0xffff0000u;
+    if (k + 1 >= tail) x &= 0x0000ffffu;
 }
 
 // Rows of the bias band touched by group gi for query positions [qa0, qa1].
@@ -155,8 +144,6 @@ __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
     return E > 0 && rd_max >= 0 && rd_min < E;
 }
 
-static_assert(kDecFp8ScratchBytes == kDecComputeWarps * 4096, "one fp16 V page per compute warp");
-
 template <int kDSlices, bool kFp8>  // d-slices per KV head = 8 / Hkv; E4M3 K/V pages
 __global__ void __launch_bounds__(kDecThreads, 1)
     ink_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
@@ -166,8 +153,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    uint8_t *vscratch = ring + (size_t)nstages * stage_bytes;  // kFp8 only
-    DecShared &sh = *reinterpret_cast<DecShared *>(vscratch + (kFp8 ? kDecFp8ScratchBytes : 0));
+    DecShared &sh = *reinterpret_cast<DecShared *>(ring + (size_t)nstages * stage_bytes);
     volatile int *abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,20 +269,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int cq = (lane & 3) * 2;              // column pair within an 8-wide tile
     const int c4 = (lane & 3) * 4;              // FP8: first of the 4 d values of a k-step a thread holds
     const float scale_log2 = kFp8 ? p.scale_log2 * k_scale : p.scale_log2;
-    // FP8: the (key, 16-d chunk) pairs of this warp's d-slice that this lane converts on every page, as
-    // byte offsets into the head's E4M3 V block and into the warp's fp16 page (chunk pair c8, c8 + 1:
-    // the second offset is the first with bit 4 flipped)
-    constexpr int kVCh = kDW / 16;
-    constexpr int kVIt = (kKeyGroup * kVCh + 31) / 32;
-    uint32_t v_src[kVIt], v_dst[kVIt];
-#pragma unroll
-    for (int i = 0; i < kVIt; ++i) {
-        const int idx = lane + 32 * i;  // 8 consecutive lanes: 8 keys of one chunk (no bank conflicts)
-        const int key = idx & (kKeyGroup - 1), d = d0 + 16 * ((idx >> 4) % kVCh);
-        v_src[i] = key * 128 + (((d >> 4) ^ (key & 7)) << 4);
-        v_dst[i] = (d >> 6) * 2048 + key * 128 + ((((d & 63) >> 3) ^ (key & 7)) << 4);
-    }
-
+    // FP8 V: 32-d blocks of this warp's d-slice read per ldmatrix.trans, and the offset of a block's second
+    // 16 d (0 when the slice is only 16 d wide: the second half then repeats the first and is not used)
+    constexpr int kVB = kDW >= 32 ? kDW / 32 : 1;
+    constexpr int kDSec = kDW >= 32 ? 16 : 0;
     uint32_t n = 0;
     for (uint32_t iseq = 0;; ++iseq) {
         const int slot = iseq & 1;
@@ -346,7 +322,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                 }
             }
-            constexpr int kMT = kDW / 16;  // m-tiles (16 d) of this warp's slice in the PV product
+            // m-tiles (16 rows of O^T) of this warp's slice in the PV product; E4M3: tile 2vb holds d = D + 2gq
+            // (+ 16) of 32-d block vb at D, tile 2vb + 1 the odd d next to them
+            constexpr int kMT = kFp8 ? 2 * kVB : kDW / 16;
             float o[kMT][4];
 #pragma unroll
             for (int mt = 0; mt < kMT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -360,13 +338,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
                 const uint8_t *st = ring + (size_t)stage * stage_bytes;
                 const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
-                uint32_t vbase = kbase + kv_bytes;
-                if constexpr (kFp8) {
-                    const uint32_t vsrc = vbase;
-                    vbase = smem_u32(vscratch) + warp * 4096;
-                    convert_v_slice<kVIt, kKeyGroup * kVCh>(vsrc, vbase, v_src, v_dst, lane);
-                    __syncwarp();
-                }
+                const uint32_t vbase = kbase + kv_bytes;
 
                 // S^T = K Q^T (16 keys x 8 rows); even and odd k-steps in two accumulators (shorter chains)
                 float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -457,8 +429,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const uint32_t pb0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
                 const uint32_t pb1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
 
-                // O^T += V^T P^T over this warp's d-slice, one m-tile of 16 d at a time
-                {
+                // O^T += V^T P^T over this warp's d-slice
+                if constexpr (kFp8) {
+                    // E4M3 V^T operands straight from the landed rows: matrices (keys 0-7 | 8-15) x (d D | D + 16)
+                    const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
+                    const int vkey = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+                    for (int vb = 0; vb < kVB; ++vb) {
+                        const int chunk = (d0 + 32 * vb + ((lane >> 3) & 1) * kDSec) >> 4;
+                        uint32_t r[4];
+                        ldsm_x4_t(vbase + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), r[0], r[1], r[2], r[3]);
+                        if (tail < kKeyGroup) {
+                            mask_key_pair(r[0], 2 * t, tail);
+                            mask_key_pair(r[1], 2 * t, tail);
+                            mask_key_pair(r[2], 2 * t + 8, tail);
+                            mask_key_pair(r[3], 2 * t + 8, tail);
+                        }
+                        const uint32_t ae[4] = {e4m3_even_f16x2(r[0]), e4m3_even_f16x2(r[1]), e4m3_even_f16x2(r[2]),
+                                                e4m3_even_f16x2(r[3])};
+                        const uint32_t ao[4] = {e4m3_odd_f16x2(r[0]), e4m3_odd_f16x2(r[1]), e4m3_odd_f16x2(r[2]),
+                                                e4m3_odd_f16x2(r[3])};
+                        mma_f16(o[2 * vb], ae, pb0, pb1);
+                        mma_f16(o[2 * vb + 1], ao, pb0, pb1);
+                    }
+                } else {  // one m-tile of 16 d at a time
                     const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
                     const int vkey = (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
@@ -475,8 +469,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                             if (k1 >= tail) { a[2] &= 0xffff0000u; a[3] &= 0xffff0000u; }
                             if (k1 + 1 >= tail) { a[2] &= 0x0000ffffu; a[3] &= 0x0000ffffu; }
                         }
-                        if constexpr (kFp8) mma_f16(o[mt], a, pb0, pb1);
-                        else mma_bf16(o[mt], a, pb0, pb1);
+                        mma_bf16(o[mt], a, pb0, pb1);
                     }
                 }
                 __syncwarp();
@@ -499,7 +492,35 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const float lse0 = l0 > 0.f ? (m0 + __log2f(l0)) * ln2 : -INFINITY;
             const float lse1 = l1 > 0.f ? (m1 + __log2f(l1)) * ln2 : -INFINITY;
             const size_t row0 = (size_t)(it.t0 + tok0) * H + h0, row1 = (size_t)(it.t0 + tok1) * H + h1;
-            if (it.nact == 1) {
+            if constexpr (kFp8) {  // tiles 2vb / 2vb + 1: the even / odd d of pair gq, at D and D + 16
+                const size_t blk = (size_t)it.index * p.dec_rows;
+                const size_t pr0 = blk + (size_t)tok0 * H + h0, pr1 = blk + (size_t)tok1 * H + h1;
+#pragma unroll
+                for (int vb = 0; vb < kVB; ++vb) {
+#pragma unroll
+                    for (int sec = 0; sec < (kDSec ? 2 : 1); ++sec) {
+                        const int d = d0 + 32 * vb + 16 * sec + 2 * gq;
+                        const float e0 = o[2 * vb][2 * sec] * inv0, f0 = o[2 * vb + 1][2 * sec] * inv0;
+                        const float e1 = o[2 * vb][2 * sec + 1] * inv1, f1 = o[2 * vb + 1][2 * sec + 1] * inv1;
+                        if (it.nact == 1) {
+                            if (v0) *reinterpret_cast<uint32_t *>(p.out + row0 * kHeadDim + d) = pack_bf16x2(e0, f0);
+                            if (v1) *reinterpret_cast<uint32_t *>(p.out + row1 * kHeadDim + d) = pack_bf16x2(e1, f1);
+                        } else {
+                            if (v0) *reinterpret_cast<float2 *>(p.part_dec_o + pr0 * kHeadDim + d) = make_float2(e0, f0);
+                            if (v1) *reinterpret_cast<float2 *>(p.part_dec_o + pr1 * kHeadDim + d) = make_float2(e1, f1);
+                        }
+                    }
+                }
+                if (dsl == 0 && gq == 0) {
+                    if (it.nact == 1) {
+                        if (p.lse && v0) p.lse[row0] = lse0;
+                        if (p.lse && v1) p.lse[row1] = lse1;
+                    } else {
+                        if (v0) p.part_dec_lse[pr0] = lse0;
+                        if (v1) p.part_dec_lse[pr1] = lse1;
+                    }
+                }
+            } else if (it.nact == 1) {
 #pragma unroll
                 for (int mt = 0; mt < kMT; ++mt) {
                     const int d = d0 + 16 * mt + gq;
@@ -593,16 +614,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
             const uint8_t *st = ring + (size_t)stage * stage_bytes;
             const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
-            uint32_t vbase = kbase + kv_bytes;
-
-            if constexpr (kFp8) {
-                // this warp's d-slice of the V page, E4M3 -> fp16, into its own buffer in the bf16 page
-                // layout ([d half][16 keys][128 B], 16-byte chunks swizzled by key & 7)
-                const uint32_t vsrc = vbase;
-                vbase = smem_u32(vscratch) + warp * 4096;
-                convert_v_slice<kVIt, kKeyGroup * kVCh>(vsrc, vbase, v_src, v_dst, lane);
-                __syncwarp();
-            }
+            const uint32_t vbase = kbase + kv_bytes;
 
             // S = Q K^T for 16 keys (2 n-tiles)
             float s[2][4];
@@ -719,7 +731,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
 
             // O += P V over this warp's d-slice
-            {
+            if constexpr (kFp8) {
+                // E4M3 V operands straight from the landed rows: matrices (keys 0-7 | 8-15) x (d D | D + 16);
+                // n-tile 4vb (+2 for D + 16) holds d = D + 2n, n-tile 4vb + 1 (+2) holds d = D + 2n + 1
+                const int tail = it.Lk - kbase_key;
+                const int vkey = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+                for (int vb = 0; vb < kVB; ++vb) {
+                    const int chunk = (d0 + 32 * vb + (lane >> 4) * kDSec) >> 4;
+                    uint32_t r[4];
+                    ldsm_x4_t(vbase + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), r[0], r[1], r[2], r[3]);
+                    if (tail < kKeyGroup) {
+                        mask_key_pair(r[0], cq, tail);
+                        mask_key_pair(r[1], cq + 8, tail);
+                        mask_key_pair(r[2], cq, tail);
+                        mask_key_pair(r[3], cq + 8, tail);
+                    }
+                    mma_f16(o[4 * vb], pa, e4m3_even_f16x2(r[0]), e4m3_even_f16x2(r[1]));
+                    mma_f16(o[4 * vb + 1], pa, e4m3_odd_f16x2(r[0]), e4m3_odd_f16x2(r[1]));
+                    if constexpr (kDSec != 0) {
+                        mma_f16(o[4 * vb + 2], pa, e4m3_even_f16x2(r[2]), e4m3_even_f16x2(r[3]));
+                        mma_f16(o[4 * vb + 3], pa, e4m3_odd_f16x2(r[2]), e4m3_odd_f16x2(r[3]));
+                    }
+                }
+            } else {
                 const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
                 const int mi = lane >> 3, rr = lane & 7;
                 const int key = rr + 8 * (mi & 1);
@@ -738,13 +773,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                         if (k1 >= tail) { b1 &= 0xffff0000u; b3 &= 0xffff0000u; }
                         if (k1 + 1 >= tail) { b1 &= 0x0000ffffu; b3 &= 0x0000ffffu; }
                     }
-                    if constexpr (kFp8) {
-                        mma_f16(o[2 * jj], pa, b0, b1);
-                        mma_f16(o[2 * jj + 1], pa, b2, b3);
-                    } else {
-                        mma_bf16(o[2 * jj], pa, b0, b1);
-                        mma_bf16(o[2 * jj + 1], pa, b2, b3);
-                    }
+                    mma_bf16(o[2 * jj], pa, b0, b1);
+                    mma_bf16(o[2 * jj + 1], pa, b2, b3);
                 }
             }
             __syncwarp();
@@ -768,7 +798,46 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float lseB = lB > 0.f ? (mB + __log2f(lB)) * ln2 : -INFINITY;
         const size_t rowA = (size_t)(it.t0 + tokA) * H + hA;
         const size_t rowB = (size_t)(it.t0 + tokB) * H + hB;
-        if (it.nact == 1) {
+        if constexpr (kFp8) {
+            // n-tiles 4vb + 2sec (even d) and 4vb + 2sec + 1 (odd d): a row's four values of a 16-d half are
+            // d .. d + 3 with d = d0 + 32vb + 16sec + 4t, in the order (even0, odd0, even1, odd1)
+            const size_t blk = (size_t)it.index * p.dec_rows;
+            const size_t pA = blk + (size_t)tokA * H + hA, pB = blk + (size_t)tokB * H + hB;
+#pragma unroll
+            for (int vb = 0; vb < kVB; ++vb) {
+#pragma unroll
+                for (int sec = 0; sec < (kDSec ? 2 : 1); ++sec) {
+                    const int je = 4 * vb + 2 * sec, jo = je + 1;
+                    const int d = d0 + 32 * vb + 16 * sec + 4 * (lane & 3);
+                    if (it.nact == 1) {
+                        if (vA) {
+                            *reinterpret_cast<uint32_t *>(p.out + rowA * kHeadDim + d) = pack_bf16x2(o[je][0] * invA, o[jo][0] * invA);
+                            *reinterpret_cast<uint32_t *>(p.out + rowA * kHeadDim + d + 2) = pack_bf16x2(o[je][1] * invA, o[jo][1] * invA);
+                        }
+                        if (vB) {
+                            *reinterpret_cast<uint32_t *>(p.out + rowB * kHeadDim + d) = pack_bf16x2(o[je][2] * invB, o[jo][2] * invB);
+                            *reinterpret_cast<uint32_t *>(p.out + rowB * kHeadDim + d + 2) = pack_bf16x2(o[je][3] * invB, o[jo][3] * invB);
+                        }
+                    } else {
+                        if (vA)
+                            *reinterpret_cast<float4 *>(p.part_dec_o + pA * kHeadDim + d) =
+                                make_float4(o[je][0] * invA, o[jo][0] * invA, o[je][1] * invA, o[jo][1] * invA);
+                        if (vB)
+                            *reinterpret_cast<float4 *>(p.part_dec_o + pB * kHeadDim + d) =
+                                make_float4(o[je][2] * invB, o[jo][2] * invB, o[je][3] * invB, o[jo][3] * invB);
+                    }
+                }
+            }
+            if (dsl == 0 && (lane & 3) == 0) {
+                if (it.nact == 1) {
+                    if (p.lse && vA) p.lse[rowA] = lseA;
+                    if (p.lse && vB) p.lse[rowB] = lseB;
+                } else {
+                    if (vA) p.part_dec_lse[pA] = lseA;
+                    if (vB) p.part_dec_lse[pB] = lseB;
+                }
+            }
+        } else if (it.nact == 1) {
 #pragma unroll
             for (int j = 0; j < kNT; ++j) {
                 const int d = d0 + j * 8 + cq;
