@@ -333,15 +333,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const float *rel1 = p.rel ? p.rel + ((size_t)(it.t0 + tok1) * H + h1) * p.E : nullptr;
             const int lkey = (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix row of this lane (K)
 
-            for (int gi = it.gb; gi < it.ge; ++gi, ++n) {
-                const int stage = n % nstages;
-                if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
-                const uint8_t *st = ring + (size_t)stage * stage_bytes;
-                const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
-                const uint32_t vbase = kbase + kv_bytes;
-
-                // S^T = K Q^T (16 keys x 8 rows); even and odd k-steps in two accumulators (shorter chains)
-                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+            // S^T of one page (16 keys x 8 rows); even and odd k-steps in two accumulators (shorter chains)
+            auto qk_page = [&](uint32_t kbase, float (&sc)[4]) {
+                float sd[4] = {0.f, 0.f, 0.f, 0.f};
+                sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
                 if constexpr (kFp8) {
 #pragma unroll
                     for (int kp = 0; kp < 4; ++kp) {  // k-steps 2kp, 2kp + 1: E4M3 chunks 2kp + (lane >> 4)
@@ -367,12 +362,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-                // sc[e]: row (e & 1 ? r1 : r0), key gq + 8 * (e >> 1)
+            };
+            // scale into the log2 domain, bias, masks: x[e] is row (e & 1 ? r1 : r0) at key gq + 8 (e >> 1)
+            auto score_page = [&](int gi, const uint8_t *st, const float (&sc)[4], float (&x)[4]) {
                 const int kbase_key = gi * kKeyGroup;
                 const bool band = group_in_band(qa0, qa1, gi, p.E);
                 const bool need_mask = (kbase_key < nlo) || (kbase_key + kKeyGroup - 1 > nhi);
                 const float *bsm = reinterpret_cast<const float *>(st + 2 * kv_bytes);
-                float x[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const bool second = e & 1;
@@ -398,8 +394,70 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                     x[e] = v;
                 }
-                // row maxima over the page: this thread's two keys, then the 8 lanes with the same t
-                float t0 = fmaxf(x[0], x[2]), t1 = fmaxf(x[1], x[3]);
+            };
+            // O^T += V^T P^T of one page over this warp's d-slice; keys >= tail are beyond the cache length
+            auto pv_page = [&](uint32_t vbase, uint32_t pb0, uint32_t pb1, int tail) {
+                if constexpr (kFp8) {
+                    // E4M3 V^T operands straight from the landed rows: matrices (keys 0-7 | 8-15) x (d D | D + 16)
+                    const int vkey = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+                    for (int vb = 0; vb < kVB; ++vb) {
+                        const int chunk = (d0 + 32 * vb + ((lane >> 3) & 1) * kDSec) >> 4;
+                        uint32_t r[4];
+                        ldsm_x4_t(vbase + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), r[0], r[1], r[2], r[3]);
+                        if (tail < kKeyGroup) {
+                            mask_key_pair(r[0], 2 * t, tail);
+                            mask_key_pair(r[1], 2 * t, tail);
+                            mask_key_pair(r[2], 2 * t + 8, tail);
+                            mask_key_pair(r[3], 2 * t + 8, tail);
+                        }
+                        const uint32_t ae[4] = {e4m3_even_f16x2(r[0]), e4m3_even_f16x2(r[1]), e4m3_even_f16x2(r[2]),
+                                                e4m3_even_f16x2(r[3])};
+                        const uint32_t ao[4] = {e4m3_odd_f16x2(r[0]), e4m3_odd_f16x2(r[1]), e4m3_odd_f16x2(r[2]),
+                                                e4m3_odd_f16x2(r[3])};
+                        mma_f16(o[2 * vb], ae, pb0, pb1);
+                        mma_f16(o[2 * vb + 1], ao, pb0, pb1);
+                    }
+                } else {  // one m-tile of 16 d at a time
+                    const int vkey = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+                    for (int mt = 0; mt < kMT; ++mt) {
+                        const int d = d0 + 16 * mt;
+                        const int chunk = ((d & 63) >> 3) + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldsm_x4_t(vbase + (d >> 6) * 2048 + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), a[0], a[1],
+                                  a[2], a[3]);
+                        if (tail < kKeyGroup) {
+                            mask_key_pair(a[0], 2 * t, tail);
+                            mask_key_pair(a[1], 2 * t, tail);
+                            mask_key_pair(a[2], 2 * t + 8, tail);
+                            mask_key_pair(a[3], 2 * t + 8, tail);
+                        }
+                        mma_bf16(o[mt], a, pb0, pb1);
+                    }
+                }
+            };
+
+            // two pages per step when the ring is deep enough to hold two and still prefetch (at least 4
+            // stages): two independent QK chains, and one max exchange and rescale decision per 32 keys
+            const bool pair_pages = nstages >= 4;
+            for (int gi = it.gb; gi < it.ge;) {
+                const bool two = pair_pages && gi + 1 < it.ge;
+                const int sa = n % nstages, sb = (n + 1) % nstages;
+                if (!mbar_wait_warp(&sh.full[sa], (n / nstages) & 1, abort, p)) break;
+                if (two && !mbar_wait_warp(&sh.full[sb], ((n + 1) / nstages) & 1, abort, p)) break;
+                const uint8_t *stA = ring + (size_t)sa * stage_bytes, *stB = ring + (size_t)sb * stage_bytes;
+                const uint32_t kA = smem_u32(stA) + g * (kFp8 ? 2048 : 4096);
+                const uint32_t kB = smem_u32(stB) + g * (kFp8 ? 2048 : 4096);
+                float scA[4], scB[4], xA[4], xB[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                qk_page(kA, scA);
+                if (two) qk_page(kB, scB);
+                score_page(gi, stA, scA, xA);
+                if (two) score_page(gi + 1, stB, scB, xB);
+
+                // row maxima over the step: this thread's keys, then the 8 lanes with the same t
+                float t0 = fmaxf(fmaxf(xA[0], xA[2]), fmaxf(xB[0], xB[2]));
+                float t1 = fmaxf(fmaxf(xA[1], xA[3]), fmaxf(xB[1], xB[3]));
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
@@ -421,59 +479,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
                 const float sub0 = (m0 == -INFINITY) ? 0.f : m0;
                 const float sub1 = (m1 == -INFINITY) ? 0.f : m1;
-                const float p0 = fast_exp2(x[0] - sub0), p1 = fast_exp2(x[1] - sub1);
-                const float p2 = fast_exp2(x[2] - sub0), p3 = fast_exp2(x[3] - sub1);
-                l0 += p0 + p2;
-                l1 += p1 + p3;
-                // P^T fragments (B operand of PV): the two 8-key blocks of P, transposed in registers
-                const uint32_t pb0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
-                const uint32_t pb1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
-
-                // O^T += V^T P^T over this warp's d-slice
-                if constexpr (kFp8) {
-                    // E4M3 V^T operands straight from the landed rows: matrices (keys 0-7 | 8-15) x (d D | D + 16)
-                    const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
-                    const int vkey = (lane & 7) + 8 * (lane >> 4);
+                float pA[4], pB[4];
 #pragma unroll
-                    for (int vb = 0; vb < kVB; ++vb) {
-                        const int chunk = (d0 + 32 * vb + ((lane >> 3) & 1) * kDSec) >> 4;
-                        uint32_t r[4];
-                        ldsm_x4_t(vbase + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), r[0], r[1], r[2], r[3]);
-                        if (tail < kKeyGroup) {
-                            mask_key_pair(r[0], 2 * t, tail);
-                            mask_key_pair(r[1], 2 * t, tail);
-                            mask_key_pair(r[2], 2 * t + 8, tail);
-                            mask_key_pair(r[3], 2 * t + 8, tail);
-                        }
-                        const uint32_t ae[4] = {e4m3_even_f16x2(r[0]), e4m3_even_f16x2(r[1]), e4m3_even_f16x2(r[2]),
-                                                e4m3_even_f16x2(r[3])};
-                        const uint32_t ao[4] = {e4m3_odd_f16x2(r[0]), e4m3_odd_f16x2(r[1]), e4m3_odd_f16x2(r[2]),
-                                                e4m3_odd_f16x2(r[3])};
-                        mma_f16(o[2 * vb], ae, pb0, pb1);
-                        mma_f16(o[2 * vb + 1], ao, pb0, pb1);
-                    }
-                } else {  // one m-tile of 16 d at a time
-                    const int tail = it.Lk - kbase_key;  // keys >= tail are beyond the cache length
-                    const int vkey = (lane & 7) + 8 * (lane >> 4);
-#pragma unroll
-                    for (int mt = 0; mt < kMT; ++mt) {
-                        const int d = d0 + 16 * mt;
-                        const int chunk = ((d & 63) >> 3) + ((lane >> 3) & 1);
-                        uint32_t a[4];
-                        ldsm_x4_t(vbase + (d >> 6) * 2048 + vkey * 128 + ((chunk ^ (vkey & 7)) << 4), a[0], a[1],
-                                  a[2], a[3]);
-                        if (tail < kKeyGroup) {  // zero V entries of keys past the cache length
-                            const int k0 = 2 * t, k1 = 2 * t + 8;
-                            if (k0 >= tail) { a[0] &= 0xffff0000u; a[1] &= 0xffff0000u; }
-                            if (k0 + 1 >= tail) { a[0] &= 0x0000ffffu; a[1] &= 0x0000ffffu; }
-                            if (k1 >= tail) { a[2] &= 0xffff0000u; a[3] &= 0xffff0000u; }
-                            if (k1 + 1 >= tail) { a[2] &= 0x0000ffffu; a[3] &= 0x0000ffffu; }
-                        }
-                        mma_bf16(o[mt], a, pb0, pb1);
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    pA[e] = fast_exp2(xA[e] - ((e & 1) ? sub1 : sub0));
+                    pB[e] = fast_exp2(xB[e] - ((e & 1) ? sub1 : sub0));
+                }
+                l0 += (pA[0] + pA[2]) + (pB[0] + pB[2]);
+                l1 += (pA[1] + pA[3]) + (pB[1] + pB[3]);
+                // P^T fragments (B operand of PV): each page's two 8-key blocks of P, transposed in registers
+                const uint32_t pa0 = movmatrix_trans(kFp8 ? pack_f16x2(pA[0], pA[1]) : pack_bf16x2(pA[0], pA[1]));
+                const uint32_t pa1 = movmatrix_trans(kFp8 ? pack_f16x2(pA[2], pA[3]) : pack_bf16x2(pA[2], pA[3]));
+                pv_page(kA + kv_bytes, pa0, pa1, it.Lk - gi * kKeyGroup);
+                if (two) {
+                    const uint32_t pc0 = movmatrix_trans(kFp8 ? pack_f16x2(pB[0], pB[1]) : pack_bf16x2(pB[0], pB[1]));
+                    const uint32_t pc1 = movmatrix_trans(kFp8 ? pack_f16x2(pB[2], pB[3]) : pack_bf16x2(pB[2], pB[3]));
+                    pv_page(kB + kv_bytes, pc0, pc1, it.Lk - (gi + 1) * kKeyGroup);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.empty[stage]);
+                if (lane == 0) {
+                    mbar_arrive(&sh.empty[sa]);
+                    if (two) mbar_arrive(&sh.empty[sb]);
+                }
+                n += two ? 2 : 1;
+                gi += two ? 2 : 1;
             }
             if (*abort) break;
 
