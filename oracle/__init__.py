@@ -218,6 +218,54 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping):
     return kc, vc
 
 
+def e4m3_encode(y) -> np.ndarray:
+    """fp32 values -> OCP FP8 E4M3 bytes: the nearest finite E4M3 value, ties to the even code (the code whose
+    last mantissa bit is 0), magnitudes above the largest finite value 448 saturated to it, NaN -> 0x7F.
+    The sign is kept, zero included (-0.0 -> 0x80).
+
+    Written as a plain search over the 127 non-negative finite codes and their values (decoded by the
+    oracle's own E4M3 decoder), not as bit arithmetic.  Pinned in ``tests/test_oracle_pins.py`` (an
+    independent E4M3 cast on a dense sweep, round trips, ties, saturation)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    codes = np.arange(0x7F, dtype=np.uint8)                  # 0x00 .. 0x7E: every finite magnitude
+    vals = e4m3_to_float64(codes)                              # ascending
+    mag = np.minimum(np.abs(y), vals[-1])                      # saturate
+    hi = np.clip(np.searchsorted(vals, mag, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = mag - vals[lo], vals[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0))
+    out = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    out = out | np.where(np.signbit(y), np.uint8(0x80), np.uint8(0))
+    out[np.isnan(y)] = 0x7F
+    return out
+
+
+def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale: float, v_scale: float):
+    """KV append into an FP8 (E4M3) cache: like ``reshape_and_cache``, with each stored element quantized as
+    E4M3(fp32(x) / fp32(scale)), k_scale for keys and v_scale for values.  The division is one IEEE fp32
+    division, then ``e4m3_encode``.  This is the quantize-on-store of the vLLM V1 attention page's
+    TurboQuant backend (section 12.1), inverse to the K = k_scale * E4M3 read of ``attention_fp8kv``.
+    Returns the new (key_cache, value_cache) as uint8 arrays; the inputs are not modified."""
+    import torch
+
+    k32 = _as_u16(key).astype(np.uint32) << 16
+    v32 = _as_u16(value).astype(np.uint32) << 16
+    kq = e4m3_encode(k32.view(np.float32) / np.float32(k_scale))
+    vq = e4m3_encode(v32.view(np.float32) / np.float32(v_scale))
+    kc = _as_u8(key_cache).copy()
+    vc = _as_u8(value_cache).copy()
+    slots = np.asarray(slot_mapping.cpu() if isinstance(slot_mapping, torch.Tensor) else slot_mapping,
+                       dtype=np.int64)
+    bs = kc.shape[1]
+    for t in range(kq.shape[0]):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        kc[s // bs, s % bs] = kq[t]
+        vc[s // bs, s % bs] = vq[t]
+    return kc, vc
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """fp64 -> nearest bf16 value (round half to even), returned as float64.
 

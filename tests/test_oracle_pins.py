@@ -487,6 +487,71 @@ def test_fp8_scales_are_a_logit_scale_and_an_output_scale(seed):
     _close(lse, ulse, 1e-12)
 
 
+def test_e4m3_encoder_matches_an_independent_cast_in_range():
+    """Every finite E4M3 value, every midpoint between neighbours (and a hair either side of it) and random
+    fp32 values in [-448, 448] against torch's float8_e4m3fn cast (round to nearest even)."""
+    vals = oracle.e4m3_to_float64(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[1:] + vals[:-1]) / 2
+    pts = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                          np.nextafter(mids.astype(np.float32), np.float32(1e9))])
+    g = np.random.default_rng(5)
+    rnd = np.concatenate([g.uniform(-448, 448, 20000), g.standard_normal(20000) * 2.0 ** g.integers(-12, 8, 20000)])
+    y = np.concatenate([pts, -pts, rnd]).astype(np.float32)
+    y = y[np.abs(y) <= 448]
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(y), ref)
+
+
+def test_e4m3_encoder_round_trip_ties_saturation():
+    codes = np.concatenate([np.arange(0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8)
+    vals = oracle.e4m3_to_float64(codes).astype(np.float32)
+    back = oracle.e4m3_encode(vals)
+    assert np.array_equal(back[vals != 0], codes[vals != 0])     # every finite value encodes to its own code
+    tie = lambda a, b: np.float32((oracle.e4m3_to_float64(np.array([a], np.uint8))[0] +
+                                   oracle.e4m3_to_float64(np.array([b], np.uint8))[0]) / 2)
+    # halfway cases go to the code with an even last mantissa bit
+    for a, b in [(0x38, 0x39), (0x39, 0x3A), (0x00, 0x01), (0x07, 0x08), (0x7D, 0x7E)]:
+        want = a if a % 2 == 0 else b
+        assert oracle.e4m3_encode(np.array([tie(a, b)]))[0] == want
+        assert oracle.e4m3_encode(np.array([-tie(a, b)]))[0] == want | 0x80
+    big = np.array([448.0, 449.0, 464.0, 1e6, np.inf, -500.0, -np.inf], dtype=np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E] * 5 + [0xFE] * 2
+    assert oracle.e4m3_encode(np.array([np.nan, 0.0, -0.0], np.float32)).tolist() == [0x7F, 0x00, 0x80]
+
+
+@pytest.mark.parametrize("bs", [1, 16])
+def test_reshape_and_cache_fp8_reads_back_quantized(bs):
+    """Each stored byte, read back through the block table, is the E4M3 code of the fp32 quotient
+    x / scale (the encoder above); nothing else in the cache changes; padding stores nothing."""
+    g = torch.Generator().manual_seed(17 + bs)
+    kv_lens, q_lens = [40, 7], [5, 7]
+    pages = [(k + bs - 1) // bs for k in kv_lens]
+    perm = torch.randperm(sum(pages) + 3, generator=g).tolist()
+    table = [perm[:pages[0]], perm[pages[0]:pages[0] + pages[1]]]
+    slots = oracle.slot_mapping(table, kv_lens, q_lens, bs) + [-1]
+    T = len(slots)
+    key = (torch.randn(T, 2, 128, generator=g) * 40).to(torch.bfloat16)    # some beyond 448 * k_scale
+    value = (torch.randn(T, 2, 128, generator=g) * 0.01).to(torch.bfloat16)
+    kc = torch.randint(0, 255, (len(perm), bs, 2, 128), generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 255, (len(perm), bs, 2, 128), generator=g, dtype=torch.uint8)
+    ks, vs = 0.07, 0.0003
+    nk, nv = oracle.reshape_and_cache_fp8(key, value, kc, vc, torch.tensor(slots), ks, vs)
+    touched = np.zeros(kc.shape[:2], dtype=bool)
+    t = 0
+    for b, (lq, lk) in enumerate(zip(q_lens, kv_lens)):
+        for j in range(lk - lq, lk):
+            page, off = table[b][j // bs], j % bs
+            kf = key[t].float().numpy() / np.float32(ks)
+            vf = value[t].float().numpy() / np.float32(vs)
+            assert np.array_equal(nk[page, off], oracle.e4m3_encode(kf))
+            assert np.array_equal(nv[page, off], oracle.e4m3_encode(vf))
+            touched[page, off] = True
+            t += 1
+    assert np.array_equal(nk[~touched], kc.numpy()[~touched])
+    assert np.array_equal(nv[~touched], vc.numpy()[~touched])
+    assert (nk[touched] == 0x7E).any() or (nk[touched] == 0xFE).any()       # saturation was exercised
+
+
 def test_round_to_bf16_matches_torch():
     x = np.random.default_rng(0).normal(size=10000) * 10.0 ** np.random.default_rng(1).integers(-6, 6, 10000)
     want = torch.from_numpy(x).float().to(torch.bfloat16).double().numpy()
