@@ -116,7 +116,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {"ink_decode_kernel": "ink_decode.cu", "ink_prefill_kernel": "ink_prefill.cu",
                   "ink_combine_kernel": "ink_combine.cu", "ink_prepass_kernel": "ink_prepass.cu",
-                  "ink_append_kernel": "ink_append.cu"}
+                  "ink_append_kernel": "ink_append.cu", "ink_append_fp8_kernel": "ink_append.cu"}
 
 
 def kernel_source_hash(kernel):
@@ -447,9 +447,22 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         return res
 
-    def measure_append(steps, warmup):
-        """KV append of one serving step: 4 x 8192 new tokens, Hkv 8, into 16-key pages (K and V)."""
+    def measure_append(steps, warmup, fp8=False):
+        """KV append of one serving step: 4 x 8192 new tokens, Hkv 8, into 16-key pages (K and V); with fp8,
+        quantized into an E4M3 cache."""
         case = build_case("kv_append", [8192] * 4, [8192] * 4, H=8, Hkv=8, E=0, seed=1100, device=dev)
+        if fp8:
+            case.key_cache = torch.zeros(case.key_cache.shape, dtype=torch.uint8, device=dev)
+            case.value_cache = torch.zeros_like(case.key_cache)
+            torch.cuda.empty_cache()
+
+        def store():
+            if fp8:
+                ink.reshape_and_cache_fp8(key, value, case.key_cache, case.value_cache, slots,
+                                          k_scale=FP8_SCALES[0], v_scale=FP8_SCALES[1])
+            else:
+                ink.reshape_and_cache(key, value, case.key_cache, case.value_cache, slots)
+
         g = torch.Generator(device=dev).manual_seed(1101)
         key = torch.randn(case.T, case.Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
         value = torch.randn(case.T, case.Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
@@ -457,7 +470,7 @@ def run_ours(args, rank, world, local_rank):
         pos = torch.arange(8192, device=dev)
         slots = torch.cat([case.block_table[b, pos // case.BS].long() * case.BS + pos % case.BS for b in range(4)])
         for _ in range(warmup):
-            ink.reshape_and_cache(key, value, case.key_cache, case.value_cache, slots)
+            store()
         torch.cuda.synchronize(dev)
         kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         stream = torch.cuda.current_stream(dev)
@@ -472,14 +485,15 @@ def run_ours(args, rank, world, local_rank):
             start.record(stream)
             for k in range(steps):
                 ink.set_timing_events("append", kev[k][0], kev[k][1])
-                ink.reshape_and_cache(key, value, case.key_cache, case.value_cache, slots)
+                store()
             end.record(stream)
             torch.cuda.synchronize(dev)
         ink.set_timing_events("append", None, None)
         barrier()
         ms = max_over_ranks(start.elapsed_time(end) / steps, dev)
         kms = sum(a.elapsed_time(b) for a, b in kev) / steps
-        nbytes = 2 * 2 * case.T * case.Hkv * 128 * 2  # K and V, read once and written once
+        # K and V, read once (bf16) and written once (bf16, or one E4M3 byte per element)
+        nbytes = 2 * case.T * case.Hkv * 128 * (2 + (1 if fp8 else 2))
         del case, key, value, slots
         torch.cuda.empty_cache()
         return {"ms_per_step": ms, "kernel_ms": kms, "bytes": nbytes, "launches": ink.launch_count() - n0,
@@ -570,6 +584,11 @@ def run_ours(args, rank, world, local_rank):
                                                   fp8=True)
             except Exception as exc:
                 sec["decode_batch_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
+        if "kv_append_fp8" not in skip:
+            try:
+                sec["kv_append_fp8"] = measure_append(max(3, steps // 2), max(3, warmup), fp8=True)
+            except Exception as exc:
+                sec["kv_append_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
         if "graph_decode" not in skip:
             try:
                 sec["graph_decode"] = measure_graph(max(50, steps * 10), max(5, warmup))
@@ -608,17 +627,18 @@ def run_ours(args, rank, world, local_rank):
         if "error" in r:
             workloads_out[name] = r
             continue
-        if name == "kv_append":
+        if name in ("kv_append", "kv_append_fp8"):
+            fp8 = name == "kv_append_fp8"
             ach = r["bytes"] / (r["kernel_ms"] * 1e-3) / 1e9
+            kern = "ink_append_fp8_kernel" if fp8 else "ink_append_kernel"
             workloads_out[name] = {
                 "metric": "KV append GB/s (K and V read and written)", "ms_per_step": round(r["ms_per_step"], 4),
                 "value": round(r["bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages", "gpu_launches": r["launches"],
-                "clocks": r["clocks"],
+                "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages" + (", quantized into an E4M3 cache" if fp8 else ""),
+                "gpu_launches": r["launches"], "clocks": r["clocks"],
                 "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": round(ach / peaks["hbm_gbs"], 4),
-                             "traffic": traffic_of("ink_append_kernel", "kv_append"),
-                             "peak_source": peaks["source"], "kernel": "ink_append_kernel"}}
+                             "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic_of(kern, name),
+                             "peak_source": peaks["source"], "kernel": kern}}
             continue
         if name == "decode_batch_fp8":
             rf = roof_decode(r, name)  # traffic from the E4M3 capture, kept under this name

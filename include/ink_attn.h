@@ -241,6 +241,24 @@ INK_API ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *
                                          void *key_cache, void *value_cache, const int64_t *slot_mapping,
                                          uint32_t *flags, ink_stream_t stream);
 
+/*
+ * KV append into an FP8 cache: the quantize-on-store of the TurboQuant
+ * backend (vLLM V1 attention page, section 12.1), inverse to the
+ * k_scale / v_scale read of ink_rel_attn_varlen_fp8kv.  Slots, padding and
+ * flags as ink_reshape_and_cache; each stored element is the OCP FP8 E4M3
+ * byte of fp32(x) / k_scale (keys) or fp32(x) / v_scale (values): one IEEE
+ * fp32 division, then round to nearest with ties to the even code, magnitudes
+ * above 448 saturated to 448, NaN stays NaN.
+ *   key, value  device, bf16 (num_tokens, num_kv_heads, 128), 16-byte aligned.
+ *   key_cache, value_cache  device, E4M3 bytes (num_blocks, block_size,
+ *               num_kv_heads, 128), 16-byte aligned.
+ *   k_scale, v_scale  finite and > 0, else INK_ERR_INVALID_ARG.
+ * Other errors as ink_reshape_and_cache.
+ */
+INK_API ink_status ink_reshape_and_cache_fp8(const ink_attn_dims *dims, const void *key, const void *value,
+                                             void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                                             float k_scale, float v_scale, uint32_t *flags, ink_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 INK_API const char *ink_status_string(ink_status status);
 

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "LibraryNotBuilt", "InkError", "Dims", "build", "load", "ink_rel_attn_varlen", "workspace_size",
     "num_splits", "read_device_errors", "version", "DEVERR", "set_timing_events", "launch_count",
-    "reshape_and_cache", "ink_rel_attn_varlen_fp8kv",
+    "reshape_and_cache", "ink_rel_attn_varlen_fp8kv", "reshape_and_cache_fp8",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -97,6 +97,8 @@ def load(path: Optional[str] = None):
         lib.ink_launch_count.restype = ctypes.c_uint64
         lib.ink_reshape_and_cache.restype = ctypes.c_int
         lib.ink_reshape_and_cache.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
+        lib.ink_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.ink_reshape_and_cache_fp8.argtypes = [dp, vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -297,6 +299,43 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *, flags
                                    None if flags is None else flags.data_ptr(), int(stream.cuda_stream))
     if rc != 0:
         raise InkError(rc, "ink_reshape_and_cache")
+
+
+def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, *, k_scale: float, v_scale: float,
+                          flags=None, stream=None) -> None:
+    """``reshape_and_cache`` into an FP8 (E4M3) cache: each element stored as E4M3(x / scale) (see
+    include/ink_attn.h).  key/value: bf16 (T, Hkv, 128); caches: uint8 or float8_e4m3fn
+    (num_blocks, block_size, Hkv, 128), written in place; slot_mapping: int64 (T,)."""
+    lib = load()
+    dev = key.device
+    if dev.type != "cuda":
+        raise ValueError("key must be a CUDA tensor")
+    if key_cache.dtype == torch.float8_e4m3fn:
+        key_cache = key_cache.view(torch.uint8)
+    if value_cache.dtype == torch.float8_e4m3fn:
+        value_cache = value_cache.view(torch.uint8)
+    _check(key, "key", torch.bfloat16, 3, dev)
+    _check(value, "value", torch.bfloat16, 3, dev)
+    _check(key_cache, "key_cache", torch.uint8, 4, dev)
+    _check(value_cache, "value_cache", torch.uint8, 4, dev)
+    _check(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    if value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("key/value or key_cache/value_cache shapes differ")
+    T, Hkv, D = key.shape
+    NB, BS, Hkv2, D2 = key_cache.shape
+    if (Hkv, D) != (Hkv2, D2) or slot_mapping.shape[0] != T:
+        raise ValueError("key, key_cache and slot_mapping shapes do not match")
+    if flags is not None:
+        _check(flags, "flags", torch.int32, 1, dev)
+    dims = Dims(T, 1, Hkv, Hkv, D, NB, BS, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ink_reshape_and_cache_fp8(ctypes.byref(dims), key.data_ptr(), value.data_ptr(), key_cache.data_ptr(),
+                                       value_cache.data_ptr(), slot_mapping.data_ptr(), float(k_scale),
+                                       float(v_scale), None if flags is None else flags.data_ptr(),
+                                       int(stream.cuda_stream))
+    if rc != 0:
+        raise InkError(rc, "ink_reshape_and_cache_fp8")
 
 
 def read_device_errors(workspace: Optional[torch.Tensor] = None, stream=None, device=None) -> int:

@@ -522,6 +522,32 @@ ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, con
     return INK_OK;
 }
 
+ink_status ink_reshape_and_cache_fp8(const ink_attn_dims *dims, const void *key, const void *value, void *key_cache,
+                                     void *value_cache, const int64_t *slot_mapping, float k_scale, float v_scale,
+                                     uint32_t *flags, ink_stream_t stream_handle)
+{
+    if (!dims || dims->num_tokens < 0 || dims->num_kv_heads < 1 || dims->head_dim < 1 || dims->num_blocks < 1 ||
+        dims->block_size < 1)
+        return INK_ERR_INVALID_ARG;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return INK_ERR_INVALID_ARG;
+    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+        return INK_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(slot_mapping, 8) || (flags && !aligned(flags, 4)))
+        return INK_ERR_INVALID_ARG;
+    if (dims->head_dim != kHeadDim) return INK_ERR_UNSUPPORTED;
+    if (dims->num_tokens == 0) return INK_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return INK_ERR_CUDA;
+    if (timed_launch(INK_KERNEL_APPEND, stream, [&] {
+            return launch_append_fp8(dims, key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale, flags,
+                                     sms, stream);
+        }) != cudaSuccess)
+        return INK_ERR_CUDA;
+    return INK_OK;
+}
+
 ink_status ink_rel_attn_read_device_errors(const void *workspace, ink_stream_t stream_handle, uint32_t *flags)
 {
     if (!workspace || !flags) return INK_ERR_INVALID_ARG;

@@ -361,5 +361,8 @@ cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
                           void *value_cache, const int64_t *slot_mapping, uint32_t *flags, int sms,
                           cudaStream_t stream);
+cudaError_t launch_append_fp8(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
+                              void *value_cache, const int64_t *slot_mapping, float k_scale, float v_scale,
+                              uint32_t *flags, int sms, cudaStream_t stream);
 
 }  // namespace ink

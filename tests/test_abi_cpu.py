@@ -138,3 +138,23 @@ def test_fp8_entry_host_validation(lib):
     assert call(scale=0.0) == 1                                # softmax_scale must be > 0
     assert call(d=ink.Dims(4, 2, 8, 2, 64, 16, 16, 4)) == 2    # head_dim 64
     assert call(d=ink.Dims(0, 2, 8, 2, 128, 16, 16, 4)) == 0   # nothing to do
+
+
+def test_fp8_append_host_validation(lib):
+    """ink_reshape_and_cache_fp8 rejects bad scales, pointers and shapes before touching the GPU."""
+    import ctypes
+
+    f = lib.ink_reshape_and_cache_fp8
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [ctypes.POINTER(ink.Dims), vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]
+    good = 0x10000
+    dims = ink.Dims(8, 1, 4, 4, 128, 16, 16, 1)
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+        assert f(ctypes.byref(dims), good, good, good, good, good, ks, vs, None, None) == 1
+    assert f(ctypes.byref(dims), None, good, good, good, good, 1.0, 1.0, None, None) == 1       # null key
+    assert f(ctypes.byref(dims), good, good, good + 8, good, good, 1.0, 1.0, None, None) == 1   # misaligned cache
+    bad = ink.Dims(8, 1, 4, 4, 256, 16, 16, 1)
+    assert f(ctypes.byref(bad), good, good, good, good, good, 1.0, 1.0, None, None) == 2        # head_dim 256
+    empty = ink.Dims(0, 1, 4, 4, 128, 16, 16, 1)
+    assert f(ctypes.byref(empty), good, good, good, good, good, 1.0, 1.0, None, None) == 0     # nothing to do

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import paged_varlen_attention_causal_gb300 as ink
-from workloads import build_case, workload
+from workloads import build_case, fp8_kv, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +118,79 @@ def test_append_then_attend():
     l = lse.cpu().double().numpy().reshape(ref_lse.shape)
     rel = np.abs(l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))
     assert rel.max() <= LSE_RTOL
+
+
+# --- FP8 (E4M3) cache: quantize on store --------------------------------------
+
+def _fp8_step(q_lens, kv_lens, bs, Hkv, seed, pad_at=()):
+    """A step of new bf16 tokens over random E4M3 caches; keys span the whole E4M3 range at k_scale 0.05
+    (some saturate), values are small (some E4M3 subnormals), and a few are exact zeros of either sign."""
+    key, value, _, _, slots = _step(q_lens, kv_lens, bs, Hkv, seed, pad_at)
+    g = torch.Generator().manual_seed(seed + 1000)
+    key = (key.float() * 12).to(torch.bfloat16)
+    value = (value.float() * 0.002).to(torch.bfloat16)
+    key.view(-1)[::97] = 0.0
+    value.view(-1)[::89] = -0.0
+    pool = int(slots.max().item()) // bs + 8
+    kc = torch.randint(0, 255, (pool, bs, Hkv, 128), generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 255, (pool, bs, Hkv, 128), generator=g, dtype=torch.uint8)
+    return key, value, kc, vc, slots
+
+
+@pytest.mark.parametrize("bs,Hkv,ks,vs", [(16, 8, 0.05, 1e-4), (1, 4, 1.0, 1.0), (32, 1, 0.3, 7e-5),
+                                          (16, 2, 0.05, 0.0017)])
+def test_append_fp8_matches_oracle_bit_for_bit(bs, Hkv, ks, vs):
+    key, value, kc, vc, slots = _fp8_step([1, 200, 3, 77], [900, 200, 40, 300], bs, Hkv, seed=bs * 7 + Hkv,
+                                          pad_at=(0, 50, 151))
+    want_k, want_v = oracle.reshape_and_cache_fp8(key, value, kc, vc, slots, ks, vs)
+    dk, dv = kc.cuda(), vc.cuda()
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ink.reshape_and_cache_fp8(key.cuda(), value.cuda(), dk, dv, slots.cuda(), k_scale=ks, v_scale=vs, flags=flags)
+    torch.cuda.synchronize()
+    assert flags.item() == 0
+    assert np.array_equal(dk.cpu().numpy(), want_k) and np.array_equal(dv.cpu().numpy(), want_v)
+    if ks == 0.05:
+        assert (want_k == 0x7E).any() and (want_k == 0xFE).any()   # saturated on both sides
+
+
+def test_append_fp8_flags_a_slot_past_the_cache():
+    key, value, kc, vc, slots = _fp8_step([40], [40], 16, 4, seed=6)
+    slots[3] = kc.shape[0] * kc.shape[1]
+    ok = slots.clone()
+    ok[3] = -1
+    want_k, want_v = oracle.reshape_and_cache_fp8(key, value, kc, vc, ok, 0.5, 0.25)
+    dk, dv = kc.cuda(), vc.cuda()
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ink.reshape_and_cache_fp8(key.cuda(), value.cuda(), dk, dv, slots.cuda(), k_scale=0.5, v_scale=0.25,
+                              flags=flags)
+    torch.cuda.synchronize()
+    assert flags.item() & ink.DEVERR["PAGE_ID"]
+    assert np.array_equal(dk.cpu().numpy(), want_k) and np.array_equal(dv.cpu().numpy(), want_v)
+
+
+def test_append_fp8_then_attend():
+    """A serving step over an E4M3 cache: quantize the new tokens into it, then decode over it."""
+    case = build_case("append-fp8", [1, 1, 2], [500, 64, 130], H=32, Hkv=8, E=96, seed=19)
+    ks, vs = 0.06, 0.05
+    k8, v8 = fp8_kv(case, ks, vs)
+    slots = torch.tensor(oracle.slot_mapping(case.block_table.tolist(), case.kv_lens, case.q_lens, case.BS),
+                         dtype=torch.int64)
+    g = torch.Generator().manual_seed(20)
+    key = torch.randn(case.T, case.Hkv, 128, generator=g).to(torch.bfloat16)
+    value = torch.randn(case.T, case.Hkv, 128, generator=g).to(torch.bfloat16)
+    want_k, want_v = oracle.reshape_and_cache_fp8(key, value, k8, v8, slots, ks, vs)
+    ref_out, ref_lse = oracle.attention_fp8kv(case.q, want_k, want_v, case.block_table, case.cache_seqlens,
+                                              case.cu_seqlens_q, k_scale=ks, v_scale=vs, **case.oracle_kwargs())
+    d = case.to("cuda")
+    dk, dv = k8.cuda(), v8.cuda()
+    ink.reshape_and_cache_fp8(key.cuda(), value.cuda(), dk, dv, slots.cuda(), k_scale=ks, v_scale=vs)
+    out, lse = ink.ink_rel_attn_varlen_fp8kv(d.q, dk, dv, k_scale=ks, v_scale=vs, block_table=d.block_table,
+                                             cache_seqlens=d.cache_seqlens, cu_seqlens_q=d.cu_seqlens_q,
+                                             max_seqlen_q=d.max_seqlen_q, softmax_scale=d.softmax_scale,
+                                             rel_extent=d.E, rel_logits=d.rel_logits, return_lse=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(dk.cpu().numpy(), want_k)
+    o = out.float().cpu().double().numpy().reshape(ref_out.shape)
+    assert np.max(np.abs(o - ref_out)) <= OUT_TOL
+    l = lse.cpu().double().numpy().reshape(ref_lse.shape)
+    assert (np.abs(l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max() <= LSE_RTOL
