@@ -195,3 +195,66 @@ def test_graph_of_a_whole_serving_step():
         after.key_cache = torch.from_numpy(want_k.view(np.int16)).view(torch.bfloat16)
         after.value_cache = torch.from_numpy(want_v.view(np.int16)).view(torch.bfloat16)
         _compare(st.out, st.lse, after, f"step {i}")
+
+
+def test_graph_of_an_fp8_serving_step():
+    """E4M3 cache: quantizing KV append and decode-shaped attention captured together, replayed on batches
+    with different mixes of 1- to 4-token requests (T = 8, G = 4)."""
+    from workloads import fp8_kv
+
+    batches = [([1, 1, 2, 4], [300, 17, 900, 64]), ([2, 2, 2, 2], [40, 40, 2000, 5]),
+               ([4, 4, 0, 0], [1000, 4, 0, 0]), ([1, 3, 4, 0], [1, 700, 33, 0])]
+    ks, vs = 0.07, 0.05
+    cases = [build_case(f"fp8-graph-{i}", q, k, H=16, Hkv=4, E=40, seed=60 + i, pool_pages=POOL,
+                        max_blocks_per_seq=WIDTH, max_seqlen_q=4) for i, (q, k) in enumerate(batches)]
+    c0 = cases[0]
+    T = c0.T
+    q = c0.q.cuda().clone()
+    bt, seqk, cu = c0.block_table.cuda().clone(), c0.cache_seqlens.cuda().clone(), c0.cu_seqlens_q.cuda().clone()
+    rel = c0.rel_logits.cuda().clone()
+    k8, v8 = (x.cuda() for x in fp8_kv(c0, ks, vs))
+    key = torch.empty(T, 4, 128, dtype=torch.bfloat16, device="cuda")
+    value = torch.empty_like(key)
+    slots = torch.full((T,), -1, dtype=torch.int64, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(T, 16, dtype=torch.float32, device="cuda")
+    ws = torch.empty(ink.workspace_size(ink.Dims(T, c0.B, 16, 4, 128, POOL, 16, WIDTH), 4, 0), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        ink.reshape_and_cache_fp8(key, value, k8, v8, slots, k_scale=ks, v_scale=vs)
+        ink.ink_rel_attn_varlen_fp8kv(q, k8, v8, k_scale=ks, v_scale=vs, block_table=bt, cache_seqlens=seqk,
+                                      cu_seqlens_q=cu, max_seqlen_q=4, softmax_scale=c0.softmax_scale,
+                                      rel_extent=40, rel_logits=rel, out=out, lse=lse, workspace=ws)
+
+    g = _capture(step)
+    for i, case in enumerate(cases):
+        gen = torch.Generator().manual_seed(900 + i)
+        new_k = torch.randn(T, 4, 128, generator=gen).to(torch.bfloat16)
+        new_v = torch.randn(T, 4, 128, generator=gen).to(torch.bfloat16)
+        sm = torch.tensor(oracle.slot_mapping(case.block_table.tolist(), case.kv_lens, case.q_lens, case.BS),
+                          dtype=torch.int64)
+        c8k, c8v = fp8_kv(case, ks, vs)
+        want_k, want_v = oracle.reshape_and_cache_fp8(new_k, new_v, c8k, c8v, sm, ks, vs)
+        ref_out, ref_lse = oracle.attention_fp8kv(case.q, want_k, want_v, case.block_table, case.cache_seqlens,
+                                                  case.cu_seqlens_q, k_scale=ks, v_scale=vs,
+                                                  **case.oracle_kwargs())
+        q.copy_(case.q)
+        bt.copy_(case.block_table)
+        seqk.copy_(case.cache_seqlens)
+        cu.copy_(case.cu_seqlens_q)
+        rel.copy_(case.rel_logits)
+        k8.copy_(c8k)
+        v8.copy_(c8v)
+        key.copy_(new_k)
+        value.copy_(new_v)
+        slots.copy_(sm)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(k8.cpu().numpy(), want_k) and np.array_equal(v8.cpu().numpy(), want_v)
+        o = out.float().cpu().double().numpy().reshape(ref_out.shape)
+        assert np.max(np.abs(o - ref_out)) <= OUT_TOL, f"step {i}"
+        fin = np.isfinite(ref_lse)
+        l = lse.cpu().double().numpy().reshape(ref_lse.shape)
+        assert np.array_equal(fin, np.isfinite(l))
+        assert (np.abs(l[fin] - ref_lse[fin]) / np.maximum(1.0, np.abs(ref_lse[fin]))).max() <= LSE_RTOL
