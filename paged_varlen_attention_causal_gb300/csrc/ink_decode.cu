@@ -6,17 +6,22 @@
 //  * persistent CTAs, one per SM, take (request, split) items from a
 //    device-built list through an atomic counter;
 //  * warp 8 is the page-gather producer: for every 16-key group of the item it
-//    reads the block_table entry and issues TMA boxes (per KV head and d-half,
-//    128-byte swizzle) for K and V, plus one fp32 box of rel_logits per query
-//    token when the group lies in the bias band, into a multi-stage ring
-//    guarded by mbarriers (paged direct addressing: no gather copy);
+//    reads the block_table entry and issues one 4-D TMA box per tensor (every
+//    KV head and d half of the page, 128-byte swizzle) for K and V, plus one
+//    fp32 box of rel_logits per query token when the group lies in the bias
+//    band, into a multi-stage ring guarded by mbarriers (paged direct
+//    addressing: no gather copy);
 //  * warps 0-7 compute.  Warp w serves KV head w % Hkv (GQA packing: the G
 //    query heads of every token of the request share one row block, so each
 //    K/V byte is read from HBM once) and, when Hkv < 8, one d-slice of the
 //    PV product, so no cross-warp merge is needed;
-//  * QK^T and PV are bf16 mma.sync m16n8k16 with fp32 accumulation: decode
-//    moves ~G flop per byte, far below any tensor-core ridge, so the kernel is
-//    bound by HBM and the legacy tensor path is ample;
+//  * QK^T and PV are mma.sync m16n8k16 with fp32 accumulation: decode moves
+//    ~G flop per byte, far below any tensor-core ridge, so the kernel is bound
+//    by HBM and the legacy tensor path is ample.  Items with at most 8 packed
+//    rows compute the transposes (S^T = K Q^T, O^T += V^T P^T) so that the 16
+//    keys of a page fill the mma's M and the rows its N = 8, half the work of
+//    the 16-row block; with a ring of at least 4 stages they take two pages
+//    per step;
 //  * online softmax in the log2 domain with the bias added after the scale
 //    (score = scale * q.k + bias); the result is written directly when the
 //    unit has one split, else as an fp32 partial plus its log-sum-exp.
@@ -27,12 +32,13 @@
 // accumulation (q converted from bf16 to fp16 once per item, p in fp16):
 //  * QK^T: ldmatrix reads the E4M3 key rows as they landed; a thread's
 //    register holds 4 consecutive bytes (d = 16 kk + 4 c .. + 3 of k-step kk),
-//    converted in registers to the two f16 pairs of its B fragment.  q's A
-//    fragment uses the same order of d within each k-step, so the dot product
-//    is unchanged.  Keys keep the bf16 path's order;
-//  * PV: each warp converts its d-slice of the V page to fp16 in a private
-//    4 KB buffer laid out like a bf16 page, and the bf16 path's transposed
-//    ldmatrix reads it;
+//    converted in registers to two f16 pairs of its K fragment.  q's fragment
+//    uses the same order of d within each k-step, so the dot product is
+//    unchanged;
+//  * PV: a transposed ldmatrix over the E4M3 V rows read as byte pairs gives a
+//    thread two keys at two adjacent d; the even bytes are the operand of the
+//    tile holding even d, the odd bytes that of the tile holding odd d, so no
+//    conversion pass through shared memory is needed;
 //  * k_scale joins the softmax scale and v_scale the final normalisation.
 #include "ink_common.cuh"
 

@@ -15,7 +15,8 @@
 //               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
 //               O += P V with P read from tensor memory (M128 N128 K16 x 8);
 //   warp 2      bias producer: per bias tile one fp32 TMA box of rel_logits per
-//               token (out-of-range distances read as 0) into a 2-slot ring;
+//               8 tokens (fewer when shared memory is short; out-of-range
+//               distances read as 0) into a 2-slot ring;
 //   warps 4-11  online softmax in two warpgroups: warps 4-7 take keys 0-63 of
 //               every S tile, warps 8-11 keys 64-127 (thread = TMEM lane = row);
 //               each adds its half of the relative bias from the staged boxes
