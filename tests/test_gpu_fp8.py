@@ -134,3 +134,12 @@ def test_fp8_decode_batch_full_size():
     check(out, lse, ref_out, ref_lse, rows=rows, what="fp8 decode_batch")
     del case, k8, v8, out, lse
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_fp8_block_sizes(bs):
+    """Pages of 32 to 128 keys: the kernel reads them as 16-key groups at the right offsets."""
+    case = build_case(f"fp8-bs{bs}", [1, 2, 1, 1], [700, 129, 33, 4000], H=32, Hkv=8, E=200, BS=bs, seed=41 + bs,
+                      device="cuda")
+    parity_fp8(case, f"fp8 block_size={bs}")
+    parity_fp8(case, f"fp8 block_size={bs} splits=5", num_splits=5)
