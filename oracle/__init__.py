@@ -250,8 +250,9 @@ def reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_sc
 
     k32 = _as_u16(key).astype(np.uint32) << 16
     v32 = _as_u16(value).astype(np.uint32) << 16
-    kq = e4m3_encode(k32.view(np.float32) / np.float32(k_scale))
-    vq = e4m3_encode(v32.view(np.float32) / np.float32(v_scale))
+    with np.errstate(over="ignore"):  # a quotient beyond fp32 is inf, which the encoder saturates
+        kq = e4m3_encode(k32.view(np.float32) / np.float32(k_scale))
+        vq = e4m3_encode(v32.view(np.float32) / np.float32(v_scale))
     kc = _as_u8(key_cache).copy()
     vc = _as_u8(value_cache).copy()
     slots = np.asarray(slot_mapping.cpu() if isinstance(slot_mapping, torch.Tensor) else slot_mapping,

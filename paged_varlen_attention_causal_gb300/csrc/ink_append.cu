@@ -9,9 +9,9 @@
 // T x Hkv x 256 bytes.
 //
 // FP8 cache (ink_append_fp8_kernel): each 16-byte chunk of 8 bf16 values is
-// stored as 8 E4M3 bytes, code = E4M3(fp32(x) / scale) with one IEEE fp32
-// division and the hardware's round-to-nearest-even, saturating conversion;
-// HBM bytes 2 x (256 read + 128 written) x T x Hkv.
+// stored as 8 E4M3 bytes, code = E4M3(fp32(x) / scale), the correctly rounded
+// fp32 quotient followed by the hardware's round-to-nearest-even, saturating
+// conversion; HBM bytes 2 x (256 read + 128 written) x T x Hkv.
 #include "ink_common.cuh"
 
 namespace ink {
@@ -50,22 +50,35 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
+// x / scale correctly rounded (fp32), with rcp = RN(1 / scale) computed once on the host: Markstein's
+// correction step (q = RN(x rcp), remainder x - q scale exact by FMA, RN(q + remainder rcp)) gives the
+// correctly rounded quotient when the quotient and its intermediates are finite normal numbers.  An exact
+// quotient (zero remainder, which keeps -0) and infinite inputs return q itself; quotients that underflow
+// quantize to an E4M3 zero of the right sign either way.
+__device__ __forceinline__ float div_by_scale(float x, float scale, float rcp)
+{
+    const float q = x * rcp;
+    const float r = fmaf(-q, scale, x);
+    return (r == 0.f || !isfinite(q)) ? q : fmaf(r, rcp, q);
+}
+
 // Eight bf16 values / scale -> eight E4M3 bytes.
-__device__ __forceinline__ uint2 quantize8(uint4 x, float scale)
+__device__ __forceinline__ uint2 quantize8(uint4 x, float scale, float rcp)
 {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t b[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        b[i] = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[i] << 16), scale),
-                               __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), scale));
+        b[i] = f32x2_to_e4m3x2(div_by_scale(__uint_as_float(w[i] << 16), scale, rcp),
+                               div_by_scale(__uint_as_float(w[i] & 0xffff0000u), scale, rcp));
     return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
 }
 
 __global__ void __launch_bounds__(kAppendThreads)
     ink_append_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint2 *key_cache,
                           uint2 *value_cache, const int64_t *__restrict__ slot_mapping, long long num_tokens,
-                          int chunks_per_token, long long num_slots, float k_scale, float v_scale, uint32_t *flags)
+                          int chunks_per_token, long long num_slots, float k_scale, float v_scale, float k_rcp,
+                          float v_rcp, uint32_t *flags)
 {
     const long long total = num_tokens * chunks_per_token;  // 16-byte bf16 chunks per tensor
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -79,8 +92,8 @@ __global__ void __launch_bounds__(kAppendThreads)
             continue;
         }
         const long long dst = s * chunks_per_token + r;  // 8-byte E4M3 chunk of the slot
-        key_cache[dst] = quantize8(__ldcs(key + c), k_scale);
-        value_cache[dst] = quantize8(__ldcs(value + c), v_scale);
+        key_cache[dst] = quantize8(__ldcs(key + c), k_scale, k_rcp);
+        value_cache[dst] = quantize8(__ldcs(value + c), v_scale, v_rcp);
     }
 }
 
@@ -95,7 +108,7 @@ cudaError_t launch_append_fp8(const ink_attn_dims *d, const void *key, const voi
     ink_append_fp8_kernel<<<grid, kAppendThreads, 0, stream>>>(
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
         static_cast<uint2 *>(value_cache), slot_mapping, d->num_tokens, chunks,
-        (long long)d->num_blocks * d->block_size, k_scale, v_scale, flags);
+        (long long)d->num_blocks * d->block_size, k_scale, v_scale, 1.0f / k_scale, 1.0f / v_scale, flags);
     return cudaGetLastError();
 }
 

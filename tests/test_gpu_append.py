@@ -194,3 +194,27 @@ def test_append_fp8_then_attend():
     assert np.max(np.abs(o - ref_out)) <= OUT_TOL
     l = lse.cpu().double().numpy().reshape(ref_lse.shape)
     assert (np.abs(l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max() <= LSE_RTOL
+
+
+@pytest.mark.parametrize("scale", [0.05, 1.0, 3.7e-3, 123.0, 2.0 ** -10, 0.3])
+def test_append_fp8_every_bf16_value(scale):
+    """Every bf16 bit pattern except the NaNs (zeros, subnormals, normals, infinities, both signs) quantized
+    with one scale: the stored codes equal the oracle's, which divides in IEEE fp32 and rounds with ties to
+    even.  Checks the kernel's quotient and conversion on the whole input range, not a sample."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    vals = bits.view(torch.bfloat16)
+    nan = torch.isnan(vals.float())
+    vals = torch.where(nan, torch.zeros_like(vals), vals)        # NaN codes are not compared
+    key = vals.reshape(512, 1, 128).contiguous()
+    value = (-vals).reshape(512, 1, 128).contiguous()
+    slots = torch.arange(512, dtype=torch.int64)
+    kc = torch.zeros(32, 16, 1, 128, dtype=torch.uint8)
+    vc = torch.zeros_like(kc)
+    want_k, want_v = oracle.reshape_and_cache_fp8(key, value, kc, vc, slots, scale, scale)
+    dk, dv = kc.cuda(), vc.cuda()
+    ink.reshape_and_cache_fp8(key.cuda(), value.cuda(), dk, dv, slots.cuda(), k_scale=scale, v_scale=scale)
+    torch.cuda.synchronize()
+    got_k, got_v = dk.cpu().numpy(), dv.cpu().numpy()
+    diff = np.flatnonzero(got_k.reshape(-1) != want_k.reshape(-1))
+    assert diff.size == 0, f"{diff.size} codes differ, first at bf16 {int(bits[diff[0]]) & 0xffff:#06x}"
+    assert np.array_equal(got_v, want_v)
