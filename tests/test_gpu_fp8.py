@@ -143,3 +143,20 @@ def test_fp8_block_sizes(bs):
                       device="cuda")
     parity_fp8(case, f"fp8 block_size={bs}")
     parity_fp8(case, f"fp8 block_size={bs} splits=5", num_splits=5)
+
+
+@pytest.mark.slow
+def test_fp8_long_decode_full_size():
+    """One decode over 1,048,576 keys (H 64, Hkv 8, E 8192) on an E4M3 cache: the transposed path with 8 rows
+    and the split-KV merge over many splits; the rows of the first and last KV heads against the oracle."""
+    case = workload("long_decode", device="cuda")
+    k8, v8 = fp8_kv(case, K_SCALE, V_SCALE)
+    case.key_cache = case.value_cache = None
+    torch.cuda.empty_cache()
+    out, lse = run_fp8(case, k8, v8)
+    assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+    rows = np.concatenate([np.arange(8), np.arange(case.H - 8, case.H)]).astype(np.int64)
+    ref_out, ref_lse = oracle_fp8(case, k8, v8, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what="fp8 long_decode")
+    del k8, v8, out, lse
+    torch.cuda.empty_cache()
