@@ -499,6 +499,45 @@ def run_ours(args, rank, world, local_rank):
         return {"ms_per_step": ms, "kernel_ms": kms, "bytes": nbytes, "launches": ink.launch_count() - n0,
                 "clocks": clk.summary()}
 
+    def measure_split_sweep(steps, warmup):
+        """The long batch-1 decode (1,048,576 keys) timed at 16 / 32 / 64 / 128 splits and at the library's own
+        choice (num_splits = 0): one step per call, CUDA events around the decode kernel and the whole step."""
+        case = workload("long_decode", device=dev)
+        out = torch.empty_like(case.q)
+        lse = torch.empty(case.T, case.H, dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        kv, _, _ = work_of(case)
+        res = {}
+        for splits in (0, 16, 32, 64, 128):
+            for _ in range(warmup):
+                call(case, out, lse, splits)
+            kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(steps)]
+            for a, b in kev:
+                a.record(stream)
+                b.record(stream)
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            torch.cuda.synchronize(dev)
+            start.record(stream)
+            for k in range(steps):
+                ink.set_timing_events("decode", kev[k][0], kev[k][1])
+                call(case, out, lse, splits)
+            end.record(stream)
+            torch.cuda.synchronize(dev)
+            ink.set_timing_events("decode", None, None)
+            ms = max_over_ranks(start.elapsed_time(end) / steps, dev)
+            kms = sum(a.elapsed_time(b) for a, b in kev) / steps
+            key = "library" if splits == 0 else str(splits)
+            res[key] = {"ms_per_step": round(ms, 4), "gbs": round(kv / (ms * 1e-3) / 1e9, 1),
+                        "kernel_gbs": round(kv / (kms * 1e-3) / 1e9, 1)}
+        res["library_splits"] = int(ink.num_splits(ink.Dims(case.T, case.B, case.H, case.Hkv, 128, case.num_blocks,
+                                                            case.BS, case.block_table.shape[1]),
+                                                   case.max_seqlen_q, max(case.kv_lens), -1, -1))
+        del case, out, lse
+        torch.cuda.empty_cache()
+        return res
+
     def measure_graph(steps, warmup):
         """A small decode step (8 requests, Lk 4096, H 32, Hkv 8, E 1024) called through the API every step
         and replayed from one captured CUDA graph: the host cost per step that the graph removes."""
@@ -589,6 +628,11 @@ def run_ours(args, rank, world, local_rank):
                 sec["kv_append_fp8"] = measure_append(max(3, steps // 2), max(3, warmup), fp8=True)
             except Exception as exc:
                 sec["kv_append_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
+        if "long_decode_splits" not in skip:
+            try:
+                sec["long_decode_splits"] = measure_split_sweep(max(5, steps // 2), max(3, warmup))
+            except Exception as exc:
+                sec["long_decode_splits"] = {"error": f"{type(exc).__name__}: {exc}"}
         if "graph_decode" not in skip:
             try:
                 sec["graph_decode"] = measure_graph(max(50, steps * 10), max(5, warmup))
@@ -648,6 +692,10 @@ def run_ours(args, rank, world, local_rank):
                 "e2e_ms": round(r["e2e_ms"], 4), "value": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
                 "unit": "GB/s", "desc": WORKLOADS["decode_batch"] + "; KV cache in E4M3 (1 byte per element)",
                 "gpu_launches": r["launches"], "clocks": r["clocks"], "roofline": rf}
+            continue
+        if name == "long_decode_splits":
+            workloads_out[name] = {"metric": "long decode KV-read GB/s by split count (step, and decode kernel)",
+                                   "desc": WORKLOADS["long_decode"], "unit": "GB/s", **r}
             continue
         if name == "graph_decode":
             workloads_out[name] = {
