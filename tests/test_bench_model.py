@@ -90,3 +90,15 @@ def test_clock_sampler_summarises_polled_samples():
     assert s["samples"] >= 3 and s["source"] == "nvml"
     assert s["sm_max_mhz"] == 2070.0 and s["sm_mhz"] in (1965.0, 2017.5, 2070.0)
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_cpu_baseline_repeats_passes_until_its_budget():
+    """The tiny mixed batch takes far less than the budget, so the baseline makes several full passes and
+    reports them; its value is the KV bytes of the requests it ran per second."""
+    r = bench.cpu_baseline("tiny_mix", 0.5)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["cores"] >= 1
+    assert r["seconds"] >= 0.5
+    passes = int(r["sample"].split("(")[1].split(" full passes")[0])
+    reqs = int(r["sample"].split(" requests")[0])
+    assert passes >= 2 and reqs >= 3 * passes
+    assert r["value"] > 0
