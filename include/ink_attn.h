@@ -27,8 +27,18 @@
  *     lse[t][h] = ln sum_j exp(s_j)           (natural log, fp32)
  * A row with no visible key gets out = 0 and lse = -inf.
  *
- * Every call is asynchronous on `stream`, allocates nothing, keeps no state
- * between calls and performs no host synchronisation.
+ * Besides the attention over a bf16 cache (ink_rel_attn_varlen and its
+ * allocation-free twin ink_rel_attn_varlen_static) the library has the same
+ * attention over an FP8 (E4M3) cache with per-tensor scales
+ * (ink_rel_attn_varlen_fp8kv, decode-shaped calls) and the KV append that
+ * precedes attention on every step (ink_reshape_and_cache, and
+ * ink_reshape_and_cache_fp8 which quantizes into an E4M3 cache).
+ *
+ * The attention and append calls are asynchronous on `stream`, allocate
+ * nothing and perform no host synchronisation; ink_rel_attn_read_device_errors
+ * is the one call that waits for its stream.  The only state kept between
+ * calls is a per-device SM count, the measurement hooks below and the static
+ * scratch area of ink_rel_attn_varlen_static.
  */
 #ifndef INK_ATTN_H
 #define INK_ATTN_H
