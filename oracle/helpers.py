@@ -21,46 +21,47 @@ def bucket_max_seqlen_q(max_seqlen_q: int) -> int:
 
 def page_num_splits(*, is_local: bool, batch_size: int, max_query_len: int, num_heads: int,
                     num_kv_heads: int, max_kv_len: int, capability_major: int = 10) -> int:
-    """Split-KV count of ``inkling_fa4_num_splits`` as the article prints it.
+    """Split-KV cap of the article's ``inkling_fa4_num_splits``, restated from its prose.
 
-    nxmr.cn article, layer 1 steps 1-5.  The page
-    lost its comparison operators; the reading taken is the one that keeps
-    the cap monotone in the number of KV heads per rank:
-      major 9 -> 1; local attention -> 1;
-      q_tiles = ceil(max_query_len * G / 256), base = batch * Hkv * q_tiles;
-      target = 256 (one q tile, batch 1), 128 (one q tile), else 64;
-      cap = 128, and for one q tile at batch 1:
-        16 if Hkv >= 8, elif Hkv >= 4 or max_kv <= 8192: 32,
-        elif max_kv <= 65536: 64, else 128;
-      result = max(1, min(target // base, cap, ceil(max_kv / 128))).
-    This is the page's Hopper/Blackwell-FA4 heuristic, kept as a pinned
+    nxmr.cn article, layer 1, the five steps that explain the function:
+      1. Hopper (capability 9) and local (windowed) attention take no split.
+      2. A KV head serves a group of max_query_len * (Hq / Hkv) query rows,
+         cut into tiles of 256 rows; one split of the whole batch launches
+         batch * Hkv * tiles CTAs.
+      3. The CTA count wanted: a lone one-tile request (long decode) 256, a
+         batch of one-tile requests 128, multi-tile prefill 64.
+      4. A hard cap, tuned only for the lone one-tile request (below); 128
+         otherwise.
+      5. The wanted CTAs over the CTAs of one split, limited by the cap and by
+         one split per 128 keys, and at least 1.
+    The page lost its comparison operators (reading R6): the caps of step 4
+    are taken as the first rule that holds in the order the article lists
+    them, with the comparisons that keep the cap monotone (more KV heads per
+    rank, fewer splits).  This is the page's heuristic, kept as a pinned
     reference function; the library's own split choice is derived for the
     GB300 SM count.  Pinned by the five workload shapes (3, 1, 1, 16, 1).
     """
-    if capability_major == 9:
+    if capability_major == 9 or is_local:  # step 1
         return 1
-    if is_local:
-        return 1
-    q_rows = max_query_len * (num_heads // num_kv_heads)
-    q_tiles = (q_rows + 255) // 256
-    base_ctas = batch_size * num_kv_heads * q_tiles
-    if q_tiles == 1 and batch_size == 1:
-        target_ctas = 256
-    elif q_tiles == 1:
-        target_ctas = 128
+    rows_per_group = max_query_len * (num_heads // num_kv_heads)  # step 2
+    tiles = -(-rows_per_group // 256)
+    ctas_per_split = batch_size * num_kv_heads * tiles
+    lone_decode = tiles == 1 and batch_size == 1
+    if lone_decode:  # step 3
+        ctas_wanted = 256
     else:
-        target_ctas = 64
-    max_splits = 128
-    if q_tiles == 1 and batch_size == 1:
-        if num_kv_heads >= 8:
-            max_splits = 16
-        elif num_kv_heads >= 4 or max_kv_len <= 8192:
-            max_splits = 32
-        elif max_kv_len <= 65536:
-            max_splits = 64
-        else:
-            max_splits = 128
-    return max(1, min(target_ctas // base_ctas, max_splits, (max_kv_len + 127) // 128))
+        ctas_wanted = 128 if tiles == 1 else 64
+    cap = 128  # step 4
+    if lone_decode:
+        rules = (
+            (num_kv_heads >= 8, 16),
+            (num_kv_heads >= 4 or max_kv_len <= 8192, 32),
+            (max_kv_len <= 65536, 64),
+            (True, 128),
+        )
+        cap = next(c for holds, c in rules if holds)
+    per_key_limit = -(-max_kv_len // 128)  # step 5
+    return max(1, min(ctas_wanted // ctas_per_split, cap, per_key_limit))
 
 
 def cu_seqlens_from_lengths(lengths: Sequence[int]) -> list[int]:
