@@ -72,6 +72,12 @@ def work_of(case):
     return kv_bytes, flops, pairs
 
 
+def prefill_keys(case):
+    """Cache keys of the prefill-shaped requests (more than 16 query rows per KV head), summed."""
+    G = case.H // case.Hkv
+    return sum(lk for lq, lk in zip(case.q_lens, case.kv_lens) if lq * G > 16)
+
+
 def total_bytes(case):
     """Compulsory HBM bytes of one step (reported beside the algorithmic headline)."""
     kv, _, _ = work_of(case)
@@ -322,7 +328,8 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     def attend(case, q, block_table, cache_seqlens, cu_seqlens_q, rel_logits, out, lse, splits=0):
-        """One call of the public API; an E4M3 cache (uint8) goes through the FP8 entry point."""
+        """One call of the public API; an E4M3 cache (uint8) goes through the FP8 entry point.  The caller knows
+        its batch, so the workspace is sized to stage the K/V of its prefill-shaped requests."""
         kw = dict(block_table=block_table, cache_seqlens=cache_seqlens, cu_seqlens_q=cu_seqlens_q,
                   max_seqlen_q=case.max_seqlen_q, softmax_scale=case.softmax_scale, causal=case.causal,
                   window_left=case.window_left, window_right=case.window_right, rel_extent=case.E,
@@ -330,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
         if case.key_cache.dtype == torch.uint8:
             return ink.ink_rel_attn_varlen_fp8kv(q, case.key_cache, case.value_cache, k_scale=FP8_SCALES[0],
                                                  v_scale=FP8_SCALES[1], **kw)
-        return ink.ink_rel_attn_varlen(q, case.key_cache, case.value_cache, **kw)
+        return ink.ink_rel_attn_varlen(q, case.key_cache, case.value_cache, stage_kv_tokens=prefill_keys(case),
+                                       **kw)
 
     def call(case, out, lse, splits=0):
         return attend(case, case.q, case.block_table, case.cache_seqlens, case.cu_seqlens_q, case.rel_logits, out,

@@ -106,6 +106,21 @@ INK_API size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t ma
                                    int32_t num_splits);
 
 /*
+ * Extra workspace bytes that let the prefill read the K and V of prefill-shaped
+ * requests (max_seqlen_q * H / Hkv > 16 rows) holding `prefill_kv_tokens` cache
+ * keys in total from a contiguous staging copy instead of the paged cache.
+ * The pages print no counterpart: this is a GB300 layout choice.  One K or V
+ * tile of one KV head is then 32 KB of consecutive bytes (one TMA box) instead
+ * of 128 rows of 256 bytes spread over 16-key pages, which the L2 delivers at a
+ * much higher rate.
+ * Workspace beyond ink_rel_attn_workspace_size is always used this way: each
+ * call copies, in request order, the pages of every prefill-shaped request
+ * whose keys (rounded up to whole 128-key tiles) still fit, and the rest read
+ * the paged cache.  Results do not depend on it.  Returns 0 for invalid dims.
+ */
+INK_API size_t ink_rel_attn_stage_bytes(const ink_attn_dims *dims, int64_t prefill_kv_tokens);
+
+/*
  * The split-KV count the library picks when called with num_splits = 0:
  * the cap on splits per work unit for decode-shaped calls
  * (max_seqlen_q * H / Hkv <= 16) and for prefill-shaped calls otherwise.
@@ -145,7 +160,8 @@ INK_API int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_s
  *   workspace     device memory of at least
  *                 ink_rel_attn_workspace_size(dims, max_seqlen_q, num_splits)
  *                 bytes, 256-byte aligned; it must not be used by another
- *                 call that overlaps this one on the GPU.
+ *                 call that overlaps this one on the GPU.  Bytes beyond that
+ *                 size stage K/V for the prefill (ink_rel_attn_stage_bytes).
  *   stream        CUDA stream the kernels are launched on.
  * Host-side checks return INK_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE
  * before anything is launched; a launch failure returns INK_ERR_CUDA.
@@ -203,10 +219,12 @@ INK_API ink_status ink_rel_attn_varlen_fp8kv(const ink_attn_dims *dims,
  * call runs on a scratch area of INK_STATIC_SCRATCH_BYTES compiled into the
  * library, which every GPU that loads the library holds until the process exits.
  *   - Work that needs more scratch than that (see ink_rel_attn_workspace_size)
- *     returns INK_ERR_WORKSPACE before anything is launched.
+ *     returns INK_ERR_WORKSPACE before anything is launched; scratch left over
+ *     stages K/V for the prefill, as with any workspace.
  *   - The first call on a device looks up the scratch area's device address for
  *     that device (with it current) and caches it; make that first call before
- *     any stream capture.
+ *     any stream capture.  The cached address is not valid after a reset of the
+ *     device (cudaDeviceReset): do not call this entry point after one.
  *   - Every call, on every stream, shares the one scratch area of its device, and
  *     the area keeps the last call's contents (each call clears what must start
  *     at zero).  Calls that overlap on the GPU race on it: order them, for
@@ -295,7 +313,8 @@ typedef enum {
     INK_KERNEL_DECODE = 2,
     INK_KERNEL_PREFILL = 3,
     INK_KERNEL_COMBINE = 4,
-    INK_KERNEL_APPEND = 5
+    INK_KERNEL_APPEND = 5,
+    INK_KERNEL_STAGE = 6
 } ink_kernel_id;
 
 INK_API void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event);

@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "LibraryNotBuilt", "InkError", "Dims", "build", "load", "ink_rel_attn_varlen", "workspace_size",
     "num_splits", "read_device_errors", "version", "DEVERR", "set_timing_events", "launch_count",
-    "reshape_and_cache", "ink_rel_attn_varlen_fp8kv", "reshape_and_cache_fp8",
+    "reshape_and_cache", "ink_rel_attn_varlen_fp8kv", "reshape_and_cache_fp8", "stage_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +77,8 @@ def load(path: Optional[str] = None):
         dp = ctypes.POINTER(Dims)
         lib.ink_rel_attn_workspace_size.restype = sz
         lib.ink_rel_attn_workspace_size.argtypes = [dp, i32, i32]
+        lib.ink_rel_attn_stage_bytes.restype = sz
+        lib.ink_rel_attn_stage_bytes.argtypes = [dp, ctypes.c_int64]
         lib.ink_rel_attn_num_splits.restype = i32
         lib.ink_rel_attn_num_splits.argtypes = [dp, i32, i32, i32, i32]
         lib.ink_rel_attn_varlen.restype = ctypes.c_int
@@ -108,7 +110,7 @@ def version() -> int:
     return int(load().ink_attn_version())
 
 
-KERNELS = {"prepass": 1, "decode": 2, "prefill": 3, "combine": 4, "append": 5}
+KERNELS = {"prepass": 1, "decode": 2, "prefill": 3, "combine": 4, "append": 5, "stage": 6}
 
 
 def set_timing_events(kernel: str, start=None, stop=None) -> None:
@@ -134,6 +136,12 @@ def workspace_size(dims: Dims, max_seqlen_q: int, num_splits: int = 0) -> int:
     if n == 0:
         raise InkError(1, "ink_rel_attn_workspace_size")
     return int(n)
+
+
+def stage_bytes(dims: Dims, prefill_kv_tokens: int) -> int:
+    """Extra workspace bytes that stage the K/V of prefill-shaped requests holding `prefill_kv_tokens` cache
+    keys in total (ink_rel_attn_stage_bytes)."""
+    return int(load().ink_rel_attn_stage_bytes(ctypes.byref(dims), int(prefill_kv_tokens)))
 
 
 def num_splits(dims: Dims, max_seqlen_q: int, max_kv_len: int, window_left: int = -1,
@@ -169,7 +177,7 @@ def _check(t: torch.Tensor, name: str, dtype, dim: int, device):
 
 
 def _prepare(q, key_cache, value_cache, cache_dtype, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
-             rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream):
+             rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream, stage_kv_tokens=0):
     """Checks and marshals the arguments both attention entry points share."""
     dev = q.device
     if dev.type != "cuda":
@@ -206,6 +214,8 @@ def _prepare(q, key_cache, value_cache, cache_dtype, block_table, cache_seqlens,
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     need = workspace_size(dims, max_seqlen_q, num_splits)
+    if stage_kv_tokens:
+        need += stage_bytes(dims, stage_kv_tokens)
     if workspace is None:
         workspace = _workspace(dev, need, stream)
     return dims, rel_ptr, out, lse, workspace, stream
@@ -215,18 +225,20 @@ def ink_rel_attn_varlen(q, key_cache, value_cache, *, block_table, cache_seqlens
                         max_seqlen_q: int, softmax_scale: float, causal: bool = True,
                         window_left: int = -1, window_right: int = -1, rel_extent: int = 0,
                         rel_logits=None, num_splits: int = 0, out=None, lse=None,
-                        return_lse: bool = False, workspace=None, stream=None):
+                        return_lse: bool = False, workspace=None, stream=None, stage_kv_tokens: int = 0):
     """Paged varlen attention with the Inkling relative bias (see include/ink_attn.h).
 
     Keyword arguments follow ``inkling_fa4_rel_attention`` (fa4_rel_attention.py
     as quoted by the nxmr.cn article, its wrapper signature), with the window
-    passed as two integers (-1 = unbounded).  Returns ``out`` (and ``lse``
-    when ``return_lse``).
+    passed as two integers (-1 = unbounded).  ``stage_kv_tokens`` (the cache
+    keys of the prefill-shaped requests, summed) sizes the workspace so that
+    their K/V is staged contiguously (ink_rel_attn_stage_bytes); results do not
+    depend on it.  Returns ``out`` (and ``lse`` when ``return_lse``).
     """
     lib = load()
     dims, rel_ptr, out, lse, workspace, stream = _prepare(
         q, key_cache, value_cache, torch.bfloat16, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
-        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream)
+        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream, stage_kv_tokens)
     rc = lib.ink_rel_attn_varlen(
         ctypes.byref(dims), q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
         block_table.data_ptr(), cache_seqlens.data_ptr(), cu_seqlens_q.data_ptr(), int(max_seqlen_q),

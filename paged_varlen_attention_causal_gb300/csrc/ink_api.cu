@@ -26,7 +26,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct TimingHook {
     cudaEvent_t start = nullptr, stop = nullptr;
 };
-TimingHook g_hooks[6];
+TimingHook g_hooks[7];
 std::mutex g_hook_mutex;
 std::atomic<unsigned long long> g_launches{0};
 
@@ -81,6 +81,7 @@ struct Plan {
     bool any_prefill = false, any_decode = false;
     // workspace offsets
     size_t off_dec_items = 0, off_pf_items = 0, off_dec_off = 0, off_unit_off = 0, off_comb_off = 0;
+    size_t off_stg_off = 0, off_stg_pg_off = 0;
     size_t off_pdo = 0, off_pdl = 0, off_ppo = 0, off_ppl = 0, total = 0;
 };
 
@@ -189,6 +190,8 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     pl.off_dec_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     pl.off_unit_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     pl.off_comb_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
+    pl.off_stg_off = off; off = align256(off + sizeof(int) * (size_t)B);
+    pl.off_stg_pg_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     const bool dec_parts = pl.any_decode && sdec_eff > 1;
     const bool pf_parts = pl.any_prefill && pl.S_pf > 1;
     const size_t dec_rows_total = dec_parts ? (size_t)pl.dec_cap * pl.dec_rows : 0;
@@ -238,7 +241,7 @@ int32_t ink_attn_version(void) { return 100; }
 
 void ink_set_timing_events(ink_kernel_id kernel, void *start_event, void *stop_event)
 {
-    if ((int)kernel < 1 || (int)kernel > 5) return;
+    if ((int)kernel < 1 || (int)kernel > 6) return;
     std::lock_guard<std::mutex> lk(g_hook_mutex);
     g_hooks[kernel].start = static_cast<cudaEvent_t>(start_event);
     g_hooks[kernel].stop = static_cast<cudaEvent_t>(stop_event);
@@ -269,6 +272,15 @@ size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t max_seqlen
     if (make_plan(dims, max_seqlen_q, num_splits, 0, -1, -1, sms > 0 ? sms : 152, pl2))
         return std::max(pl.total, pl2.total);
     return pl.total;
+}
+
+size_t ink_rel_attn_stage_bytes(const ink_attn_dims *dims, int64_t prefill_kv_tokens)
+{
+    if (!dims_ok(dims) || prefill_kv_tokens < 0) return 0;
+    // every staged request occupies whole 128-key tiles: at most 127 keys of rounding per request
+    const long long keys = prefill_kv_tokens + (long long)dims->batch * (kTileKeys - 1);
+    const long long tiles = (keys + kTileKeys - 1) / kTileKeys;
+    return (size_t)tiles * kTileKeys * dims->num_kv_heads * kHeadDim * 2 * 2;
 }
 
 int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_seqlen_q, int32_t max_kv_len,
@@ -378,6 +390,19 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.part_dec_lse = reinterpret_cast<float *>(ws + pl.off_pdl);
     p.part_dec_o = reinterpret_cast<float *>(ws + pl.off_pdo);
     p.dec_rows = pl.dec_rows;
+    p.stg_off = reinterpret_cast<int *>(ws + pl.off_stg_off);
+    p.stg_pg_off = reinterpret_cast<int *>(ws + pl.off_stg_pg_off);
+    // K/V staging: workspace beyond the minimum holds whole 128-key tiles of K and V planes for
+    // prefill-shaped requests (an FP8 cache and decode-only calls stage nothing)
+    {
+        const size_t per_key = (size_t)Hkv * kHeadDim * 2 * 2;  // K and V, every KV head
+        const size_t extra = workspace_bytes - pl.total;
+        long long cap = (long long)(extra / per_key) / kTileKeys * kTileKeys;
+        cap = std::min<long long>(cap, 1ll << 24);
+        p.stage_cap = (!kv.fp8 && pl.any_prefill && cap >= kTileKeys) ? (int)cap : 0;
+        p.ks = reinterpret_cast<__nv_bfloat16 *>(ws + pl.total);
+        p.vs = p.ks + (size_t)Hkv * p.stage_cap * kHeadDim;
+    }
     p.part_pf_lse = reinterpret_cast<float *>(ws + pl.off_ppl);
     p.part_pf_o = reinterpret_cast<float *>(ws + pl.off_ppo);
     p.units_cap = (int)pl.units_cap;
@@ -444,9 +469,28 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
                              CU_TENSOR_MAP_SWIZZLE_NONE);
     }
 
+    // staging planes as (64 d, keys, d half, Hkv): one (64, 128, 2, 1) box is a 128-key tile of one
+    // KV head, 32 KB of consecutive bytes, landing as [d half][128 keys][128 B] (128-byte swizzle)
+    alignas(64) CUtensorMap tm_ks, tm_vs;
+    memset(&tm_ks, 0, sizeof tm_ks); memset(&tm_vs, 0, sizeof tm_vs);
+    if (p.stage_cap > 0) {
+        const cuuint64_t gds[4] = {64, (cuuint64_t)p.stage_cap, 2, (cuuint64_t)Hkv};
+        const cuuint64_t gss[3] = {(cuuint64_t)kHeadDim * 2, 128, (cuuint64_t)p.stage_cap * kHeadDim * 2};
+        const cuuint32_t boxs[4] = {64, (cuuint32_t)kTileKeys, 2, 1};
+        if (!encode(&tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.ks, gds, gss, boxs, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.vs, gds, gss, boxs, CU_TENSOR_MAP_SWIZZLE_128B))
+            return INK_ERR_CUDA;
+    }
+
     // 1. device-side plan
     if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, stream); }) != cudaSuccess)
         return INK_ERR_CUDA;
+
+    // 1b. K/V staging copy for the prefill
+    if (p.stage_cap > 0) {
+        if (timed_launch(INK_KERNEL_STAGE, stream, [&] { return launch_stage(p, sms, stream); }) != cudaSuccess)
+            return INK_ERR_CUDA;
+    }
 
     // 2. decode kernel
     if (pl.any_decode && pl.dec_cap > 0) {
@@ -479,7 +523,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);
         if (timed_launch(INK_KERNEL_PREFILL, stream,
-                         [&] { return launch_prefill(pp, tm_k, tm_vp, tm_bpf, grid, smem, stream); }) != cudaSuccess)
+                         [&] { return launch_prefill(pp, tm_k, tm_vp, tm_bpf, tm_ks, tm_vs, grid, smem, stream); }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
 

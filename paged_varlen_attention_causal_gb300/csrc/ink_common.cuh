@@ -32,7 +32,8 @@ struct WsHeader {
     uint32_t dec_next;     // dynamic scheduler counter of the decode kernel
     uint32_t pf_next;      // dynamic scheduler counter of the prefill kernel
     uint32_t comb_tokens;  // tokens whose rows the split-KV merge visits (prepass)
-    uint32_t pad[58];
+    uint32_t stage_pages;  // 16-key pages the K/V staging copies (prepass)
+    uint32_t pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 
@@ -57,6 +58,12 @@ struct Params {
     int *dec_off;      // (B+1) first decode item of each request (prepass)
     int *unit_off;     // (B+1) first prefill unit (q tile) of each request (prepass)
     int *comb_off;     // (B+1) first merge-list token of each request (prepass)
+    // K/V staging: prefill-shaped requests whose keys fit get a contiguous copy of their K and V
+    // pages, per KV head, in the workspace (see ink_stage.cu)
+    int *stg_off;      // (B) first staged key of each request, -1 when it reads the paged cache (prepass)
+    int *stg_pg_off;   // (B+1) first staged page of each request in the copy's work list (prepass)
+    int stage_cap;     // keys per KV head the staging area holds (0: no staging)
+    __nv_bfloat16 *ks, *vs;  // staging area: (Hkv, stage_cap, D) each
     // split partials: one block per decode item, and per (prefill unit, split)
     float *part_dec_o, *part_dec_lse;  // (dec_items_cap, dec_rows, D), (dec_items_cap, dec_rows)
     int dec_rows;                      // rows per decode block: (16 / G) * H
@@ -141,6 +148,10 @@ __host__ __device__ __forceinline__ UnitSplit unit_split(int qa0, int qa1, int L
     return u;
 }
 
+// Keys a staged request occupies in the staging area: its cache length rounded up to whole
+// 128-key tiles, so that every tile box of the request stays inside its own keys.
+__host__ __device__ __forceinline__ int stage_keys_of(int Lk) { return (Lk + kTileKeys - 1) / kTileKeys * kTileKeys; }
+
 // Prefill bias staging.  One TMA box holds the rel_logits rows of nb consecutive tokens
 // (all G heads) for one 128-key tile.  The distance span of token k + 1 starts one key
 // later than token k's, so a common start rounded down to 16 bytes and a width of
@@ -222,6 +233,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Non-blocking test of a phase parity (acquire when it has completed).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The same test for a whole warp: true only when every lane has seen the phase complete
+// (each lane acquires for itself), so the lanes agree and stay converged.
+__device__ __forceinline__ bool warp_poll(uint64_t *bar, uint32_t parity)
+{
+    return __all_sync(0xffffffffu, mbar_test_wait(bar, parity));
 }
 
 // try_wait whose suspension is bounded by a hint (ns), so that a caller can
@@ -356,8 +388,10 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
                           int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int grid, size_t smem,
                           cudaStream_t stream);
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream);
+                           const CUtensorMap &tm_bias, const CUtensorMap &tm_ks, const CUtensorMap &tm_vs, int grid,
+                           size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
+cudaError_t launch_stage(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
                           void *value_cache, const int64_t *slot_mapping, uint32_t *flags, int sms,
                           cudaStream_t stream);

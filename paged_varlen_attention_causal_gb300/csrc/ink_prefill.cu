@@ -31,6 +31,11 @@
 namespace ink {
 
 constexpr int kPfThreads = 12 * 32;
+constexpr int kPfLaunchRegs = 168;          // registers per thread at launch (65536 / 384, rounded down to 8)
+constexpr int kPfProducerRegs = 80;         // warpgroup 0 (warps 0-3) after setmaxnreg.dec
+constexpr int kPfSoftmaxRegs = 208;        // warpgroups 1 and 2 (softmax) after setmaxnreg.inc
+static_assert(128 * kPfProducerRegs + 256 * kPfSoftmaxRegs <= kPfThreads * kPfLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kKvSlots = 2;
 constexpr int kSSlots = 2;
 constexpr int kBiasSlots = 2;
@@ -194,13 +199,14 @@ __device__ __forceinline__ int pf_item_index(int r)
 // 16-byte chunk and O = (q_abs - j0 - 127) mod 4 is a compile-time constant
 // here.  17 aligned 16-byte loads cover the 68 floats the half needs.
 template <int O>
-__device__ __forceinline__ void bias_add(const float *box, float inv_scale, uint32_t (&s)[64])
+__device__ __forceinline__ void bias_add(uint32_t box, float inv_scale, uint32_t (&s)[64])
 {
-    const float4 *b4 = reinterpret_cast<const float4 *>(box);
 #pragma unroll
     for (int m = 0; m < 17; ++m) {
-        const float4 f = b4[m];
-        const float e[4] = {f.x, f.y, f.z, f.w};
+        float e[4];
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(e[0]), "=f"(e[1]), "=f"(e[2]), "=f"(e[3])
+                     : "r"(box + 16 * m));
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int c = O + 63 - (4 * m + u);
@@ -211,7 +217,8 @@ __device__ __forceinline__ void bias_add(const float *box, float inv_scale, uint
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     ink_prefill_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias)
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
+                       const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs)
 {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
@@ -269,11 +276,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem_o = tmem + kSSlots * 128;
     const uint32_t tmem_q = tmem_o + 128;
 
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfProducerRegs));
     if (warp == 0) {
         // ---------------------------------------------------------------- K/V producer
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
+            if (p.stage_cap > 0) {
+                prefetch_tmap(&tm_ks);
+                prefetch_tmap(&tm_vs);
+            }
         }
         const uint64_t pol_kv = policy_evict_last();
         uint32_t seq = 0;
@@ -282,6 +295,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (idx >= total || *abort) break;
             const PfItem it = pf_item(p, p.pf_items[idx]);
             if (it.ntiles == 0) continue;
+            // staged request: its keys sit at staged key so + j of each KV head's plane
+            const int so = p.stage_cap > 0 ? __ldg(p.stg_off + it.b) : -1;
             const int32_t *bt_row = p.bt + (size_t)it.b * p.MAXBLK;
             // key coordinate of group gb + 32 * chunk + lane (-16, i.e. zero fill, past the split or on a bad page)
             auto load_keys = [&](int chunk) {
@@ -294,7 +309,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 return key;
             };
-            int keys_cur = load_keys(0), keys_nxt = load_keys(1), chunk = 0;
+            int keys_cur = so >= 0 ? 0 : load_keys(0), keys_nxt = so >= 0 ? 0 : load_keys(1), chunk = 0;
             // load order: K0, then K_n, V_{n-1} for n >= 1, then V_{last}
             for (int step = 0; step <= it.ntiles; ++step) {
                 for (int which = 0; which < 2; ++which) {
@@ -303,7 +318,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     else if (step == it.ntiles) { if (which) break; n = it.ntiles - 1; isV = 1; }
                     else { n = which ? step - 1 : step; isV = which; }
                     int key0;
-                    if (!isV) {
+                    if (so >= 0) {
+                        key0 = so + pf_tile_key0(it, n);
+                    } else if (!isV) {
                         while (chunk < n / 4) {  // advance the prefetch window by 32 groups
                             keys_cur = keys_nxt;
                             ++chunk;
@@ -319,7 +336,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!mbar_wait_warp(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
                     if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
                     __syncwarp();
-                    if (!isV && lane < 16) {
+                    if (so >= 0) {
+                        // staged: the tile is 128 consecutive keys of the KV head's plane, one box that
+                        // lands as [d half][128 keys][128 B] for K and for V
+                        if (lane == 0)
+                            tma_load_4d_hint(kv_smem + slot * kSlotBytes, isV ? &tm_vs : &tm_ks, 0, key0, 0, it.g,
+                                             &sh.kv_full[slot], pol_kv);
+                    } else if (!isV && lane < 16) {
                         // K tile: [d half][128 keys][128 B]; one box per page and d half
                         const int grp = lane & 7, dh = lane >> 3;
                         uint8_t *dst = kv_smem + slot * kSlotBytes + dh * 16384 + grp * 2048;
@@ -384,11 +407,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (it.ntiles == 0) continue;
             if (!mbar_wait_warp(&sh.q_full, qseq & 1, abort, p)) break;
             const uint32_t tc0 = tc;
+            const bool staged = p.stage_cap > 0 && __ldg(p.stg_off + it.b) >= 0;
             auto zero_tail = [&](int slot, int n, bool v_layout) {
-                // keys at or beyond Lk inside loaded groups may hold stale data: zero them
+                // keys at or beyond Lk inside loaded groups may hold stale data: zero them.  A
+                // staged tile holds 128 keys whatever the split: zero every key past the split
+                // too (the staging area beyond a request's last page is never written).
                 const int j0 = pf_tile_key0(it, n);
-                const int loaded = min(8, it.ge - (it.gb + 8 * n)) * kKeyGroup;
-                const int z0 = max(0, it.Lk - j0);
+                int loaded = min(8, it.ge - (it.gb + 8 * n)) * kKeyGroup;
+                int z0 = max(0, it.Lk - j0);
+                if (staged) {
+                    z0 = min(z0, loaded);
+                    loaded = kTileKeys;
+                    v_layout = false;  // staged V lands as [d half][128 keys][128 B], like K
+                }
                 if (z0 < loaded) {
                     uint8_t *t = kv_smem + slot * kSlotBytes;
                     for (int c = lane; c < (loaded - z0) * 16; c += 32) {  // 16 chunks of 16 B per row
@@ -401,35 +432,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 __syncwarp();
             };
-            auto issue_pv = [&](int m) {
-                const uint32_t t = tc0 + m;
-                const int ss = t % kSSlots;
-                if (!mbar_wait_warp(&sh.p_full[ss], (t / kSSlots) & 1, abort, p)) return false;
-                const int slot = seq % kKvSlots;
-                if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) return false;
-                zero_tail(slot, m, true);
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t vaddr = smem_u32(kv_smem + slot * kSlotBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // keys 16kk .. 16kk + 15 are page kk: d halves 2 KB apart, 8-key groups 1 KB apart
-                        const uint64_t bdesc = smem_desc(vaddr + kk * 4096, 2048, 1024);
-                        mma_ts(tmem_o, tmem + ss * 128 + kk * 8, bdesc, kIdescPV, (m > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&sh.kv_empty[slot]);
-                    mma_commit(&sh.pv_done[ss]);
-                }
-                __syncwarp();
-                ++seq;
-                return true;
-            };
-            bool ok = true;
-            for (int n = 0; n < it.ntiles && ok; ++n) {
-                const uint32_t t = tc0 + n;
-                const int ss = t % kSSlots;
-                const int slot = seq % kKvSlots;
-                if (!mbar_wait_warp(&sh.kv_full[slot], (seq / kKvSlots) & 1, abort, p)) { ok = false; break; }
+            // Ring positions of the item's K and V tiles in the producer's order (K0, then K_n, V_{n-1}
+            // for n >= 1, then V_last).
+            auto seq_k = [&](int n) { return seq + (n == 0 ? 0u : (uint32_t)(2 * n - 1)); };
+            auto seq_v = [&](int m) { return seq + (m == it.ntiles - 1 ? (uint32_t)(2 * it.ntiles - 1) : (uint32_t)(2 * m + 2)); };
+            auto issue_qk = [&](int n) {
+                const uint32_t t = tc0 + n, sq = seq_k(n);
+                const int ss = t % kSSlots, slot = sq % kKvSlots;
                 zero_tail(slot, n, false);
                 tc_fence_after();
                 if (lane == 0) {
@@ -446,17 +455,73 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     mma_commit(&sh.kv_empty[slot]);
                 }
                 __syncwarp();
-                ++seq;
-                if (n >= 1) ok = issue_pv(n - 1);
+            };
+            auto issue_pv = [&](int m) {
+                const uint32_t t = tc0 + m, sq = seq_v(m);
+                const int ss = t % kSSlots, slot = sq % kKvSlots;
+                zero_tail(slot, m, true);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t vaddr = smem_u32(kv_smem + slot * kSlotBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // keys 16kk .. 16kk + 15: paged, page kk, d halves 2 KB apart; staged, rows
+                        // 16kk.. of [d half][128 keys], d halves 16 KB apart; 8-key groups 1 KB apart
+                        const uint64_t bdesc = staged ? smem_desc(vaddr + kk * 2048, 16384, 1024)
+                                                      : smem_desc(vaddr + kk * 4096, 2048, 1024);
+                        mma_ts(tmem_o, tmem + ss * 128 + kk * 8, bdesc, kIdescPV, (m > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&sh.kv_empty[slot]);
+                    mma_commit(&sh.pv_done[ss]);
+                }
+                __syncwarp();
+            };
+            // Step n issues QK(n) and PV(n - 1), whichever can go first: QK(n) needs K(n), PV(n - 1)
+            // needs P(n - 1) and V(n - 1).  They touch different S slots, and QK(n)'s slot was last
+            // read by PV(n - 2), issued in the previous step, so either order is safe.  Polling both
+            // keeps a late K(n) from holding back PV(n - 1) and the reverse.
+            bool ok = true;
+            for (int n = 0; n <= it.ntiles && ok; ++n) {
+                bool qk_todo = n < it.ntiles, pv_todo = n >= 1;
+                const uint64_t t0 = global_timer_ns();
+                while (qk_todo || pv_todo) {
+                    if (qk_todo) {
+                        const uint32_t sq = seq_k(n);
+                        if (warp_poll(&sh.kv_full[sq % kKvSlots], (sq / kKvSlots) & 1)) {
+                            issue_qk(n);
+                            qk_todo = false;
+                            continue;
+                        }
+                    }
+                    if (pv_todo) {
+                        const uint32_t t = tc0 + n - 1, sq = seq_v(n - 1);
+                        if (warp_poll(&sh.p_full[t % kSSlots], (t / kSSlots) & 1) &&
+                            warp_poll(&sh.kv_full[sq % kKvSlots], (sq / kKvSlots) & 1)) {
+                            issue_pv(n - 1);
+                            pv_todo = false;
+                            continue;
+                        }
+                    }
+                    if (*abort) { ok = false; break; }
+                    __nanosleep(20);
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        report(p, INK_DEVERR_TIMEOUT);
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                }
             }
-            if (ok) ok = issue_pv(it.ntiles - 1);
+            seq += 2 * it.ntiles;
             if (ok && lane == 0) mma_commit(&sh.o_full);
             __syncwarp();
             tc += it.ntiles;
             ++qseq;
             if (!ok) break;
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfSoftmaxRegs));
         // ---------------------------------------------------------------- softmax + epilogue + Q
         const int h = (warp >= 8) ? 1 : 0;   // key half: columns 64h .. 64h + 63 of every S tile
         const int quarter = warp & 3;        // TMEM lanes 32 * quarter .. + 31
@@ -537,8 +602,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int kb = k >> p.bias_tok_log2, ki = k & (bias_nb - 1);
             const int ko = (qa - (kTileKeys - 1)) - ((it.qa_min + (kb << p.bias_tok_log2) - (kTileKeys - 1)) & ~3);
             const int bo = ko & 3;
-            const float *box_row = reinterpret_cast<const float *>(bias_smem + kb * bias_box) +
-                                   (ki * p.G + j) * bias_w + 4 * (ko >> 2) + 64 * (1 - h);
+            const uint32_t box_row = smem_u32(bias_smem) + kb * bias_box +
+                                     ((ki * p.G + j) * bias_w + 4 * (ko >> 2) + 64 * (1 - h)) * 4;
             const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
             float m_used = -INFINITY;  // raw-score units
             float l = 0.f;             // this half's share of the row sum
@@ -559,7 +624,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         const int bs = bseq % kBiasSlots;
                         if (!mbar_wait_warp(&sh.bias_full[bs], (bseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
                         if (row_ok) {
-                            const float *box = box_row + bs * (bias_stage / 4);
+                            const uint32_t box = box_row + bs * bias_stage;
                             switch (bo) {
                                 case 0: bias_add<0>(box, inv_scale, sv); break;
                                 case 1: bias_add<1>(box, inv_scale, sv); break;
@@ -725,11 +790,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_bias, int grid, size_t smem, cudaStream_t stream)
+                           const CUtensorMap &tm_bias, const CUtensorMap &tm_ks, const CUtensorMap &tm_vs, int grid,
+                           size_t smem, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(ink_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // setmaxnreg redistributes the registers the CTA was launched with: the split above
+    // assumes exactly kPfLaunchRegs per thread, so refuse to launch on any other count.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, ink_prefill_kernel);
     if (e != cudaSuccess) return e;
-    ink_prefill_kernel<<<grid, kPfThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias);
+    if (fa.numRegs != kPfLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(ink_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ink_prefill_kernel<<<grid, kPfThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias, tm_ks, tm_vs);
     return cudaGetLastError();
 }
 

@@ -45,6 +45,34 @@ __device__ int block_exclusive_scan(int v, int *out, int *warp_sums)
     return total;
 }
 
+// The same scan in 64 bits (sums that may exceed the int range).
+__device__ long long block_exclusive_scan_ll(long long v, long long *out, long long *warp_sums)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const long long total = warp_sums[31];
+    *out = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    __syncthreads();
+    return total;
+}
+
 __device__ __forceinline__ void pf_unit_of(const Params &p, const Req &r, int qt, int &qa0, int &qa1)
 {
     const int i0 = qt * p.tpt, i1 = min(r.Lq, i0 + p.tpt) - 1;
@@ -66,6 +94,9 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     __shared__ int bucket_count[kCostBuckets];
     __shared__ int bucket_base[kCostBuckets];
     __shared__ int s_carry[3];
+    __shared__ long long warp_sums_ll[32];
+    __shared__ long long s_stg_carry;
+    __shared__ int s_pg_carry;
     __shared__ uint32_t s_err;
     __shared__ int s_overflow;
 
@@ -82,6 +113,9 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         p.hdr->pf_next = 0;
         p.hdr->comb_tokens = 0;
         s_carry[0] = s_carry[1] = s_carry[2] = 0;
+        s_stg_carry = 0;
+        s_pg_carry = 0;
+        p.hdr->stage_pages = 0;
         uint32_t e = 0;
         if (__ldg(p.cu) != 0 || __ldg(p.cu + p.B) != p.T) e |= INK_DEVERR_CU_SEQLENS;
         s_err = e;
@@ -142,6 +176,46 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     if (my_err) atomicOr(&s_err, my_err);
     __syncthreads();
     __threadfence_block();
+
+    // K/V staging: prefill-shaped requests, in request order, take whole 128-key tiles of the
+    // staging area while it has room; the rest read the paged cache.  Then the page work list
+    // of the copy (one entry per staged 16-key page).
+    if (p.stage_cap > 0) {
+        for (int base = 0; base < p.B; base += blockDim.x) {
+            const int b = base + tid;
+            long long need = 0;
+            int pages = 0;
+            if (b < p.B) {
+                const Req r = load_req(p, b);
+                if (r.ok && r.Lq > 0 && !is_decode_req(p, r) && r.Lk > 0) need = stage_keys_of(r.Lk);
+            }
+            long long x;
+            const long long tot = block_exclusive_scan_ll(need, &x, warp_sums_ll);
+            bool staged = false;
+            if (b < p.B) {
+                const long long at = s_stg_carry + x;
+                staged = need > 0 && at + need <= p.stage_cap;
+                p.stg_off[b] = staged ? (int)at : -1;
+                if (staged) pages = (__ldg(p.seqk + b) + kKeyGroup - 1) / kKeyGroup;
+            }
+            int xp;
+            const int totp = block_exclusive_scan(pages, &xp, warp_sums);
+            if (b < p.B) p.stg_pg_off[b] = s_pg_carry + xp;
+            __syncthreads();
+            if (tid == 0) {
+                s_stg_carry += tot;
+                s_pg_carry += totp;
+            }
+            __syncthreads();
+        }
+        if (tid == 0) {
+            p.stg_pg_off[p.B] = s_pg_carry;
+            p.hdr->stage_pages = (uint32_t)s_pg_carry;
+        }
+    } else {
+        for (int b = tid; b < p.B; b += blockDim.x) p.stg_off[b] = -1;
+    }
+    __syncthreads();
 
     const int n_dec = s_overflow ? 0 : min(s_carry[0], p.dec_items_cap);
     const int n_units = s_overflow ? 0 : s_carry[1];

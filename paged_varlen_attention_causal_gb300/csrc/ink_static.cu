@@ -47,9 +47,9 @@ extern "C" INK_API ink_status ink_rel_attn_varlen_static(
     float softmax_scale, int causal, int32_t window_left, int32_t window_right, int32_t rel_extent,
     const float *rel_logits, int32_t num_splits, void *out, float *lse, ink_stream_t stream)
 {
-    // Work that needs more scratch than the fixed area is refused before anything runs.
-    const size_t need = ink_rel_attn_workspace_size(dims, max_seqlen_q, num_splits);
-    if (need > (size_t)INK_STATIC_SCRATCH_BYTES) return INK_ERR_WORKSPACE;
+    // Work that needs more scratch than the fixed area is refused before anything runs: the call
+    // below checks its actual plan (window and causality included) against the area and returns
+    // INK_ERR_WORKSPACE; room left over stages K/V for the prefill as with any workspace.
     void *scratch = nullptr;
     const ink_status st = scratch_address(&scratch);
     if (st != INK_OK) return st;
