@@ -148,7 +148,7 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     // prefill bias boxes: as many tokens per box (up to 8) as the shared-memory budget allows
     for (int lg = 3; lg >= 0; --lg) {
         if ((1 << lg) > pl.tpt) continue;
-        const size_t need = 1024 + 2 * 32768 + 2 * (size_t)pf_bias_stage_bytes(pl.G, pl.tpt, 1 << lg) + kPfSharedBytes;
+        const size_t need = 1024 + pf_layout_bytes(pl.G, pl.tpt, 1 << lg);
         if (need <= kSmemLimit || lg == 0) {
             pl.bias_tok_log2 = lg;
             break;
@@ -518,7 +518,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         pp.bias_tma = bias_pf_tma ? 1 : 0;
         // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
         const size_t layout =
-            2 * 32768 + 2 * (size_t)pf_bias_stage_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2) + kPfSharedBytes;
+            pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2);
         if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);

@@ -152,18 +152,26 @@ __host__ __device__ __forceinline__ UnitSplit unit_split(int qa0, int qa1, int L
 // 128-key tiles, so that every tile box of the request stays inside its own keys.
 __host__ __device__ __forceinline__ int stage_keys_of(int Lk) { return (Lk + kTileKeys - 1) / kTileKeys * kTileKeys; }
 
-// Prefill bias staging.  One TMA box holds the rel_logits rows of nb consecutive tokens
-// (all G heads) for one 128-key tile.  The distance span of token k + 1 starts one key
-// later than token k's, so a common start rounded down to 16 bytes and a width of
-// 128 + 3 + (nb - 1) floats, rounded up to 16 bytes, cover every token of the box.
-__host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (131 + nb + 3) & ~3; }
+// Prefill bias staging, by half tiles: one TMA box holds, for one 64-key half of a 128-key
+// tile, the rel_logits rows of nb consecutive tokens (all G heads).  The distance span of
+// token k + 1 starts one key later than token k's, so a common start rounded down to 16
+// bytes and a width of 64 + 3 + (nb - 1) floats, rounded up to 16 bytes, cover every token
+// of the box (the softmax reads 17 whole 16-byte chunks from the one holding a row's start).
+constexpr int kPfKvSlots = 3;     // prefill K/V ring (32 KB slots)
+constexpr int kPfBiasSlots = 3;   // prefill bias ring (half-tile stages)
+__host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (70 + nb) & ~3; }
 // Bytes a box transfers, and its shared-memory footprint (a TMA destination is 128-byte aligned).
 __host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb) { return nb * G * pf_bias_width(nb) * 4; }
 __host__ __device__ __forceinline__ int pf_bias_box_stride(int G, int nb) { return (pf_bias_box_bytes(G, nb) + 127) & ~127; }
-// One stage: the boxes of a q tile of tpt tokens.
+// One stage: the boxes of a q tile of tpt tokens, for one key half.
 __host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int nb)
 {
     return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb);
+}
+// The prefill kernel's shared-memory layout: K/V ring, bias ring, bookkeeping.
+__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb)
+{
+    return (size_t)kPfKvSlots * 32768 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
 }
 
 // Packed row of (token offset k, head j) inside a prefill tile, and back.

@@ -10,13 +10,14 @@
 //   warp 0      page-gather producer: block_table entries are prefetched 32
 //               groups ahead; per 16-key page two TMA boxes of K (d halves,
 //               128-byte swizzle) and one 4-D box of V (both d halves) into
-//               a 2-slot K/V ring;
+//               a 3-slot K/V ring (a staged request: one 32 KB box per tile);
 //   warp 1      tensor-memory allocator and single-thread MMA issuer:
 //               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
 //               O += P V with P read from tensor memory (M128 N128 K16 x 8);
-//   warp 2      bias producer: per bias tile one fp32 TMA box of rel_logits per
-//               8 tokens (fewer when shared memory is short; out-of-range
-//               distances read as 0) into a 2-slot ring;
+//   warp 2      bias producer: per bias tile and key half one fp32 TMA box of
+//               rel_logits per 8 tokens (fewer when shared memory is short;
+//               out-of-range distances read as 0) into a 3-stage ring of half
+//               tiles, each stage read by one softmax warpgroup;
 //   warps 4-11  online softmax in two warpgroups: warps 4-7 take keys 0-63 of
 //               every S tile, warps 8-11 keys 64-127 (thread = TMEM lane = row);
 //               each adds its half of the relative bias from the staged boxes
@@ -36,9 +37,9 @@ constexpr int kPfProducerRegs = 80;         // warpgroup 0 (warps 0-3) after set
 constexpr int kPfSoftmaxRegs = 208;        // warpgroups 1 and 2 (softmax) after setmaxnreg.inc
 static_assert(128 * kPfProducerRegs + 256 * kPfSoftmaxRegs <= kPfThreads * kPfLaunchRegs,
               "register split exceeds the launch allocation");
-constexpr int kKvSlots = 2;
+constexpr int kKvSlots = kPfKvSlots;
 constexpr int kSSlots = 2;
-constexpr int kBiasSlots = 2;
+constexpr int kBiasSlots = kPfBiasSlots;      // half-tile bias stages
 constexpr int kSlotBytes = 32768;           // one K or V tile: 2 d halves x 128 rows x 128 B
 constexpr int kRescaleThreshold = 8;        // log2 units (factor 256)
 constexpr uint32_t kTmemCols = 512;         // S ring 2 x 128 | O 128 | Q 64 (bf16 pairs)
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int s = 0; s < kBiasSlots; ++s) {
             mbar_init(&sh.bias_full[s], 1);
-            mbar_init(&sh.bias_empty[s], kSoftmaxWarps);
+            mbar_init(&sh.bias_empty[s], kSoftmaxWarps / 2);
         }
         mbar_init(&sh.q_full, kSoftmaxWarps);
         for (int s = 0; s < kSSlots; ++s) {
@@ -372,24 +373,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int idx = pf_item_index(r);
                 if (idx >= total || *abort) break;
                 const PfItem it = pf_item(p, p.pf_items[idx]);
-                for (int n = 0; n < it.ntiles; ++n) {
+                bool stop = false;
+                for (int n = 0; n < it.ntiles && !stop; ++n) {
                     if (!pf_tile_bias(p, it, n)) continue;
-                    const int bs = bseq % kBiasSlots;
-                    if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) break;
-                    const int j0 = pf_tile_key0(it, n);
                     const int nbox = (it.ntok + bias_nb - 1) >> p.bias_tok_log2;
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)(nbox * pf_bias_box_bytes(p.G, bias_nb)));
-                    __syncwarp();
-                    for (int b = lane; b < nbox; b += 32) {
-                        const int k0 = b << p.bias_tok_log2;
-                        // distance span of token k0: from q_abs - (j0 + 127) up; rounded down to 16 bytes
-                        const int x0 = (it.qa_min + k0 - j0 - (kTileKeys - 1)) & ~3;
-                        tma_load_3d_hint(bias_smem + bs * bias_stage + b * bias_box, &tm_bias, x0, it.g * p.G,
-                                         it.t0 + it.i0 + k0, &sh.bias_full[bs], pol_bias);
+                    // keys 64h .. 64h + 63 of the tile, read by softmax warpgroup h
+                    for (int h = 0; h < 2; ++h) {
+                        const int bs = bseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) {
+                            stop = true;
+                            break;
+                        }
+                        const int j0 = pf_tile_key0(it, n) + 64 * h;
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&sh.bias_full[bs], (uint32_t)(nbox * pf_bias_box_bytes(p.G, bias_nb)));
+                        __syncwarp();
+                        for (int b = lane; b < nbox; b += 32) {
+                            const int k0 = b << p.bias_tok_log2;
+                            // distance span of token k0: from q_abs - (j0 + 63) up; rounded down to 16 bytes
+                            const int x0 = (it.qa_min + k0 - j0 - 63) & ~3;
+                            tma_load_3d_hint(bias_smem + bs * bias_stage + b * bias_box, &tm_bias, x0, it.g * p.G,
+                                             it.t0 + it.i0 + k0, &sh.bias_full[bs], pol_bias);
+                        }
+                        __syncwarp();
+                        ++bseq;
                     }
-                    __syncwarp();
-                    ++bseq;
                 }
                 if (*abort) break;
             }
@@ -602,8 +610,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int kb = k >> p.bias_tok_log2, ki = k & (bias_nb - 1);
             const int ko = (qa - (kTileKeys - 1)) - ((it.qa_min + (kb << p.bias_tok_log2) - (kTileKeys - 1)) & ~3);
             const int bo = ko & 3;
-            const uint32_t box_row = smem_u32(bias_smem) + kb * bias_box +
-                                     ((ki * p.G + j) * bias_w + 4 * (ko >> 2) + 64 * (1 - h)) * 4;
+            const uint32_t box_row = smem_u32(bias_smem) + kb * bias_box + ((ki * p.G + j) * bias_w + 4 * (ko >> 2)) * 4;
             const float *rel_row = p.rel ? p.rel + ((size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j) * p.E : nullptr;
             float m_used = -INFINITY;  // raw-score units
             float l = 0.f;             // this half's share of the row sum
@@ -621,8 +628,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_wait_ld();
                 if (pf_tile_bias(p, it, n)) {
                     if (p.bias_tma) {
-                        const int bs = bseq % kBiasSlots;
-                        if (!mbar_wait_warp(&sh.bias_full[bs], (bseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
+                        // the tile's two half stages are bias sequence numbers 2 bseq (keys 0-63) and 2 bseq + 1
+                        const uint32_t hseq = 2 * bseq + h;
+                        const int bs = hseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_full[bs], (hseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
                         if (row_ok) {
                             const uint32_t box = box_row + bs * bias_stage;
                             switch (bo) {
