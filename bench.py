@@ -32,6 +32,7 @@ METRIC = "paged rel-bias attn: decode KV-read GB/s & prefill TFLOP/s (% of roofl
 HEADLINE = "decode_batch"
 SECONDARY = ["chunked_prefill", "long_decode", "continuous_batch"]
 FP8_SCALES = (0.0625, 0.05)  # k_scale, v_scale of the E4M3 caches the bench builds
+TIMED_KERNELS = ("prepass", "stage", "decode", "prefill", "combine")
 D = 128
 
 
@@ -78,19 +79,16 @@ def prefill_keys(case):
     return sum(lk for lq, lk in zip(case.q_lens, case.kv_lens) if lq * G > 16)
 
 
-def total_bytes(case):
-    """Compulsory HBM bytes of one step (reported beside the algorithmic headline)."""
+def total_bytes(case, fp8=False):
+    """Compulsory HBM bytes of one step: q in and out, the decode rows' visible K/V, every key of the prefill
+    requests' K/V once, and the rel_logits band each row reads (E4M3 caches: one byte per K/V element)."""
     kv, _, _ = work_of(case)
-    G = case.H // case.Hkv
+    el = 1 if fp8 else 2
     b = case.q.numel() * 2 * 2  # q in, out
-    pre_keys = 0
-    for lq, lk in zip(case.q_lens, case.kv_lens):
-        if lq * G > 16:
-            pre_keys += lk
-    b += pre_keys * case.Hkv * D * 2 * 2
+    b += prefill_keys(case) * case.Hkv * D * 2 * el
     if case.E > 0:
         b += _bias_bytes(case)
-    return kv + b
+    return kv * el // 2 + b
 
 
 def _bias_bytes(case):
@@ -336,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
                   rel_logits=rel_logits, num_splits=splits, out=out, lse=lse)
         if case.key_cache.dtype == torch.uint8:
             return ink.ink_rel_attn_varlen_fp8kv(q, case.key_cache, case.value_cache, k_scale=FP8_SCALES[0],
-                                                 v_scale=FP8_SCALES[1], **kw)
+                                                 v_scale=FP8_SCALES[1], stage_kv_tokens=prefill_keys(case), **kw)
         return ink.ink_rel_attn_varlen(q, case.key_cache, case.value_cache, stage_kv_tokens=prefill_keys(case),
                                        **kw)
 
@@ -358,32 +356,45 @@ def run_ours(args, rank, world, local_rank):
         flags = ink.read_device_errors()
         if flags & ~ink.DEVERR["EMPTY_ROWS"]:
             raise RuntimeError(f"{name}: device error flags {flags:#x}")
-        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        # every kernel of the step is bracketed by its own pair of events on the launching stream (the
+        # library's measurement hooks; this loop is the only thread calling it)
+        kev = {kn: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(steps)] for kn in TIMED_KERNELS}
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for a, b in kev:  # torch creates the CUDA events on first record; the library needs real handles
-            a.record(stream)
-            b.record(stream)
+        for pairs_ in kev.values():  # torch creates the CUDA events on first record; the library needs real handles
+            for a, b in pairs_:  # stop before start: a kernel the step does not launch reads as a negative time
+                b.record(stream)
+                a.record(stream)
+        torch.cuda.synchronize(dev)
         n0 = ink.launch_count()
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(local_rank) as clk:
             start.record(stream)
             for k in range(steps):
-                ink.set_timing_events(main_kernel, kev[k][0], kev[k][1])
+                for kn in TIMED_KERNELS:
+                    ink.set_timing_events(kn, kev[kn][k][0], kev[kn][k][1])
                 call(case, out, lse)
             end.record(stream)
             torch.cuda.synchronize(dev)
-        ink.set_timing_events(main_kernel, None, None)
+        for kn in TIMED_KERNELS:
+            ink.set_timing_events(kn, None, None)
         barrier()
         launches = ink.launch_count() - n0
         ms = start.elapsed_time(end) / steps
-        kms = sum(a.elapsed_time(b) for a, b in kev) / steps
+
+        def kernel_ms(kn):
+            t = [a.elapsed_time(b) for a, b in kev[kn]]
+            return sum(t) / steps if all(x > 0 for x in t) else 0.0
+
+        per_kernel = {kn: kernel_ms(kn) for kn in TIMED_KERNELS}
         ms_max = max_over_ranks(ms, dev)
         kv, flops, pairs = work_of(case)
         if fp8:
             kv //= 2  # one byte per K / V element
-        res = {"workload": name, "desc": WORKLOADS[name], "ms_per_step": ms_max, "kernel_ms": kms,
-               "kv_bytes": kv, "flops": flops, "launches": launches, "clocks": clk.summary()}
+        res = {"workload": name, "desc": WORKLOADS[name], "ms_per_step": ms_max, "kernel_ms": per_kernel[main_kernel],
+               "per_kernel_ms": per_kernel, "kv_bytes": kv, "flops": flops, "launches": launches,
+               "clocks": clk.summary(), "compulsory_bytes": total_bytes(case, fp8)}
         # end-to-end through the public API with host buffers: every step uploads its inputs from pinned
         # host memory and reads its out/lse back; step k + 1's upload runs while step k computes, and
         # the host waits for each step's result one step later (double-buffered on both sides)
@@ -606,74 +617,77 @@ def run_ours(args, rank, world, local_rank):
     steps, warmup = args.steps, args.warmup
     headline = args.workload
     head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
-    if args.kv_fp8 and head_kernel != "decode":
-        raise SystemExit("--kv-fp8 applies to decode-shaped workloads only")
     head = measure(headline, steps, warmup, head_kernel, fp8=args.kv_fp8)
     sec = {}
+    skip = {x for x in args.skip.split(",") if x}
     if not args.headline_only:
-        skip = {x for x in args.skip.split(",") if x}
-        for name in [HEADLINE] + SECONDARY:
-            if name == headline or name in skip:
+        s2, w2 = max(3, steps // 2), max(3, warmup)
+        jobs = [
+            ("kv_append", lambda: measure_append(s2, w2)),
+            ("kv_append_fp8", lambda: measure_append(s2, w2, fp8=True)),
+            ("graph_decode", lambda: measure_graph(max(50, steps * 10), max(5, warmup))),
+            ("long_decode_splits", lambda: measure_split_sweep(max(5, steps // 2), w2)),
+            ("decode_batch_fp8", lambda: measure("decode_batch", s2, w2, "decode", fp8=True)),
+            ("long_decode", lambda: measure("long_decode", s2, w2, "decode")),
+            ("decode_batch", lambda: measure("decode_batch", s2, w2, "decode")),
+            ("continuous_batch", lambda: measure("continuous_batch", s2, w2, "prefill")),
+            ("chunked_prefill_fp8", lambda: measure("chunked_prefill", s2, w2, "prefill", fp8=True)),
+            ("chunked_prefill", lambda: measure("chunked_prefill", s2, w2, "prefill")),
+        ]
+        for name, fn in jobs:  # this order is also the order of the "workloads" object: the prefill last
+            if name in skip or name == headline + ("_fp8" if args.kv_fp8 else ""):
                 continue
-            kern = "prefill" if name == "chunked_prefill" else "decode"
             try:
-                sec[name] = measure(name, max(3, steps // 2), max(3, warmup), kern)
+                sec[name] = fn()
             except Exception as exc:  # report, keep the headline line
                 sec[name] = {"error": f"{type(exc).__name__}: {exc}"}
-        if "kv_append" not in skip:
-            try:
-                sec["kv_append"] = measure_append(max(3, steps // 2), max(3, warmup))
-            except Exception as exc:
-                sec["kv_append"] = {"error": f"{type(exc).__name__}: {exc}"}
-        if "decode_batch_fp8" not in skip:
-            try:
-                sec["decode_batch_fp8"] = measure("decode_batch", max(3, steps // 2), max(3, warmup), "decode",
-                                                  fp8=True)
-            except Exception as exc:
-                sec["decode_batch_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
-        if "kv_append_fp8" not in skip:
-            try:
-                sec["kv_append_fp8"] = measure_append(max(3, steps // 2), max(3, warmup), fp8=True)
-            except Exception as exc:
-                sec["kv_append_fp8"] = {"error": f"{type(exc).__name__}: {exc}"}
-        if "long_decode_splits" not in skip:
-            try:
-                sec["long_decode_splits"] = measure_split_sweep(max(5, steps // 2), max(3, warmup))
-            except Exception as exc:
-                sec["long_decode_splits"] = {"error": f"{type(exc).__name__}: {exc}"}
-        if "graph_decode" not in skip:
-            try:
-                sec["graph_decode"] = measure_graph(max(50, steps * 10), max(5, warmup))
-            except Exception as exc:
-                sec["graph_decode"] = {"error": f"{type(exc).__name__}: {exc}"}
 
-    def roof_decode(r, name):
-        bytes_ = r["kv_bytes"]
-        ach = bytes_ / (r["kernel_ms"] * 1e-3) / 1e9
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9
+
+    def tfs(flops, ms):
+        return flops / (ms * 1e-3) / 1e12
+
+    def roof_decode(r, name, fp8=False):
+        ach = gbs(r["kv_bytes"], r["kernel_ms"])
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic_of("ink_decode_kernel", name),
-                "peak_source": peaks["source"], "kernel": "ink_decode_kernel"}
+                "frac": round(ach / peaks["hbm_gbs"], 4), "frac_of_8000": round(ach / 8000.0, 4),
+                "traffic": traffic_of("ink_decode_kernel", name),
+                "peak_source": peaks["source"], "kernel": "ink_decode_kernel" + (" (E4M3 cache)" if fp8 else "")}
 
-    def roof_prefill(r, name):
-        ach = r["flops"] / (r["kernel_ms"] * 1e-3) / 1e12
+    def roof_prefill(r, name, fp8=False):
+        ach = tfs(r["flops"], r["kernel_ms"])
         return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic_of("ink_prefill_kernel", name),
-                "peak_source": peaks["source"], "kernel": "ink_prefill_kernel"}
+                "peak_source": peaks["source"], "kernel": "ink_prefill_kernel" + (" (E4M3 cache, staged)" if fp8 else "")}
+
+    def step_bound(r):
+        """The step's own floor: its flops at the tensor peak or its compulsory bytes at the HBM peak."""
+        t = max(r["flops"] / (peaks["bf16_tflops"] * 1e12), r["compulsory_bytes"] / (peaks["hbm_gbs"] * 1e9))
+        return {"bound_ms": round(t * 1e3, 4), "frac": round(t * 1e3 / r["ms_per_step"], 4),
+                "compulsory_bytes": r["compulsory_bytes"], "flops": r["flops"]}
+
+    def kernels_of(r):
+        return {k: round(v, 4) for k, v in r["per_kernel_ms"].items() if v > 0}
+
+    def clk_of(r):
+        c = r["clocks"]
+        return {"sm_mhz": c["sm_mhz"], "sm_max_mhz": c["sm_max_mhz"], "reasons": c["reasons"]}
 
     if rank != 0:
         return
+    fp8_head = args.kv_fp8
     if headline.startswith("chunked_prefill"):
         unit = "TFLOP/s"
         value = job_throughput(head["flops"], world, head["ms_per_step"]) / 1e12
         e2e = job_throughput(head["flops"], world, head["e2e_ms"]) / 1e12
-        roof = roof_prefill(head, headline)
+        roof = roof_prefill(head, headline + ("_fp8" if fp8_head else ""), fp8_head)
     else:
         unit = "GB/s"
         value = job_throughput(head["kv_bytes"], world, head["ms_per_step"]) / 1e9
         e2e = job_throughput(head["kv_bytes"], world, head["e2e_ms"]) / 1e9
-        roof = roof_decode(head, headline + ("_fp8" if args.kv_fp8 else ""))
-        if args.kv_fp8:
-            roof["kernel"] = "ink_decode_kernel (E4M3 cache)"
+        roof = roof_decode(head, headline + ("_fp8" if fp8_head else ""), fp8_head)
+    cpu_secs = args.cpu_seconds_each
     workloads_out = {}
     for name, r in sec.items():
         if "error" in r:
@@ -681,65 +695,62 @@ def run_ours(args, rank, world, local_rank):
             continue
         if name in ("kv_append", "kv_append_fp8"):
             fp8 = name == "kv_append_fp8"
-            ach = r["bytes"] / (r["kernel_ms"] * 1e-3) / 1e9
+            ach = gbs(r["bytes"], r["kernel_ms"])
             kern = "ink_append_fp8_kernel" if fp8 else "ink_append_kernel"
             workloads_out[name] = {
                 "metric": "KV append GB/s (K and V read and written)", "ms_per_step": round(r["ms_per_step"], 4),
-                "value": round(r["bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages" + (", quantized into an E4M3 cache" if fp8 else ""),
-                "gpu_launches": r["launches"], "clocks": r["clocks"],
+                "value": round(gbs(r["bytes"], r["ms_per_step"]), 1), "unit": "GB/s",
+                "desc": "4 x 8192 new tokens, Hkv 8, 16-key pages" + (", into an E4M3 cache" if fp8 else ""),
+                "gpu_launches": r["launches"], "clocks": clk_of(r),
                 "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic_of(kern, name),
                              "peak_source": peaks["source"], "kernel": kern}}
             continue
-        if name == "decode_batch_fp8":
-            rf = roof_decode(r, name)  # traffic from the E4M3 capture, kept under this name
-            rf["kernel"] = "ink_decode_kernel (E4M3 cache)"
-            workloads_out[name] = {
-                "metric": "decode KV-read GB/s (E4M3 cache bytes)", "ms_per_step": round(r["ms_per_step"], 4),
-                "e2e_ms": round(r["e2e_ms"], 4), "value": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
-                "unit": "GB/s", "desc": WORKLOADS["decode_batch"] + "; KV cache in E4M3 (1 byte per element)",
-                "gpu_launches": r["launches"], "clocks": r["clocks"], "roofline": rf}
-            continue
         if name == "long_decode_splits":
             workloads_out[name] = {"metric": "long decode KV-read GB/s by split count (step, and decode kernel)",
-                                   "desc": WORKLOADS["long_decode"], "unit": "GB/s", **r}
+                                   "unit": "GB/s", **r}
             continue
         if name == "graph_decode":
             workloads_out[name] = {
                 "metric": "decode step time, direct API call vs CUDA graph replay (ms)",
                 "desc": "8 decodes, Lk 4096, H 32, Hkv 8, E 1024 (KV 134 MB, not flushed)",
                 "eager_ms": round(r["eager_ms"], 4), "graph_ms": round(r["graph_ms"], 4),
-                "graph_speedup": round(r["eager_ms"] / r["graph_ms"], 3),
-                "graph_kv_gbs": round(r["kv_bytes"] / (r["graph_ms"] * 1e-3) / 1e9, 1),
-                "gpu_launches_per_step": r["launches_per_step"], "clocks": r["clocks"]}
+                "graph_kv_gbs": round(gbs(r["kv_bytes"], r["graph_ms"]), 1),
+                "gpu_launches_per_step": r["launches_per_step"], "clocks": clk_of(r)}
             continue
-        entry = {"ms_per_step": round(r["ms_per_step"], 4), "e2e_ms": round(r["e2e_ms"], 4),
-                 "gpu_launches": r["launches"], "clocks": r["clocks"]}
-        if name == "chunked_prefill":
-            entry.update({"metric": "prefill TFLOP/s (visible pairs)",
-                          "value": round(r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                          "roofline": roof_prefill(r, name)})
-        elif name == "long_decode":
-            entry.update({"metric": "decode KV-read GB/s", "value": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
-                          "unit": "GB/s", "roofline": roof_decode(r, name)})
+        fp8 = name.endswith("_fp8")
+        base = name[:-4] if fp8 else name
+        entry = {"ms_per_step": round(r["ms_per_step"], 4), "kernel_ms": kernels_of(r),
+                 "e2e_ms": round(r["e2e_ms"], 4), "gpu_launches": r["launches"], "clocks": clk_of(r)}
+        if base == "chunked_prefill":
+            entry.update({"metric": "prefill TFLOP/s (visible pairs)", "value": round(tfs(r["flops"], r["ms_per_step"]), 2),
+                          "unit": "TFLOP/s", "roofline": roof_prefill(r, name, fp8), "step_roofline": step_bound(r)})
+        elif base == "continuous_batch":
+            entry.update({"metric": "decode KV-read GB/s + prefill TFLOP/s over the step",
+                          "decode_gbs": round(gbs(r["kv_bytes"], r["ms_per_step"]), 1),
+                          "prefill_tflops": round(tfs(r["flops"], r["ms_per_step"]), 2),
+                          "step_roofline": step_bound(r),
+                          "roofline": roof_prefill(r, name),
+                          "roofline_decode": roof_decode({**r, "kernel_ms": r["per_kernel_ms"]["decode"]}, name)})
         else:
-            entry.update({"metric": "decode KV-read GB/s + prefill TFLOP/s",
-                          "decode_gbs": round(r["kv_bytes"] / (r["ms_per_step"] * 1e-3) / 1e9, 1),
-                          "prefill_tflops": round(r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12, 2),
-                          "roofline_time_frac": round(max(r["kv_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                                                          r["flops"] / (peaks["bf16_tflops"] * 1e12))
-                                                      / (r["ms_per_step"] * 1e-3), 4)})
+            entry.update({"metric": "decode KV-read GB/s" + (" (E4M3 cache bytes)" if fp8 else ""),
+                          "value": round(gbs(r["kv_bytes"], r["ms_per_step"]), 1), "unit": "GB/s",
+                          "roofline": roof_decode(r, name, fp8)})
+        if not args.no_cpu_baseline:
+            try:
+                entry["cpu_baseline"] = cpu_baseline(base, cpu_secs, fp8=fp8, short=True)
+            except Exception as exc:
+                entry["cpu_baseline"] = {"error": f"{type(exc).__name__}: {exc}"}
         workloads_out[name] = entry
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(headline, args.cpu_seconds)
+        cpu = cpu_baseline(headline, args.cpu_seconds, fp8=fp8_head)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(head["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads/)",
         "config": {"workload": headline, "desc": WORKLOADS[headline], "parallelism": f"replicas x{world}",
-                   "kv_cache": "e4m3" if args.kv_fp8 else "bf16",
+                   "kv_cache": "e4m3" if fp8_head else "bf16",
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": roof,
         "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": head["h2d_bytes"],
@@ -748,6 +759,7 @@ def run_ours(args, rank, world, local_rank):
                         "every step (the next step's upload overlaps this step's compute); the paged KV cache is "
                         "resident state in HBM"},
         "gpu_launches": head["launches"],
+        "kernel_ms": kernels_of(head),
         "clocks": head["clocks"],
         "cpu_baseline": cpu,
         "workloads": workloads_out,
@@ -757,49 +769,82 @@ def run_ours(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------------------------- oracle arm
 
-def cpu_baseline(name, seconds):
-    """The fp64 oracle, as it stands, on the host cores over a bounded sample of the workload:
-    whole requests (all heads) in order, pass after pass over the batch, until about `seconds` of CPU work;
-    returns the same metric."""
+def _row_pairs(case, lq, lk, i):
+    """Visible keys of query row i of a request with lq queries and lk keys."""
+    qa = i + lk - lq
+    lo = max(0, qa - case.window_left) if case.window_left >= 0 else 0
+    hi = lk - 1
+    if case.causal:
+        hi = min(hi, qa)
+    if case.window_right >= 0:
+        hi = min(hi, qa + case.window_right)
+    return max(0, hi - lo + 1)
+
+
+def cpu_baseline(name, seconds, fp8=False, short=False, case=None):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample of the workload (about
+    `seconds` of CPU work), in the GPU line's own units.
+
+    Decode-shaped requests: whole requests (all heads), in order, pass after pass -> KV GB/s.
+    Prefill-shaped requests: stratified rows -- batches of 64 (token, head) rows drawn uniformly from each
+    prefill request in turn (seeded) -> TFLOP/s on the rows' visible pairs.  A mix gets half the time for
+    each and also reports the step time those two rates imply.  fp8: the same workload over the E4M3
+    cache the GPU line reads, through the oracle's FP8 entry.  `case`: the workload already built on the
+    host (the reference arm times several samples of one build)."""
     import numpy as np
 
     import oracle
-    from workloads import workload
+    from workloads import fp8_kv, workload
 
-    case = workload(name, device="cpu")
+    if case is None:
+        case = workload(name, device="cpu")
     oracle.build()
     threads = oracle.threads()
     kw = case.oracle_kwargs()
     G = case.H // case.Hkv
-    done_bytes = 0
-    done_flops = 0
-    reqs = 0
-    t0 = time.perf_counter()
+    kc, vc = case.key_cache, case.value_cache
+    if fp8:
+        kc, vc = fp8_kv(case, *FP8_SCALES)
     cu = case.cu_seqlens_q.tolist()
-    passes = 0
-    stop = False
-    while not stop:
-        for b in range(case.B):
-            rows = np.arange(cu[b] * case.H, cu[b + 1] * case.H, dtype=np.int64)
-            if rows.size == 0:
-                continue
-            oracle.attention(case.q, case.key_cache, case.value_cache, case.block_table, case.cache_seqlens,
-                             case.cu_seqlens_q, rows=rows, **kw)
-            lq, lk = case.q_lens[b], case.kv_lens[b]
-            sub = type("S", (), {})()
-            sub.H, sub.Hkv, sub.E, sub.causal = case.H, case.Hkv, case.E, case.causal
-            sub.window_left, sub.window_right = case.window_left, case.window_right
-            sub.q_lens, sub.kv_lens = [lq], [lk]
-            kvb, fl, _ = work_of(sub)
-            done_bytes += kvb
-            done_flops += fl
-            reqs += 1
-            if time.perf_counter() - t0 > seconds:
-                stop = True
-                break
+    dec = [b for b in range(case.B) if case.q_lens[b] * G <= 16 and case.q_lens[b] > 0]
+    pre = [b for b in range(case.B) if case.q_lens[b] * G > 16]
+
+    def run(rows):
+        if fp8:
+            oracle.attention_fp8kv(case.q, kc, vc, case.block_table, case.cache_seqlens, case.cu_seqlens_q,
+                                   k_scale=FP8_SCALES[0], v_scale=FP8_SCALES[1], rows=rows, **kw)
         else:
-            passes += 1
-    dt = time.perf_counter() - t0
+            oracle.attention(case.q, kc, vc, case.block_table, case.cache_seqlens, case.cu_seqlens_q, rows=rows, **kw)
+
+    budget = seconds / (2 if dec and pre else 1)
+    el = 1 if fp8 else 2
+    dec_bytes, dec_s, dec_reqs = 0, 0.0, 0
+    if dec:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget:
+            for b in dec:
+                run(np.arange(cu[b] * case.H, cu[b + 1] * case.H, dtype=np.int64))
+                lq, lk = case.q_lens[b], case.kv_lens[b]
+                keys = max(_row_pairs(case, lq, lk, i) for i in range(lq))  # the union of the rows' ranges
+                dec_bytes += keys * case.Hkv * D * 2 * el
+                dec_reqs += 1
+                if time.perf_counter() - t0 >= budget:
+                    break
+        dec_s = time.perf_counter() - t0
+    pre_flops, pre_s, pre_rows = 0, 0.0, 0
+    if pre:
+        g = np.random.default_rng(17)
+        t0 = time.perf_counter()
+        k = 0
+        while time.perf_counter() - t0 < budget:
+            b = pre[k % len(pre)]
+            k += 1
+            lq, lk = case.q_lens[b], case.kv_lens[b]
+            rows = np.unique(g.integers(cu[b] * case.H, cu[b + 1] * case.H, size=64)).astype(np.int64)
+            run(rows)
+            pre_flops += sum(4 * D * _row_pairs(case, lq, lk, int(r) // case.H - cu[b]) for r in rows)
+            pre_rows += rows.size
+        pre_s = time.perf_counter() - t0
     cpu_name = ""
     try:
         with open("/proc/cpuinfo") as f:
@@ -809,13 +854,28 @@ def cpu_baseline(name, seconds):
                     break
     except Exception:
         pass
-    if name.startswith("chunked_prefill"):
-        value, unit = done_flops / dt / 1e12, "TFLOP/s"
+    res = {"kind": "oracle", "cores": threads}
+    parts = []
+    if dec:
+        parts.append(f"{dec_reqs} whole decode requests ({dec_s:.1f} s)")
+    if pre:
+        parts.append(f"{pre_rows} stratified prefill rows ({pre_s:.1f} s)")
+    res["sample"] = f"{name}{' (E4M3 cache)' if fp8 else ''}: " + ", ".join(parts)
+    dec_rate = dec_bytes / dec_s if dec_s > 0 else 0.0
+    pre_rate = pre_flops / pre_s if pre_s > 0 else 0.0
+    if dec and pre:
+        kv, flops, _ = work_of(case)
+        step_s = kv * el / 2 / dec_rate + flops / pre_rate
+        res.update({"value": round(step_s * 1e3, 3), "unit": "ms per step (extrapolated)",
+                    "decode_gbs": round(dec_rate / 1e9, 6), "prefill_tflops": round(pre_rate / 1e12, 6)})
+    elif pre:
+        res.update({"value": round(pre_rate / 1e12, 6), "unit": "TFLOP/s"})
     else:
-        value, unit = done_bytes / dt / 1e9, "GB/s"
-    return {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
-            "sample": f"{reqs} requests of {name} ({passes} full passes over its {case.B}; all heads), {dt:.1f} s",
-            "seconds": round(dt, 2), "cpu": cpu_name}
+        res.update({"value": round(dec_rate / 1e9, 6), "unit": "GB/s"})
+    if not short:
+        res["seconds"] = round(dec_s + pre_s, 2)
+        res["cpu"] = cpu_name
+    return res
 
 
 def run_reference(args, rank, world):
@@ -823,11 +883,14 @@ def run_reference(args, rank, world):
         return
     from workloads import PROFILE_WORKLOADS, WORKLOADS  # noqa: F401
 
+    from workloads import workload
+
     WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+    case = workload(args.workload, device="cpu")
     times = []
     val = None
     for k in range(args.warmup + args.steps):
-        r = cpu_baseline(args.workload, args.cpu_seconds / max(1, args.steps))
+        r = cpu_baseline(args.workload, args.cpu_seconds / max(1, args.steps), fp8=args.kv_fp8, case=case)
         if k >= args.warmup:
             times.append(r)
     vals = [r["value"] for r in times]
@@ -835,9 +898,11 @@ def run_reference(args, rank, world):
     last = times[-1]
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": last["unit"], "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": not last["unit"].startswith("ms"),
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads/)",
-        "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "parallelism": "host cores"},
+        "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "parallelism": "host cores",
+                   "kv_cache": "e4m3" if args.kv_fp8 else "bf16"},
         "cpu_baseline": {"value": val, "unit": last["unit"], "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": val, "unit": last["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -858,10 +923,12 @@ def main():
                              "decode_batch_quarter", "chunked_prefill_quarter"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--kv-fp8", action="store_true",
-                    help="run the (decode-shaped) headline workload over an E4M3 copy of its KV cache")
+                    help="run the headline workload over an E4M3 copy of its KV cache")
     ap.add_argument("--skip", default="", help="comma-separated secondary workloads to leave out")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle time for the headline's cpu_baseline")
+    ap.add_argument("--cpu-seconds-each", type=float, default=6.0,
+                    help="oracle time for each other workload's cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

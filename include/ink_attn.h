@@ -93,6 +93,7 @@ typedef enum {
 #define INK_DEVERR_EMPTY_ROWS 0x10u /* informational: some rows saw no key (out 0, lse -inf), e.g. causal with Lk < Lq */
 #define INK_DEVERR_TIMEOUT    0x100u /* a bounded pipeline wait gave up; outputs of the call are undefined */
 #define INK_DEVERR_SMEM       0x200u /* a kernel found less shared memory than its layout needs and did nothing */
+#define INK_DEVERR_STAGE      0x400u /* an FP8-cache prefill-shaped request found no room in the K/V staging area: it was skipped */
 
 /*
  * Bytes of device workspace one call needs.  `num_splits` as in
@@ -180,7 +181,7 @@ INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
                                ink_stream_t stream);
 
 /*
- * The same attention over an FP8 KV cache (decode path).  The FP8 cache is
+ * The same attention over an FP8 KV cache.  The FP8 cache is
  * the TurboQuant backend's (vLLM V1 attention page, section 12.1: an FP8
  * cache dequantized when decoding), with per-tensor k_scale / v_scale applied
  * to the gathered K and V rows as paged_attention_v2_pytorch does on the
@@ -188,14 +189,19 @@ INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
  *   key_cache, value_cache  OCP FP8 E4M3 bytes, (num_blocks, block_size,
  *                 Hkv, D), contiguous, 16-byte aligned; the values attended
  *                 over are k_scale * E4M3(byte) and v_scale * E4M3(byte).
- *   k_scale, v_scale  finite and > 0, else INK_ERR_INVALID_ARG.
- * Decode-shaped calls only: max_seqlen_q * (H / Hkv) <= 16 and Hkv in
- * {1, 2, 4, 8}; any other call returns INK_ERR_UNSUPPORTED before anything
- * is launched.  The products run in fp16 with fp32 accumulation: every E4M3
- * value is exact in fp16, and q is converted from bf16 to fp16 (exact for
- * magnitudes in [2^-14, 65504]; smaller ones lose bits, larger ones
- * overflow).  All other arguments, the workspace (same size query), results
- * and errors are those of ink_rel_attn_varlen.
+ *   k_scale, v_scale  in [2^-126, 2^126] (normal, with a normal reciprocal),
+ *                 else INK_ERR_INVALID_ARG.
+ * Decode-shaped requests (max_seqlen_q * (H / Hkv) <= 16 with Hkv in
+ * {1, 2, 4, 8}) run in the decode kernel: the products run in fp16 with fp32
+ * accumulation (every E4M3 value is exact in fp16; q is converted from bf16 to
+ * fp16, exact for magnitudes in [2^-14, 65504]).  Prefill-shaped requests are
+ * read from the K/V staging area (ink_rel_attn_stage_bytes), into which each
+ * call copies their pages converted to bf16 (exact for every E4M3 value); the
+ * prefill then multiplies bf16 q with them, k_scale joining the softmax scale
+ * and v_scale the output.  A call with prefill-shaped requests needs staging
+ * room: none at all returns INK_ERR_WORKSPACE, and a request that does not fit
+ * raises INK_DEVERR_STAGE and is skipped.  All other arguments, results and
+ * errors are those of ink_rel_attn_varlen.
  */
 INK_API ink_status ink_rel_attn_varlen_fp8kv(const ink_attn_dims *dims,
                                              const void *q, const void *key_cache, const void *value_cache,
@@ -280,7 +286,8 @@ INK_API ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *
  *   key, value  device, bf16 (num_tokens, num_kv_heads, 128), 16-byte aligned.
  *   key_cache, value_cache  device, E4M3 bytes (num_blocks, block_size,
  *               num_kv_heads, 128), 16-byte aligned.
- *   k_scale, v_scale  finite and > 0, else INK_ERR_INVALID_ARG.
+ *   k_scale, v_scale  in [2^-126, 2^126] (normal, with a normal reciprocal),
+ *                 else INK_ERR_INVALID_ARG.
  * Other errors as ink_reshape_and_cache.
  */
 INK_API ink_status ink_reshape_and_cache_fp8(const ink_attn_dims *dims, const void *key, const void *value,
@@ -304,7 +311,13 @@ INK_API int32_t ink_attn_version(void);
  * Measurement hooks (no effect on results).
  * ink_set_timing_events: while set, every call records `start_event` on its
  * stream just before launching the named kernel and `stop_event` just after
- * it (both cudaEvent_t, owned by the caller; NULL clears the hook).
+ * it (both cudaEvent_t, owned by the caller; NULL clears the hook).  The hooks
+ * are process-wide, one per kernel id, and are the only state the library keeps
+ * between calls besides the launch counter: they are for single-threaded
+ * measurement -- set them, make calls from one host thread on one stream, clear
+ * them -- because a call from any other thread or stream made meanwhile records
+ * into the same events.  Setting or clearing a hook while another thread is
+ * inside a call is a data race.
  * ink_launch_count: number of kernels this library has launched in the
  * process so far.
  */

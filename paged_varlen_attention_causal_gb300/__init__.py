@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "libinkattn.so")
 
 DEVERR = {
     "PAGE_ID": 0x01, "CU_SEQLENS": 0x02, "SEQLEN_Q": 0x04, "SEQLEN_K": 0x08, "EMPTY_ROWS": 0x10,
-    "TIMEOUT": 0x100, "SMEM": 0x200,
+    "TIMEOUT": 0x100, "SMEM": 0x200, "STAGE": 0x400,
 }
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "workspace too small",
            4: "CUDA error"}
@@ -254,11 +254,13 @@ def ink_rel_attn_varlen_fp8kv(q, key_cache, value_cache, *, k_scale: float, v_sc
                               cache_seqlens, cu_seqlens_q, max_seqlen_q: int, softmax_scale: float,
                               causal: bool = True, window_left: int = -1, window_right: int = -1,
                               rel_extent: int = 0, rel_logits=None, num_splits: int = 0, out=None, lse=None,
-                              return_lse: bool = False, workspace=None, stream=None):
-    """``ink_rel_attn_varlen`` over an FP8 KV cache (decode-shaped calls; see include/ink_attn.h).
+                              return_lse: bool = False, workspace=None, stream=None, stage_kv_tokens: int = 0):
+    """``ink_rel_attn_varlen`` over an FP8 KV cache (see include/ink_attn.h).
 
     key_cache / value_cache: E4M3 bytes as uint8 (or float8_e4m3fn) tensors of shape
     (num_blocks, block_size, Hkv, 128); the values attended over are k_scale * E4M3 and v_scale * E4M3.
+    Prefill-shaped requests are read from the K/V staging area: ``stage_kv_tokens`` (their cache keys,
+    summed) sizes it.
     """
     lib = load()
     if key_cache.dtype == torch.float8_e4m3fn:
@@ -267,7 +269,7 @@ def ink_rel_attn_varlen_fp8kv(q, key_cache, value_cache, *, k_scale: float, v_sc
         value_cache = value_cache.view(torch.uint8)
     dims, rel_ptr, out, lse, workspace, stream = _prepare(
         q, key_cache, value_cache, torch.uint8, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
-        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream)
+        rel_extent, rel_logits, num_splits, out, lse, return_lse, workspace, stream, stage_kv_tokens)
     rc = lib.ink_rel_attn_varlen_fp8kv(
         ctypes.byref(dims), q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), float(k_scale),
         float(v_scale), block_table.data_ptr(), cache_seqlens.data_ptr(), cu_seqlens_q.data_ptr(),

@@ -206,6 +206,11 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// FP8 cache scales: normal fp32 numbers whose reciprocal is normal too, so that the append's
+// quotient x * (1 / scale), corrected by one remainder step, is the correctly rounded x / scale
+// (and a zero input stays zero), and the attention's scale products stay finite.
+bool fp8_scale_ok(float s) { return std::isfinite(s) && s >= 0x1p-126f && s <= 0x1p126f; }
+
 bool encode(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base, const cuuint64_t *dims,
             const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swz)
 {
@@ -319,8 +324,7 @@ ink_status ink_rel_attn_varlen_fp8kv(const ink_attn_dims *dims, const void *q, c
                                      const float *rel_logits, int32_t num_splits, void *out, float *lse,
                                      void *workspace, size_t workspace_bytes, ink_stream_t stream_handle)
 {
-    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
-        return INK_ERR_INVALID_ARG;
+    if (!fp8_scale_ok(k_scale) || !fp8_scale_ok(v_scale)) return INK_ERR_INVALID_ARG;
     return attn_impl(dims, q, key_cache, value_cache, KvFormat{1, k_scale, v_scale}, block_table, cache_seqlens,
                      cu_seqlens_q, max_seqlen_q, softmax_scale, causal, window_left, window_right, rel_extent,
                      rel_logits, num_splits, out, lse, workspace, workspace_bytes, stream_handle);
@@ -358,8 +362,6 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     Plan pl;
     if (!make_plan(dims, max_seqlen_q, num_splits, causal ? 1 : 0, window_left, window_right, sms, pl))
         return INK_ERR_UNSUPPORTED;
-    // an FP8 cache is read by the decode kernel only: every request must be decode-shaped
-    if (kv.fp8 && (!pl.decode_kernel || pl.any_prefill)) return INK_ERR_UNSUPPORTED;
     if (workspace_bytes < pl.total) return INK_ERR_WORKSPACE;
 
     const int T = dims->num_tokens, H = dims->num_heads, Hkv = dims->num_kv_heads, E = rel_extent;
@@ -399,7 +401,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const size_t extra = workspace_bytes - pl.total;
         long long cap = (long long)(extra / per_key) / kTileKeys * kTileKeys;
         cap = std::min<long long>(cap, 1ll << 24);
-        p.stage_cap = (!kv.fp8 && pl.any_prefill && cap >= kTileKeys) ? (int)cap : 0;
+        p.stage_cap = (pl.any_prefill && cap >= kTileKeys) ? (int)cap : 0;
+        // an FP8 cache reaches the prefill only through the staging copy (converted to bf16)
+        if (kv.fp8 && pl.any_prefill && p.stage_cap == 0) return INK_ERR_WORKSPACE;
         p.ks = reinterpret_cast<__nv_bfloat16 *>(ws + pl.total);
         p.vs = p.ks + (size_t)Hkv * p.stage_cap * kHeadDim;
     }
@@ -413,6 +417,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.tpt = pl.tpt;
     p.fast_pack = pl.fast_pack;
     p.bias_tok_log2 = pl.bias_tok_log2;
+    p.kv_fp8 = kv.fp8;
+    p.out_scale = 1.f;
 
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
     alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_kd, tm_vd, tm_bdec, tm_bpf;
@@ -516,6 +522,13 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     if (pl.any_prefill && pl.pf_cap > 0) {
         Params pp = p;
         pp.bias_tma = bias_pf_tma ? 1 : 0;
+        if (kv.fp8) {
+            // staged K and V hold the E4M3 values themselves: k_scale joins the softmax scale, v_scale the output
+            const float eff = softmax_scale * kv.k_scale;
+            pp.scale_log2 = eff * 1.4426950408889634f;
+            pp.inv_scale = 1.0f / eff;
+            pp.out_scale = kv.v_scale;
+        }
         // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
         const size_t layout =
             pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2);
@@ -574,8 +587,7 @@ ink_status ink_reshape_and_cache_fp8(const ink_attn_dims *dims, const void *key,
         dims->block_size < 1)
         return INK_ERR_INVALID_ARG;
     if (!key || !value || !key_cache || !value_cache || !slot_mapping) return INK_ERR_INVALID_ARG;
-    if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
-        return INK_ERR_INVALID_ARG;
+    if (!fp8_scale_ok(k_scale) || !fp8_scale_ok(v_scale)) return INK_ERR_INVALID_ARG;
     if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
         !aligned(slot_mapping, 8) || (flags && !aligned(flags, 4)))
         return INK_ERR_INVALID_ARG;

@@ -64,6 +64,8 @@ struct Params {
     int *stg_pg_off;   // (B+1) first staged page of each request in the copy's work list (prepass)
     int stage_cap;     // keys per KV head the staging area holds (0: no staging)
     __nv_bfloat16 *ks, *vs;  // staging area: (Hkv, stage_cap, D) each
+    int kv_fp8;        // the caches hold E4M3 bytes (the staging copy converts them to bf16)
+    float out_scale;   // prefill: multiplies every output row (v_scale of an FP8 cache, else 1)
     // split partials: one block per decode item, and per (prefill unit, split)
     float *part_dec_o, *part_dec_lse;  // (dec_items_cap, dec_rows, D), (dec_items_cap, dec_rows)
     int dec_rows;                      // rows per decode block: (16 / G) * H

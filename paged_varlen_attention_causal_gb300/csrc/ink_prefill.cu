@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- K/V producer
         if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
+            if (!p.kv_fp8) {  // an FP8 call has no paged maps: it reads staged tiles only
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+            }
             if (p.stage_cap > 0) {
                 prefetch_tmap(&tm_ks);
                 prefetch_tmap(&tm_vs);
@@ -737,7 +739,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float l_other;
             if (!exchange(l, l_other)) break;
             l += l_other;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.out_scale / l : 0.f;
             const float lse = l > 0.f ? (m_used * sl2 + __log2f(l)) * ln2 : -INFINITY;
             const size_t row = (size_t)(it.t0 + it.i0 + k) * p.H + it.g * p.G + j;
             const bool final_out = it.nact == 1;

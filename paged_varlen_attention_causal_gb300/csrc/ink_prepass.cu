@@ -123,60 +123,6 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     for (int i = tid; i < kCostBuckets; i += blockDim.x) bucket_count[i] = 0;
     __syncthreads();
 
-    // pass 1: per request, decode split count, prefill q-tile count and the tokens whose
-    // rows the split-KV merge must visit (all of a request's tokens once it is split); scans.
-    uint32_t my_err = 0;
-    for (int base = 0; base < p.B; base += blockDim.x) {
-        const int b = base + tid;
-        int ndec = 0, nq = 0, nc = 0;
-        if (b < p.B) {
-            Req r = load_req(p, b);
-            my_err |= r.err;
-            if (r.ok && r.Lq > 0) {
-                if (is_decode_req(p, r)) {
-                    UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
-                    ndec = u.nact;
-                    nc = ndec > 1 ? r.Lq : 0;
-                } else {
-                    nq = (r.Lq + p.tpt - 1) / p.tpt;
-                    nc = p.S_pf > 1 ? r.Lq : 0;
-                }
-                if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
-            }
-        }
-        int xd, xq, xc;
-        const int td = block_exclusive_scan(ndec, &xd, warp_sums);
-        const int tq = block_exclusive_scan(nq, &xq, warp_sums);
-        const int tcb = block_exclusive_scan(nc, &xc, warp_sums);
-        if (b < p.B) {
-            dec_off[b] = s_carry[0] + xd;
-            unit_off[b] = s_carry[1] + xq;
-            comb_off[b] = s_carry[2] + xc;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            s_carry[0] += td;
-            s_carry[1] += tq;
-            s_carry[2] += tcb;
-        }
-        __syncthreads();
-    }
-    if (tid == 0) {
-        dec_off[p.B] = s_carry[0];
-        unit_off[p.B] = s_carry[1];
-        comb_off[p.B] = s_carry[2];
-        // Requests whose token ranges overlap (a cu_seqlens_q entry that steps back between valid
-        // neighbours) can need more q tiles than T tokens allow, and the prefill partials are sized
-        // for T: such a batch is flagged and runs nothing.
-        s_overflow = s_carry[1] > p.units_cap;
-        if (s_overflow) s_err |= INK_DEVERR_CU_SEQLENS;
-        p.hdr->comb_tokens = s_overflow ? 0u : (uint32_t)s_carry[2];
-    }
-    __syncthreads();
-    if (my_err) atomicOr(&s_err, my_err);
-    __syncthreads();
-    __threadfence_block();
-
     // K/V staging: prefill-shaped requests, in request order, take whole 128-key tiles of the
     // staging area while it has room; the rest read the paged cache.  Then the page work list
     // of the copy (one entry per staged 16-key page).
@@ -216,6 +162,63 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         for (int b = tid; b < p.B; b += blockDim.x) p.stg_off[b] = -1;
     }
     __syncthreads();
+
+    // pass 1: per request, decode split count, prefill q-tile count and the tokens whose
+    // rows the split-KV merge must visit (all of a request's tokens once it is split); scans.
+    uint32_t my_err = 0;
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        const int b = base + tid;
+        int ndec = 0, nq = 0, nc = 0;
+        if (b < p.B) {
+            Req r = load_req(p, b);
+            my_err |= r.err;
+            if (r.ok && r.Lq > 0) {
+                if (is_decode_req(p, r)) {
+                    UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
+                    ndec = u.nact;
+                    nc = ndec > 1 ? r.Lq : 0;
+                } else if (p.kv_fp8 && p.stg_off[b] < 0) {
+                    // an FP8 cache is read by the prefill only through the staging copy
+                    my_err |= INK_DEVERR_STAGE;
+                } else {
+                    nq = (r.Lq + p.tpt - 1) / p.tpt;
+                    nc = p.S_pf > 1 ? r.Lq : 0;
+                }
+                if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
+            }
+        }
+        int xd, xq, xc;
+        const int td = block_exclusive_scan(ndec, &xd, warp_sums);
+        const int tq = block_exclusive_scan(nq, &xq, warp_sums);
+        const int tcb = block_exclusive_scan(nc, &xc, warp_sums);
+        if (b < p.B) {
+            dec_off[b] = s_carry[0] + xd;
+            unit_off[b] = s_carry[1] + xq;
+            comb_off[b] = s_carry[2] + xc;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            s_carry[0] += td;
+            s_carry[1] += tq;
+            s_carry[2] += tcb;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        dec_off[p.B] = s_carry[0];
+        unit_off[p.B] = s_carry[1];
+        comb_off[p.B] = s_carry[2];
+        // Requests whose token ranges overlap (a cu_seqlens_q entry that steps back between valid
+        // neighbours) can need more q tiles than T tokens allow, and the prefill partials are sized
+        // for T: such a batch is flagged and runs nothing.
+        s_overflow = s_carry[1] > p.units_cap;
+        if (s_overflow) s_err |= INK_DEVERR_CU_SEQLENS;
+        p.hdr->comb_tokens = s_overflow ? 0u : (uint32_t)s_carry[2];
+    }
+    __syncthreads();
+    if (my_err) atomicOr(&s_err, my_err);
+    __syncthreads();
+    __threadfence_block();
 
     const int n_dec = s_overflow ? 0 : min(s_carry[0], p.dec_items_cap);
     const int n_units = s_overflow ? 0 : s_carry[1];

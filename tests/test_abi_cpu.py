@@ -131,7 +131,8 @@ def test_fp8_entry_host_validation(lib):
         return f(ctypes.byref(d), q, good, good, ks, vs, good, good, good, 2, scale, 1, -1, -1, 0, None, 0,
                  good, None, good, 1 << 20, None)
 
-    for ks, vs in [(0.0, 1.0), (1.0, 0.0), (-2.0, 1.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+    for ks, vs in [(0.0, 1.0), (1.0, 0.0), (-2.0, 1.0), (float("nan"), 1.0), (1.0, float("inf")),
+                   (2.0 ** -127, 1.0), (1.0, 2.0 ** 127), (1e-40, 1.0)]:   # outside [2^-126, 2^126]
         assert call(ks, vs) == 1
     assert call(q=None) == 1                                   # null q
     assert call(q=good + 2) == 1                               # misaligned q
@@ -150,7 +151,8 @@ def test_fp8_append_host_validation(lib):
     f.argtypes = [ctypes.POINTER(ink.Dims), vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]
     good = 0x10000
     dims = ink.Dims(8, 1, 4, 4, 128, 16, 16, 1)
-    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf")), (2.0 ** -127, 1.0),
+                   (1.0, 2.0 ** 127), (1e-40, 1.0)]:   # the reciprocal of a scale below 2^-126 overflows
         assert f(ctypes.byref(dims), good, good, good, good, good, ks, vs, None, None) == 1
     assert f(ctypes.byref(dims), None, good, good, good, good, 1.0, 1.0, None, None) == 1       # null key
     assert f(ctypes.byref(dims), good, good, good + 8, good, good, 1.0, 1.0, None, None) == 1   # misaligned cache

@@ -196,11 +196,12 @@ def test_append_fp8_then_attend():
     assert (np.abs(l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max() <= LSE_RTOL
 
 
-@pytest.mark.parametrize("scale", [0.05, 1.0, 3.7e-3, 123.0, 2.0 ** -10, 0.3])
+@pytest.mark.parametrize("scale", [0.05, 1.0, 3.7e-3, 123.0, 2.0 ** -10, 0.3, 2.0 ** -126, 2.0 ** 126])
 def test_append_fp8_every_bf16_value(scale):
     """Every bf16 bit pattern except the NaNs (zeros, subnormals, normals, infinities, both signs) quantized
     with one scale: the stored codes equal the oracle's, which divides in IEEE fp32 and rounds with ties to
-    even.  Checks the kernel's quotient and conversion on the whole input range, not a sample."""
+    even.  Checks the kernel's quotient and conversion on the whole input range, not a sample, down to the
+    extreme scales the entry point accepts (2^-126: zeros stay zero, everything else saturates)."""
     bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
     vals = bits.view(torch.bfloat16)
     nan = torch.isnan(vals.float())

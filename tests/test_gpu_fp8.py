@@ -2,8 +2,9 @@
 
 The cache bytes come from the seeded generator (bf16 workload values divided
 by a per-tensor scale and rounded to E4M3); the oracle decodes the same bytes
-exactly, so the only differences are the kernel's fp32 accumulation and its
-fp16 q and probabilities.  Tolerances are those of the bf16 path.
+exactly, so the only differences are the kernels' fp32 accumulation and their
+fp16 (decode) or bf16 (prefill) q and probabilities.  Prefill-shaped requests
+read a staged bf16 copy of their pages.  Tolerances are those of the bf16 path.
 """
 import numpy as np
 import pytest
@@ -43,8 +44,15 @@ def oracle_fp8(case, k8, v8, ks=K_SCALE, vs=V_SCALE, rows=None):
                                   k_scale=ks, v_scale=vs, rows=rows, **c.oracle_kwargs())
 
 
+def prefill_keys(case):
+    """Cache keys of the prefill-shaped requests: what the call stages (converted to bf16)."""
+    G = case.H // case.Hkv
+    return sum(lk for lq, lk in zip(case.q_lens, case.kv_lens) if lq * G > 16)
+
+
 def parity_fp8(case, what, ks=K_SCALE, vs=V_SCALE, **kw):
     k8, v8 = fp8_kv(case, ks, vs)
+    kw.setdefault("stage_kv_tokens", prefill_keys(case))
     out, lse = run_fp8(case, k8, v8, ks, vs, **kw)
     ref_out, ref_lse = oracle_fp8(case, k8, v8, ks, vs)
     return check(out, lse, ref_out, ref_lse, what=what)
@@ -98,18 +106,87 @@ def test_fp8_bad_page_reads_as_zero_and_is_flagged():
     assert ink.read_device_errors() & ink.DEVERR["PAGE_ID"]
 
 
-def test_fp8_refuses_prefill_shaped_calls_and_bad_scales():
+def _dims(case):
+    return ink.Dims(case.T, case.B, case.H, case.Hkv, 128, case.num_blocks, case.BS, case.block_table.shape[1])
+
+
+def test_fp8_prefill_needs_staging_room_and_valid_scales():
+    """Prefill-shaped requests over an E4M3 cache are read through the staging copy: a workspace with no
+    room for it is refused; scales outside [2^-126, 2^126] are refused."""
     case = build_case("fp8-pf", [1, 64], [100, 64], H=16, Hkv=4, E=0, seed=29, device="cuda")
     k8, v8 = fp8_kv(case, K_SCALE, V_SCALE)
+    base = ink.workspace_size(_dims(case), case.max_seqlen_q, 0)
     with pytest.raises(ink.InkError) as e:
-        run_fp8(case, k8, v8)
-    assert e.value.status == 2  # unsupported: a request with 64 query tokens is prefill-shaped
-    case = build_case("fp8-d", [1, 1], [100, 64], H=16, Hkv=4, E=0, seed=29, device="cuda")
-    k8, v8 = fp8_kv(case, K_SCALE, V_SCALE)
-    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))]:
+        run_fp8(case, k8, v8, workspace=torch.empty(base, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 3  # workspace too small: nowhere to stage the prefill request
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf")), (2.0 ** -127, 1.0),
+                   (1.0, 2.0 ** 127)]:
         with pytest.raises(ink.InkError) as e:
-            run_fp8(case, k8, v8, ks, vs)
+            run_fp8(case, k8, v8, ks, vs, stage_kv_tokens=64)
         assert e.value.status == 1
+
+
+@pytest.mark.parametrize("H,Hkv", [(32, 8), (8, 1), (16, 2), (64, 8), (8, 8), (12, 4)])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_fp8_prefill_and_mixed_match_oracle(H, Hkv, splits):
+    """Prefill-shaped requests (read from the staged bf16 copy) next to decodes (read from the E4M3 pages)."""
+    case = build_case(f"fp8-pf-{H}-{Hkv}", [1, 130, 1, 37, 300], [700, 130, 33, 900, 300], H=H, Hkv=Hkv, E=96,
+                      seed=H * 3 + Hkv, device="cuda")
+    parity_fp8(case, f"fp8 prefill H={H} Hkv={Hkv} splits={splits}", num_splits=splits)
+    assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+
+
+def test_fp8_tiny_mix():
+    case = workload("tiny_mix", device="cuda")
+    for splits in (1, 4):
+        parity_fp8(case, f"fp8 tiny_mix splits={splits}", num_splits=splits)
+
+
+@pytest.mark.parametrize("window,causal", [((64, 0), True), ((100, 30), False), ((-1, -1), False)])
+def test_fp8_prefill_windows(window, causal):
+    case = build_case(f"fp8-pfw{window}", [140, 1, 33], [400, 800, 33], H=16, Hkv=4, E=64, seed=7, device="cuda",
+                      window=window, causal=causal)
+    parity_fp8(case, f"fp8 prefill window={window} causal={causal}")
+
+
+@pytest.mark.parametrize("ks,vs", [(1.0, 1.0), (0.013, 2.5), (3.0, 0.004)])
+def test_fp8_prefill_scales(ks, vs):
+    case = build_case("fp8-pf-scales", [200, 1], [513, 90], H=32, Hkv=8, E=128, seed=23, device="cuda")
+    parity_fp8(case, f"fp8 prefill k_scale={ks} v_scale={vs}", ks=ks, vs=vs)
+
+
+def test_fp8_prefill_without_room_is_skipped_and_flagged():
+    """Room for the first prefill request only: the second is skipped (its rows keep their contents) and
+    flagged; the decode and the first prefill request match the oracle."""
+    case = build_case("fp8-part", [100, 1, 120], [300, 500, 1000], H=16, Hkv=4, E=32, seed=37, device="cuda")
+    k8, v8 = fp8_kv(case, K_SCALE, V_SCALE)
+    base = ink.workspace_size(_dims(case), case.max_seqlen_q, 0)
+    ws = torch.empty(base + 384 * case.Hkv * 128 * 2 * 2, dtype=torch.uint8, device="cuda")  # 384 staged keys
+    out = torch.full_like(case.q, 7.0)
+    out, lse = run_fp8(case, k8, v8, workspace=ws, out=out)
+    assert ink.read_device_errors(ws) & ink.DEVERR["STAGE"]
+    cu = case.cu_seqlens_q.tolist()
+    assert torch.all(out[cu[2]:cu[3]] == 7.0)  # skipped: left as it was
+    rows = np.arange(0, cu[2] * case.H, dtype=np.int64)
+    ref_out, ref_lse = oracle_fp8(case, k8, v8, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what="fp8 partial staging")
+
+
+@pytest.mark.slow
+def test_fp8_chunked_prefill_full_size():
+    """The chunked prefill (4 x Lq 2048 on prior 0 .. 14336 keys, H 32, Hkv 8, E 4096) over an E4M3 cache,
+    staged; sampled rows against the oracle."""
+    case = workload("chunked_prefill", device="cuda")
+    k8, v8 = fp8_kv(case, K_SCALE, V_SCALE)
+    case.key_cache = case.value_cache = None
+    torch.cuda.empty_cache()
+    out, lse = run_fp8(case, k8, v8, stage_kv_tokens=prefill_keys(case))
+    assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+    rows = sampled_rows(case, 128, 13)
+    ref_out, ref_lse = oracle_fp8(case, k8, v8, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what="fp8 chunked_prefill")
+    del k8, v8, out, lse
+    torch.cuda.empty_cache()
 
 
 def test_fp8_batch_of_decodes_reads_half_the_bytes():
