@@ -80,6 +80,8 @@ struct Params {
     int fast_pack;       // prefill: warp-strided token packing (G divides 32)
     int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
     int bias_tok_log2;   // prefill: tokens per bias TMA box = 1 << bias_tok_log2
+    int pf_kv_slots;     // prefill: K/V ring depth (32 KB slots)
+    int pf_bias_slots;   // prefill: bias ring depth (half-tile stages; 0 without bias boxes)
 };
 
 // ---------------------------------------------------------------------------
@@ -159,8 +161,8 @@ __host__ __device__ __forceinline__ int stage_keys_of(int Lk) { return (Lk + kTi
 // token k + 1 starts one key later than token k's, so a common start rounded down to 16
 // bytes and a width of 64 + 3 + (nb - 1) floats, rounded up to 16 bytes, cover every token
 // of the box (the softmax reads 17 whole 16-byte chunks from the one holding a row's start).
-constexpr int kPfKvSlots = 3;     // prefill K/V ring (32 KB slots)
-constexpr int kPfBiasSlots = 3;   // prefill bias ring (half-tile stages)
+constexpr int kPfMaxKvSlots = 6;    // prefill K/V ring: 32 KB slots, as many as shared memory holds (up to 6)
+constexpr int kPfMaxBiasSlots = 3;  // prefill bias ring: half-tile stages (0 when the call has no bias boxes)
 __host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (70 + nb) & ~3; }
 // Bytes a box transfers, and its shared-memory footprint (a TMA destination is 128-byte aligned).
 __host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb) { return nb * G * pf_bias_width(nb) * 4; }
@@ -171,9 +173,9 @@ __host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int 
     return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb);
 }
 // The prefill kernel's shared-memory layout: K/V ring, bias ring, bookkeeping.
-__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb)
+__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb, int kv_slots, int bias_slots)
 {
-    return (size_t)kPfKvSlots * 32768 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
+    return (size_t)kv_slots * 32768 + (size_t)bias_slots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
 }
 
 // Packed row of (token offset k, head j) inside a prefill tile, and back.

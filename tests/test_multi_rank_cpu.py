@@ -51,3 +51,18 @@ def test_single_process_is_identity():
 
     assert bench.max_over_ranks(1.25) == 1.25
     assert bench.job_throughput(10.0, 1, 1000.0) == pytest.approx(10.0)
+
+
+def test_gpus_flag_starts_one_rank_per_gpu():
+    """`bench.py --gpus N` outside torchrun re-runs itself as N ranks of torch.distributed.run on 127.0.0.1."""
+    import sys
+
+    import bench
+
+    cmd = bench.relaunch_cmd(8, ["--gpus", "8", "--steps", "5"], 29511)
+    assert cmd[:3] == [sys.executable, "-m", "torch.distributed.run"]
+    assert "--nproc-per-node=8" in cmd and "--nnodes=1" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[cmd.index("--master-port") + 1] == "29511"
+    assert cmd[-5].endswith("bench.py") and cmd[-4:] == ["--gpus", "8", "--steps", "5"]
+    assert 0 < bench.free_port() < 65536
