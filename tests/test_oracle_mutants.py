@@ -37,6 +37,7 @@ MUTANTS = {
     "unnormalised partials": ("tot[d] += w * (acc[d] / l);", "tot[d] += w * acc[d];"),
     "query of group leader": ("const uint16_t *qrow = a->q + ((int64_t)t * a->H + h) * a->D;",
                               "const uint16_t *qrow = a->q + ((int64_t)t * a->H + (h / G) * G) * a->D;"),
+    "head dim half read": ("            for (int32_t d = 0; d < a->D; ++d)\n", "            for (int32_t d = 0; d < a->D / 2; ++d)\n"),
     "page index by row": ("a->bt[(int64_t)b * a->MAXBLK + j / a->BS];\n            if (page < 0",
                           "a->bt[(int64_t)b * a->MAXBLK + j % a->BS];\n            if (page < 0"),
 }

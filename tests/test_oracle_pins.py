@@ -159,9 +159,11 @@ def test_oracle_matches_dense_bruteforce(seed):
     _close(lse, dlse, 1e-12)
 
 
-@pytest.mark.parametrize("seed", range(12))
-def test_oracle_matches_dense_head_dim_128(seed):
-    case = random_case(500 + seed, D=128)
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("seed", range(8))
+def test_oracle_matches_dense_wide_head_dims(seed, D):
+    """The head sizes a paged backend serves (64, 128, 256) against the dense formulation."""
+    case = random_case(500 + seed + 31 * D, D=D)
     out, lse = _run(case)
     dout, dlse = _dense(case)
     _close(out, dout, 1e-12)
@@ -170,8 +172,8 @@ def test_oracle_matches_dense_head_dim_128(seed):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_zero_bias_is_sdpa_with_explicit_mask(seed):
-    """rel_logits == 0 reduces to plain causal GQA attention (fp64 SDPA)."""
-    case = random_case(900 + seed, D=32, E=16)
+    """rel_logits == 0 reduces to plain causal GQA attention (fp64 SDPA), at head sizes 32, 64 and 256."""
+    case = random_case(900 + seed, D=[32, 64, 256][seed % 3], E=16)
     case.rel_logits = torch.zeros_like(case.rel_logits)
     out, lse = _run(case)
     out0, _ = _run(case, rel_extent=0, rel_logits=None)
@@ -211,9 +213,10 @@ def test_zero_bias_is_sdpa_with_explicit_mask(seed):
 
 # --- closed forms -------------------------------------------------------------
 
-def test_single_key_decode_closed_form():
+@pytest.mark.parametrize("D", [16, 64, 256])
+def test_single_key_decode_closed_form(D):
     """Lk = 1: the output is the single V row and lse the single score."""
-    case = build_case("one", [1, 1], [1, 1], H=4, Hkv=2, D=16, BS=4, E=3, seed=7)
+    case = build_case("one", [1, 1], [1, 1], H=4, Hkv=2, D=D, BS=4, E=3, seed=7)
     out, lse = _run(case)
     for b in range(2):
         t = b
