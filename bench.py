@@ -33,6 +33,7 @@ HEADLINE = "decode_batch"
 SECONDARY = ["chunked_prefill", "long_decode", "continuous_batch"]
 FP8_SCALES = (0.0625, 0.05)  # k_scale, v_scale of the E4M3 caches the bench builds
 TIMED_KERNELS = ("prepass", "stage", "decode", "prefill", "combine")
+HEADDIM = ("decode_batch_d64", "chunked_prefill_d64", "decode_batch_d256", "chunked_prefill_d256")
 D = 128
 
 
@@ -45,6 +46,7 @@ def work_of(case):
     Prefill: 4 * D * H * (#visible (q, k) pairs) over prefill requests.
     """
     G = case.H // case.Hkv
+    D = getattr(case, "D", 128)
     kv_bytes = 0
     flops = 0
     pairs = 0
@@ -85,7 +87,7 @@ def total_bytes(case, fp8=False):
     kv, _, _ = work_of(case)
     el = 1 if fp8 else 2
     b = case.q.numel() * 2 * 2  # q in, out
-    b += prefill_keys(case) * case.Hkv * D * 2 * el
+    b += prefill_keys(case) * case.Hkv * case.D * 2 * el
     if case.E > 0:
         b += _bias_bytes(case)
     return kv * el // 2 + b
@@ -309,9 +311,9 @@ def run_ours(args, rank, world, local_rank):
     import torch
 
     import paged_varlen_attention_causal_gb300 as ink
-    from workloads import PROFILE_WORKLOADS, WORKLOADS, build_case, fp8_kv, workload
+    from workloads import HEADDIM_WORKLOADS, PROFILE_WORKLOADS, WORKLOADS, build_case, fp8_kv, workload
 
-    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS, **HEADDIM_WORKLOADS}
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     ink.build()
@@ -616,7 +618,8 @@ def run_ours(args, rank, world, local_rank):
 
     steps, warmup = args.steps, args.warmup
     headline = args.workload
-    head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
+    # head sizes 64 / 256 run every request in the head-size-generic kernel, timed under the prefill's id
+    head_kernel = "prefill" if headline.startswith("chunked_prefill") or headline in HEADDIM else "decode"
     head = measure(headline, steps, warmup, head_kernel, fp8=args.kv_fp8)
     sec = {}
     skip = {x for x in args.skip.split(",") if x}
@@ -627,6 +630,10 @@ def run_ours(args, rank, world, local_rank):
             ("kv_append_fp8", lambda: measure_append(s2, w2, fp8=True)),
             ("graph_decode", lambda: measure_graph(max(50, steps * 10), max(5, warmup))),
             ("long_decode_splits", lambda: measure_split_sweep(max(5, steps // 2), w2)),
+            ("decode_batch_d64", lambda: measure("decode_batch_d64", s2, w2, "prefill")),
+            ("chunked_prefill_d64", lambda: measure("chunked_prefill_d64", s2, w2, "prefill")),
+            ("decode_batch_d256", lambda: measure("decode_batch_d256", s2, w2, "prefill")),
+            ("chunked_prefill_d256", lambda: measure("chunked_prefill_d256", s2, w2, "prefill")),
             ("decode_batch_fp8", lambda: measure("decode_batch", s2, w2, "decode", fp8=True)),
             ("long_decode", lambda: measure("long_decode", s2, w2, "decode")),
             ("decode_batch", lambda: measure("decode_batch", s2, w2, "decode")),
@@ -648,18 +655,18 @@ def run_ours(args, rank, world, local_rank):
     def tfs(flops, ms):
         return flops / (ms * 1e-3) / 1e12
 
-    def roof_decode(r, name, fp8=False):
+    def roof_decode(r, name, fp8=False, kernel="ink_decode_kernel"):
         ach = gbs(r["kv_bytes"], r["kernel_ms"])
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "frac_of_8000": round(ach / 8000.0, 4),
-                "traffic": traffic_of("ink_decode_kernel", name),
-                "peak_source": peaks["source"], "kernel": "ink_decode_kernel" + (" (E4M3 cache)" if fp8 else "")}
+                "traffic": traffic_of(kernel, name),
+                "peak_source": peaks["source"], "kernel": kernel + (" (E4M3 cache)" if fp8 else "")}
 
-    def roof_prefill(r, name, fp8=False):
+    def roof_prefill(r, name, fp8=False, kernel="ink_prefill_kernel"):
         ach = tfs(r["flops"], r["kernel_ms"])
         return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic_of("ink_prefill_kernel", name),
-                "peak_source": peaks["source"], "kernel": "ink_prefill_kernel" + (" (E4M3 cache, staged)" if fp8 else "")}
+                "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic_of(kernel, name),
+                "peak_source": peaks["source"], "kernel": kernel + (" (E4M3 cache, staged)" if fp8 else "")}
 
     def step_bound(r):
         """The step's own floor: its flops at the tensor peak or its compulsory bytes at the HBM peak."""
@@ -677,16 +684,17 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     fp8_head = args.kv_fp8
+    hkw = {"kernel": "ink_generic_kernel"} if headline in HEADDIM else {}
     if headline.startswith("chunked_prefill"):
         unit = "TFLOP/s"
         value = job_throughput(head["flops"], world, head["ms_per_step"]) / 1e12
         e2e = job_throughput(head["flops"], world, head["e2e_ms"]) / 1e12
-        roof = roof_prefill(head, headline + ("_fp8" if fp8_head else ""), fp8_head)
+        roof = roof_prefill(head, headline + ("_fp8" if fp8_head else ""), fp8_head, **hkw)
     else:
         unit = "GB/s"
         value = job_throughput(head["kv_bytes"], world, head["ms_per_step"]) / 1e9
         e2e = job_throughput(head["kv_bytes"], world, head["e2e_ms"]) / 1e9
-        roof = roof_decode(head, headline + ("_fp8" if fp8_head else ""), fp8_head)
+        roof = roof_decode(head, headline + ("_fp8" if fp8_head else ""), fp8_head, **hkw)
     cpu_secs = args.cpu_seconds_each
     workloads_out = {}
     for name, r in sec.items():
@@ -720,11 +728,13 @@ def run_ours(args, rank, world, local_rank):
             continue
         fp8 = name.endswith("_fp8")
         base = name[:-4] if fp8 else name
+        kern = "ink_generic_kernel" if base in HEADDIM else None
+        kw = {"kernel": kern} if kern else {}
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "kernel_ms": kernels_of(r),
                  "e2e_ms": round(r["e2e_ms"], 4), "gpu_launches": r["launches"], "clocks": clk_of(r)}
-        if base == "chunked_prefill":
+        if base.startswith("chunked_prefill"):
             entry.update({"metric": "prefill TFLOP/s (visible pairs)", "value": round(tfs(r["flops"], r["ms_per_step"]), 2),
-                          "unit": "TFLOP/s", "roofline": roof_prefill(r, name, fp8), "step_roofline": step_bound(r)})
+                          "unit": "TFLOP/s", "roofline": roof_prefill(r, name, fp8, **kw), "step_roofline": step_bound(r)})
         elif base == "continuous_batch":
             entry.update({"metric": "decode KV-read GB/s + prefill TFLOP/s over the step",
                           "decode_gbs": round(gbs(r["kv_bytes"], r["ms_per_step"]), 1),
@@ -735,7 +745,7 @@ def run_ours(args, rank, world, local_rank):
         else:
             entry.update({"metric": "decode KV-read GB/s" + (" (E4M3 cache bytes)" if fp8 else ""),
                           "value": round(gbs(r["kv_bytes"], r["ms_per_step"]), 1), "unit": "GB/s",
-                          "roofline": roof_decode(r, name, fp8)})
+                          "roofline": roof_decode(r, name, fp8, **kw)})
         if not args.no_cpu_baseline:
             try:
                 entry["cpu_baseline"] = cpu_baseline(base, cpu_secs, fp8=fp8, short=True)
@@ -826,7 +836,7 @@ def cpu_baseline(name, seconds, fp8=False, short=False, case=None):
                 run(np.arange(cu[b] * case.H, cu[b + 1] * case.H, dtype=np.int64))
                 lq, lk = case.q_lens[b], case.kv_lens[b]
                 keys = max(_row_pairs(case, lq, lk, i) for i in range(lq))  # the union of the rows' ranges
-                dec_bytes += keys * case.Hkv * D * 2 * el
+                dec_bytes += keys * case.Hkv * case.D * 2 * el
                 dec_reqs += 1
                 if time.perf_counter() - t0 >= budget:
                     break
@@ -842,7 +852,7 @@ def cpu_baseline(name, seconds, fp8=False, short=False, case=None):
             lq, lk = case.q_lens[b], case.kv_lens[b]
             rows = np.unique(g.integers(cu[b] * case.H, cu[b + 1] * case.H, size=64)).astype(np.int64)
             run(rows)
-            pre_flops += sum(4 * D * _row_pairs(case, lq, lk, int(r) // case.H - cu[b]) for r in rows)
+            pre_flops += sum(4 * case.D * _row_pairs(case, lq, lk, int(r) // case.H - cu[b]) for r in rows)
             pre_rows += rows.size
         pre_s = time.perf_counter() - t0
     cpu_name = ""
@@ -881,11 +891,9 @@ def cpu_baseline(name, seconds, fp8=False, short=False, case=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    from workloads import PROFILE_WORKLOADS, WORKLOADS  # noqa: F401
+    from workloads import HEADDIM_WORKLOADS, PROFILE_WORKLOADS, WORKLOADS, workload
 
-    from workloads import workload
-
-    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+    WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS, **HEADDIM_WORKLOADS}
     case = workload(args.workload, device="cpu")
     times = []
     val = None
@@ -934,7 +942,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["decode_batch", "chunked_prefill", "long_decode", "continuous_batch",
-                             "decode_batch_quarter", "chunked_prefill_quarter"])
+                             "decode_batch_quarter", "chunked_prefill_quarter", "decode_batch_d64",
+                             "chunked_prefill_d64", "decode_batch_d256", "chunked_prefill_d256"])
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="run the headline workload over an E4M3 copy of its KV cache")

@@ -30,7 +30,7 @@
  * Besides the attention over a bf16 cache (ink_rel_attn_varlen and its
  * allocation-free twin ink_rel_attn_varlen_static) the library has the same
  * attention over an FP8 (E4M3) cache with per-tensor scales
- * (ink_rel_attn_varlen_fp8kv, decode-shaped calls) and the KV append that
+ * (ink_rel_attn_varlen_fp8kv) and the KV append that
  * precedes attention on every step (ink_reshape_and_cache, and
  * ink_reshape_and_cache_fp8 which quantizes into an E4M3 cache).
  *
@@ -65,7 +65,7 @@ typedef struct {
     int32_t batch;               /* B: requests                               */
     int32_t num_heads;           /* H: query heads                            */
     int32_t num_kv_heads;        /* Hkv: KV heads, H % Hkv == 0               */
-    int32_t head_dim;            /* D: must be 128                            */
+    int32_t head_dim;            /* D: 64, 128 or 256 (FP8 cache: 128 only)   */
     int32_t num_blocks;          /* physical pages in each cache              */
     int32_t block_size;          /* keys per page: a multiple of 16           */
     int32_t max_blocks_per_seq;  /* width of block_table                      */
@@ -74,7 +74,7 @@ typedef struct {
 typedef enum {
     INK_OK = 0,
     INK_ERR_INVALID_ARG = 1,  /* bad pointer, shape, scalar or alignment     */
-    INK_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, ...   */
+    INK_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim not in {64, 128, 256}, ... */
     INK_ERR_WORKSPACE = 3,    /* workspace smaller than the size query says  */
     INK_ERR_CUDA = 4          /* a CUDA runtime / driver call failed         */
 } ink_status;
@@ -117,7 +117,9 @@ INK_API size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t ma
  * Workspace beyond ink_rel_attn_workspace_size is always used this way: each
  * call copies, in request order, the pages of every prefill-shaped request
  * whose keys (rounded up to whole 128-key tiles) still fit, and the rest read
- * the paged cache.  Results do not depend on it.  Returns 0 for invalid dims.
+ * the paged cache.  Results do not depend on it.  Returns 0 for invalid dims
+ * and for head sizes other than 128 (the head-size-generic kernel reads the
+ * paged cache directly).
  */
 INK_API size_t ink_rel_attn_stage_bytes(const ink_attn_dims *dims, int64_t prefill_kv_tokens);
 
@@ -164,6 +166,10 @@ INK_API int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_s
  *                 call that overlaps this one on the GPU.  Bytes beyond that
  *                 size stage K/V for the prefill (ink_rel_attn_stage_bytes).
  *   stream        CUDA stream the kernels are launched on.
+ * Head sizes: D = 128 runs the tcgen05 prefill and the decode kernel; D = 64
+ * and 256 (the other head sizes the vLLM V1 attention page lists for a paged
+ * backend; the PagedAttention V2 page's GQA example uses 256) run one
+ * head-size-generic kernel (mma.sync, the same work list) for every request.
  * Host-side checks return INK_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE
  * before anything is launched; a launch failure returns INK_ERR_CUDA.
  * Data errors found on the device are reported through the error word.
@@ -187,7 +193,8 @@ INK_API ink_status ink_rel_attn_varlen(const ink_attn_dims *dims,
  * to the gathered K and V rows as paged_attention_v2_pytorch does on the
  * PagedAttention V2 page.
  *   key_cache, value_cache  OCP FP8 E4M3 bytes, (num_blocks, block_size,
- *                 Hkv, D), contiguous, 16-byte aligned; the values attended
+ *                 Hkv, D) with D = 128 (other head sizes return
+ *                 INK_ERR_UNSUPPORTED), contiguous, 16-byte aligned; the values attended
  *                 over are k_scale * E4M3(byte) and v_scale * E4M3(byte).
  *   k_scale, v_scale  in [2^-126, 2^126] (normal, with a normal reciprocal),
  *                 else INK_ERR_INVALID_ARG.
@@ -257,8 +264,8 @@ INK_API ink_status ink_rel_attn_varlen_static(const ink_attn_dims *dims,
  *     value_cache[s / block_size][s % block_size][h][:] = value[t][h][:]
  * for every KV head h; negative slots are padding and are skipped.
  *
- *   dims        num_tokens, num_kv_heads, head_dim (128), num_blocks and
- *               block_size are read; the other fields are ignored.
+ *   dims        num_tokens, num_kv_heads, head_dim (64, 128 or 256), num_blocks
+ *               and block_size are read; the other fields are ignored.
  *   key, value  device, bf16 (num_tokens, num_kv_heads, head_dim), 16-byte
  *               aligned; read only.
  *   key_cache, value_cache
@@ -269,7 +276,8 @@ INK_API ink_status ink_rel_attn_varlen_static(const ink_attn_dims *dims,
  *               slot is >= num_blocks * block_size (that token is skipped).
  *   stream      the call is stream-ordered; it allocates nothing.
  * Returns INK_ERR_INVALID_ARG for null pointers, bad shapes or misalignment,
- * INK_ERR_UNSUPPORTED for head_dim != 128, INK_ERR_CUDA on a launch error.
+ * INK_ERR_UNSUPPORTED for a head_dim outside {64, 128, 256}, INK_ERR_CUDA on a
+ * launch error.
  */
 INK_API ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, const void *value,
                                          void *key_cache, void *value_cache, const int64_t *slot_mapping,
@@ -288,7 +296,8 @@ INK_API ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *
  *               num_kv_heads, 128), 16-byte aligned.
  *   k_scale, v_scale  in [2^-126, 2^126] (normal, with a normal reciprocal),
  *                 else INK_ERR_INVALID_ARG.
- * Other errors as ink_reshape_and_cache.
+ * Other errors as ink_reshape_and_cache, except that head_dim must be 128
+ * (the size the FP8 attention reads), else INK_ERR_UNSUPPORTED.
  */
 INK_API ink_status ink_reshape_and_cache_fp8(const ink_attn_dims *dims, const void *key, const void *value,
                                              void *key_cache, void *value_cache, const int64_t *slot_mapping,

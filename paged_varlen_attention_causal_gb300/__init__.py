@@ -127,6 +127,8 @@ def launch_count() -> int:
 def _dims(q, key_cache, block_table) -> Dims:
     T, H, D = q.shape
     NB, BS, Hkv, D2 = key_cache.shape
+    if D2 != D:
+        raise ValueError("q and the caches differ in head_dim")
     B, W = block_table.shape
     return Dims(T, B, H, Hkv, D, NB, BS, W)
 
@@ -284,7 +286,7 @@ def ink_rel_attn_varlen_fp8kv(q, key_cache, value_cache, *, k_scale: float, v_sc
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *, flags=None, stream=None) -> None:
     """Write this step's keys and values into the paged cache at ``slot_mapping`` (see include/ink_attn.h).
 
-    key/value: bf16 (T, Hkv, 128); caches: bf16 (num_blocks, block_size, Hkv, 128), written in place;
+    key/value: bf16 (T, Hkv, D) with D = 64, 128 or 256; caches: bf16 (num_blocks, block_size, Hkv, D), written in place;
     slot_mapping: int64 (T,), negative = padding; flags: optional int32 (1,) device tensor that receives
     DEVERR["PAGE_ID"] for slots past the cache.
     """

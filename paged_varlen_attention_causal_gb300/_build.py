@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libinkattn.so")
 SOURCES = ["ink_api.cu", "ink_prepass.cu", "ink_decode.cu", "ink_prefill.cu", "ink_combine.cu", "ink_static.cu",
-           "ink_append.cu", "ink_stage.cu"]
+           "ink_append.cu", "ink_stage.cu", "ink_generic.cu"]
 HEADERS = [os.path.join(CSRC, "ink_common.cuh"), os.path.join(ROOT, "include", "ink_attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

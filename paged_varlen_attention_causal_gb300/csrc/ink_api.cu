@@ -94,10 +94,14 @@ bool dims_ok(const ink_attn_dims *d)
            d->max_blocks_per_seq >= 1;
 }
 
+// Head sizes: 128 runs the tcgen05 prefill and the decode kernel; 64 and 256 run the
+// head-size-generic kernel.
+bool head_dim_supported(int D) { return D == 64 || D == kHeadDim || D == 256; }
+
 bool dims_supported(const ink_attn_dims *d)
 {
     const int G = d->num_heads / d->num_kv_heads;
-    return d->head_dim == kHeadDim && d->block_size % kKeyGroup == 0 && G <= kTileRows &&
+    return head_dim_supported(d->head_dim) && d->block_size % kKeyGroup == 0 && G <= kTileRows &&
            (long long)d->num_blocks * d->block_size < (1ll << 31);
 }
 
@@ -158,8 +162,9 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
             break;
         }
     }
-    pl.fast_pack = (32 % pl.G == 0) ? 1 : 0;
-    pl.decode_kernel = (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
+    const bool generic = d->head_dim != kHeadDim;  // head-size-generic kernel: every request as 128-row items
+    pl.fast_pack = (!generic && 32 % pl.G == 0) ? 1 : 0;
+    pl.decode_kernel = !generic && (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
     const long long msq = std::min<long long>(max_seqlen_q, std::max(T, 1));
     pl.any_decode = pl.decode_kernel != 0;
     pl.any_prefill = !pl.decode_kernel || msq * pl.G > kDecodeRows;
@@ -201,9 +206,9 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     const size_t dec_rows_total = dec_parts ? (size_t)pl.dec_cap * pl.dec_rows : 0;
     const size_t pf_rows_total = pf_parts ? (size_t)pl.units_cap * pl.S_pf * Hkv * kTileRows : 0;
     pl.off_pdl = off; off = align256(off + sizeof(float) * dec_rows_total);
-    pl.off_pdo = off; off = align256(off + sizeof(float) * dec_rows_total * kHeadDim);
+    pl.off_pdo = off; off = align256(off + sizeof(float) * dec_rows_total * d->head_dim);
     pl.off_ppl = off; off = align256(off + sizeof(float) * pf_rows_total);
-    pl.off_ppo = off; off = align256(off + sizeof(float) * pf_rows_total * kHeadDim);
+    pl.off_ppo = off; off = align256(off + sizeof(float) * pf_rows_total * d->head_dim);
     pl.total = off;
     return true;
 }
@@ -286,6 +291,7 @@ size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t max_seqlen
 size_t ink_rel_attn_stage_bytes(const ink_attn_dims *dims, int64_t prefill_kv_tokens)
 {
     if (!dims_ok(dims) || prefill_kv_tokens < 0) return 0;
+    if (dims->head_dim != kHeadDim) return 0;  // the head-size-generic kernel reads the paged cache directly
     // every staged request occupies whole 128-key tiles: at most 127 keys of rounding per request
     const long long keys = prefill_kv_tokens + (long long)dims->batch * (kTileKeys - 1);
     const long long tiles = (keys + kTileKeys - 1) / kTileKeys;
@@ -358,6 +364,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         (lse && !aligned(lse, 4)) || (rel_logits && !aligned(rel_logits, 4)) || !aligned(workspace, 256))
         return INK_ERR_INVALID_ARG;
     if (!dims_supported(dims)) return INK_ERR_UNSUPPORTED;
+    if (kv.fp8 && dims->head_dim != kHeadDim) return INK_ERR_UNSUPPORTED;  // an E4M3 cache is read at D = 128 only
     if (dims->num_tokens == 0) return INK_OK;
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
@@ -372,7 +379,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     Params p;
     memset(&p, 0, sizeof p);
+    const bool generic = dims->head_dim != kHeadDim;  // head size 64 or 256: the head-size-generic kernel
     p.T = T; p.B = dims->batch; p.H = H; p.Hkv = Hkv; p.G = pl.G; p.NB = dims->num_blocks;
+    p.D = dims->head_dim;
     p.BS = dims->block_size; p.MAXBLK = dims->max_blocks_per_seq; p.max_seqlen_q = max_seqlen_q;
     p.softmax_scale = softmax_scale;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -405,7 +414,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const size_t extra = workspace_bytes - pl.total;
         long long cap = (long long)(extra / per_key) / kTileKeys * kTileKeys;
         cap = std::min<long long>(cap, 1ll << 24);
-        p.stage_cap = (pl.any_prefill && cap >= kTileKeys) ? (int)cap : 0;
+        p.stage_cap = (!generic && pl.any_prefill && cap >= kTileKeys) ? (int)cap : 0;
         // an FP8 cache reaches the prefill only through the staging copy (converted to bf16)
         if (kv.fp8 && pl.any_prefill && p.stage_cap == 0) return INK_ERR_WORKSPACE;
         p.ks = reinterpret_cast<__nv_bfloat16 *>(ws + pl.total);
@@ -423,6 +432,22 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.bias_tok_log2 = pl.bias_tok_log2;
     p.kv_fp8 = kv.fp8;
     p.out_scale = 1.f;
+
+    if (generic) {
+        // head size 64 or 256: the device plan, the head-size-generic kernel over every request's
+        // 128-row items (timed as the prefill kernel), and the split-KV merge
+        if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, stream); }) != cudaSuccess)
+            return INK_ERR_CUDA;
+        if (pl.any_prefill && pl.pf_cap > 0) {
+            if (timed_launch(INK_KERNEL_PREFILL, stream, [&] { return launch_generic(p, sms, stream); }) != cudaSuccess)
+                return INK_ERR_CUDA;
+        }
+        if (pl.any_prefill && pl.S_pf > 1) {
+            if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, stream); }) != cudaSuccess)
+                return INK_ERR_CUDA;
+        }
+        return INK_OK;
+    }
 
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
     alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_kd, tm_vd, tm_bdec, tm_bpf;
@@ -573,7 +598,7 @@ ink_status ink_reshape_and_cache(const ink_attn_dims *dims, const void *key, con
     if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
         !aligned(slot_mapping, 8) || (flags && !aligned(flags, 4)))
         return INK_ERR_INVALID_ARG;
-    if (dims->head_dim != kHeadDim) return INK_ERR_UNSUPPORTED;
+    if (!head_dim_supported(dims->head_dim)) return INK_ERR_UNSUPPORTED;
     if (dims->num_tokens == 0) return INK_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     const int sms = sm_count_of_current_device();

@@ -101,7 +101,7 @@ cudaError_t launch_append_fp8(const ink_attn_dims *d, const void *key, const voi
                               void *value_cache, const int64_t *slot_mapping, float k_scale, float v_scale,
                               uint32_t *flags, int sms, cudaStream_t stream)
 {
-    const int chunks = d->num_kv_heads * kHeadDim * 2 / 16;
+    const int chunks = d->num_kv_heads * d->head_dim * 2 / 16;
     const long long total = (long long)d->num_tokens * chunks;
     const long long want = (total + kAppendThreads - 1) / kAppendThreads;
     const int grid = (int)(want < 8ll * sms ? (want > 0 ? want : 1) : 8ll * sms);
@@ -116,7 +116,7 @@ cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *v
                           void *value_cache, const int64_t *slot_mapping, uint32_t *flags, int sms,
                           cudaStream_t stream)
 {
-    const int chunks = d->num_kv_heads * kHeadDim * 2 / 16;
+    const int chunks = d->num_kv_heads * d->head_dim * 2 / 16;
     const long long total = (long long)d->num_tokens * chunks;
     // enough CTAs to fill every SM a few times over; each thread loops over its chunks
     const long long want = (total + kAppendThreads - 1) / kAppendThreads;

@@ -9,8 +9,8 @@
 // Splits with no visible key carry lse_s = -inf and weigh nothing.
 //
 // kWarpsPerRow warps share one row (warp w takes splits w, w + kWarpsPerRow, ...)
-// and merge their states through shared memory; lane l owns d values
-// 4l..4l+3.  Loads are issued kBatch splits at a time.
+// and merge their states through shared memory; lane l owns D / 32 consecutive
+// d values.  Loads are issued kBatch splits at a time.
 #include <algorithm>
 
 #include "ink_common.cuh"
@@ -72,12 +72,44 @@ __device__ __forceinline__ bool row_partials(const Params &p, int b, int t, int 
     return true;
 }
 
-template <int kWarpsPerRow>
+// V consecutive floats of one lane (V = D / 32): loads and the bf16 store.
+template <int V>
+__device__ __forceinline__ void ld_vec(const float *src, float (&x)[V])
+{
+    if constexpr (V == 2) {
+        const float2 a = __ldg(reinterpret_cast<const float2 *>(src));
+        x[0] = a.x; x[1] = a.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < V / 4; ++q) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src) + q);
+            x[4 * q] = a.x; x[4 * q + 1] = a.y; x[4 * q + 2] = a.z; x[4 * q + 3] = a.w;
+        }
+    }
+}
+
+template <int V>
+__device__ __forceinline__ void st_bf16(__nv_bfloat16 *dst, const float (&x)[V], float scale)
+{
+    uint32_t w[V / 2];
+#pragma unroll
+    for (int q = 0; q < V / 2; ++q) w[q] = pack_bf16x2(x[2 * q] * scale, x[2 * q + 1] * scale);
+    if constexpr (V == 2) {
+        *reinterpret_cast<uint32_t *>(dst) = w[0];
+    } else if constexpr (V == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int kWarpsPerRow, int D>
 __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Params p)
 {
     constexpr int kRowsPerCta = kCombineThreads / 32 / kWarpsPerRow;
+    constexpr int V = D / 32;  // head-dim values per lane: lane l owns V l .. V l + V - 1
     __shared__ float s_m[kCombineThreads / 32], s_l[kCombineThreads / 32];
-    __shared__ float4 s_acc[kWarpsPerRow > 1 ? kCombineThreads / 32 : 1][32];
+    __shared__ float s_acc[kWarpsPerRow > 1 ? kCombineThreads / 32 : 1][32][V];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = warp % kWarpsPerRow;  // this warp's share of the row's splits
     const long long nrows = (long long)*(volatile uint32_t *)&p.hdr->comb_tokens * p.H;
@@ -92,20 +124,23 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
             active = row_partials(p, b, t, h, rp);
         }
         float m = -INFINITY, l = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float acc[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = 0.f;
         if (active) {
             for (int s0 = sub; s0 < rp.nact; s0 += kWarpsPerRow * kBatch) {
                 float ls[kBatch];
-                float4 os[kBatch];
+                float os[kBatch][V];
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {  // issue the batch's loads before using any of them
                     const int s = s0 + u * kWarpsPerRow;
                     ls[u] = -INFINITY;
-                    os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) os[u][e] = 0.f;
                     if (s < rp.nact) {
                         const size_t pr = rp.first + (size_t)s * rp.stride;
                         ls[u] = __ldg(rp.pl + pr);
-                        os[u] = __ldg(reinterpret_cast<const float4 *>(rp.po + pr * kHeadDim) + lane);
+                        ld_vec<V>(rp.po + pr * D + V * lane, os[u]);
                     }
                 }
 #pragma unroll
@@ -113,16 +148,15 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
                     if (ls[u] == -INFINITY) continue;
                     if (ls[u] > m) {
                         const float a = __expf(m - ls[u]);  // m = -inf gives 0
-                        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+#pragma unroll
+                        for (int e = 0; e < V; ++e) acc[e] *= a;
                         l *= a;
                         m = ls[u];
                     }
                     const float w = __expf(ls[u] - m);
                     l += w;
-                    acc.x = fmaf(w, os[u].x, acc.x);
-                    acc.y = fmaf(w, os[u].y, acc.y);
-                    acc.z = fmaf(w, os[u].z, acc.z);
-                    acc.w = fmaf(w, os[u].w, acc.w);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = fmaf(w, os[u][e], acc[e]);
                 }
             }
         }
@@ -131,25 +165,24 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
                 s_m[warp] = m;
                 s_l[warp] = l;
             }
-            s_acc[warp][lane] = acc;
+#pragma unroll
+            for (int e = 0; e < V; ++e) s_acc[warp][lane][e] = acc[e];
             __syncthreads();
             if (active && sub == 0) {
                 float gm = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kWarpsPerRow; ++w) gm = fmaxf(gm, s_m[warp + w]);
                 l = 0.f;
-                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] = 0.f;
                 if (gm != -INFINITY) {
 #pragma unroll
                     for (int w = 0; w < kWarpsPerRow; ++w) {
                         if (s_m[warp + w] == -INFINITY) continue;
                         const float a = __expf(s_m[warp + w] - gm);
-                        const float4 v = s_acc[warp + w][lane];
                         l = fmaf(a, s_l[warp + w], l);
-                        acc.x = fmaf(a, v.x, acc.x);
-                        acc.y = fmaf(a, v.y, acc.y);
-                        acc.z = fmaf(a, v.z, acc.z);
-                        acc.w = fmaf(a, v.w, acc.w);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) acc[e] = fmaf(a, s_acc[warp + w][lane][e], acc[e]);
                     }
                 }
                 m = gm;
@@ -159,12 +192,21 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
         }
         if (!active) continue;
         const size_t orow = (size_t)t * p.H + h;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint2 outv;
-        outv.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        outv.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(p.out + orow * kHeadDim + 4 * lane) = outv;
+        st_bf16<V>(p.out + orow * D + V * lane, acc, l > 0.f ? 1.f / l : 0.f);
         if (p.lse && lane == 0) p.lse[orow] = l > 0.f ? m + __logf(l) : -INFINITY;
+    }
+}
+
+template <int D>
+void launch_combine_d(const Params &p, int sms, cudaStream_t stream)
+{
+    const long long rows = (long long)p.T * p.H;
+    if (rows * 8 <= 4ll * sms * (kCombineThreads / 32)) {
+        ink_combine_kernel<8, D><<<(unsigned)rows, kCombineThreads, 0, stream>>>(p);
+    } else {
+        const long long per = kCombineThreads / 32;
+        const long long grid = std::min<long long>((rows + per - 1) / per, 16ll * sms);
+        ink_combine_kernel<1, D><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
     }
 }
 
@@ -172,13 +214,11 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
 // sized for every row of the call; CTAs past the merge list the prepass wrote return at once.
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream)
 {
-    const long long rows = (long long)p.T * p.H;
-    if (rows * 8 <= 4ll * sms * (kCombineThreads / 32)) {
-        ink_combine_kernel<8><<<(unsigned)rows, kCombineThreads, 0, stream>>>(p);
-    } else {
-        const long long per = kCombineThreads / 32;
-        const long long grid = std::min<long long>((rows + per - 1) / per, 16ll * sms);
-        ink_combine_kernel<1><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
+    switch (p.D) {
+        case 64: launch_combine_d<64>(p, sms, stream); break;
+        case 128: launch_combine_d<128>(p, sms, stream); break;
+        case 256: launch_combine_d<256>(p, sms, stream); break;
+        default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 struct Params {
     // shapes
     int T, B, H, Hkv, G, NB, BS, MAXBLK, max_seqlen_q;
+    int D;  // head size: 128 on the tcgen05 prefill / decode path, 64 or 256 on the head-size-generic path
     // scalars
     float softmax_scale, scale_log2, inv_scale;
     int causal, wl, wr, E;
@@ -404,6 +405,7 @@ cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUten
                            size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_stage(const Params &p, int sms, cudaStream_t stream);
+cudaError_t launch_generic(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
                           void *value_cache, const int64_t *slot_mapping, uint32_t *flags, int sms,
                           cudaStream_t stream);

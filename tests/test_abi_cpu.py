@@ -81,7 +81,8 @@ def test_host_validation(lib, over, status):
 
 
 @pytest.mark.parametrize("dims_over,status", [
-    (dict(head_dim=64), 2), (dict(block_size=8), 2), (dict(block_size=24), 2),
+    (dict(head_dim=96), 2), (dict(head_dim=32), 2), (dict(head_dim=512), 2), (dict(block_size=8), 2),
+    (dict(block_size=24), 2),
     (dict(num_heads=6, num_kv_heads=4), 1), (dict(batch=0), 1), (dict(num_tokens=-1), 1),
 ])
 def test_unsupported_or_invalid_dims(lib, dims_over, status):
@@ -109,8 +110,8 @@ def test_append_host_validation(lib):
     assert f(ctypes.byref(dims), None, good, good, good, good, None, None) == 1          # null key
     assert f(ctypes.byref(dims), good, good, good, good, good + 4, None, None) == 1      # misaligned slots
     assert f(ctypes.byref(dims), good + 8, good, good, good, good, None, None) == 1      # misaligned key
-    bad = ink.Dims(8, 1, 4, 4, 64, 16, 16, 1)
-    assert f(ctypes.byref(bad), good, good, good, good, good, None, None) == 2           # head_dim 64
+    bad = ink.Dims(8, 1, 4, 4, 96, 16, 16, 1)
+    assert f(ctypes.byref(bad), good, good, good, good, good, None, None) == 2           # head_dim 96
     empty = ink.Dims(0, 1, 4, 4, 128, 16, 16, 1)
     assert f(ctypes.byref(empty), good, good, good, good, good, None, None) == 0         # nothing to do
 
@@ -160,3 +161,21 @@ def test_fp8_append_host_validation(lib):
     assert f(ctypes.byref(bad), good, good, good, good, good, 1.0, 1.0, None, None) == 2        # head_dim 256
     empty = ink.Dims(0, 1, 4, 4, 128, 16, 16, 1)
     assert f(ctypes.byref(empty), good, good, good, good, good, 1.0, 1.0, None, None) == 0     # nothing to do
+
+
+def test_head_sizes_64_and_256(lib):
+    """D = 64 and 256 are served (head-size-generic kernel): workspace sizes follow D, nothing is staged,
+    and an FP8 cache is refused at those sizes."""
+    sizes = {D: ink.workspace_size(_dims(head_dim=D), 128, 8) for D in (64, 128, 256)}
+    assert 0 < sizes[64] < sizes[256]
+    assert ink.stage_bytes(_dims(head_dim=64), 1000) == 0 and ink.stage_bytes(_dims(head_dim=256), 1000) == 0
+    assert ink.stage_bytes(_dims(head_dim=128), 1000) > 0
+    f = lib.ink_rel_attn_varlen_fp8kv
+    vp, fl, i32 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int32
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(ink.Dims), vp, vp, vp, fl, fl, vp, vp, vp, i32, fl, ctypes.c_int, i32, i32, i32,
+                  vp, i32, vp, vp, vp, ctypes.c_size_t, vp]
+    P = 4096
+    d = _dims(head_dim=64)
+    assert f(ctypes.byref(d), P, P, P, 1.0, 1.0, P, P, P, 128, 0.088, 1, -1, -1, 0, None, 0, P, None, P, 1 << 40,
+             None) == 2

@@ -92,13 +92,18 @@ def test_clock_sampler_summarises_polled_samples():
     assert s["reasons"] == ["sw_power_cap"]
 
 
-def test_cpu_baseline_repeats_passes_until_its_budget():
-    """The tiny mixed batch takes far less than the budget, so the baseline makes several full passes and
-    reports them; its value is the KV bytes of the requests it ran per second."""
+def test_cpu_baseline_splits_its_budget_between_decode_and_prefill():
+    """The tiny mixed batch has decode-shaped and prefill-shaped requests: the oracle runs whole decode
+    requests for half the budget and stratified prefill rows for the other half, and the line reports
+    both rates and the step time they imply."""
+    from workloads import workload
+
     r = bench.cpu_baseline("tiny_mix", 0.5)
-    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["cores"] >= 1
-    assert r["seconds"] >= 0.5
-    passes = int(r["sample"].split("(")[1].split(" full passes")[0])
-    reqs = int(r["sample"].split(" requests")[0])
-    assert passes >= 2 and reqs >= 3 * passes
-    assert r["value"] > 0
+    assert r["kind"] == "oracle" and r["cores"] >= 1 and r["seconds"] >= 0.5
+    assert r["unit"].startswith("ms per step")
+    assert r["decode_gbs"] > 0 and r["prefill_tflops"] > 0
+    assert "whole decode requests" in r["sample"] and "stratified prefill rows" in r["sample"]
+    kv, flops, _ = bench.work_of(workload("tiny_mix"))
+    implied = (kv / (r["decode_gbs"] * 1e9) + flops / (r["prefill_tflops"] * 1e12)) * 1e3
+    assert abs(implied - r["value"]) <= 0.01 * r["value"]
+

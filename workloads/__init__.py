@@ -155,6 +155,17 @@ PROFILE_WORKLOADS = {
 }
 
 
+# Head sizes 64 and 256 (the other sizes a paged backend serves): the decode batch's and the chunked
+# prefill's request lengths, at D = 64 with H 32, Hkv 8 and at D = 256 with H 24, Hkv 4 (G 6, the
+# PagedAttention V2 page's GQA example); seeds 1101 .. 1104.
+HEADDIM_WORKLOADS = {
+    "decode_batch_d64": "decode_batch lengths (64 decodes, Lk ~ U{1024..32768}), H 32, Hkv 8, D 64, E 1024",
+    "chunked_prefill_d64": "chunked_prefill lengths (4 x Lq 2048 on 0/2048/6144/14336), H 32, Hkv 8, D 64, E 4096",
+    "decode_batch_d256": "decode_batch lengths (64 decodes, Lk ~ U{1024..32768}), H 24, Hkv 4, D 256, E 1024",
+    "chunked_prefill_d256": "chunked_prefill lengths (4 x Lq 2048 on 0/2048/6144/14336), H 24, Hkv 4, D 256, E 4096",
+}
+
+
 def workload_lengths(name: str):
     """(q_lens, kv_lens) of a named workload, drawn from seed 1000 + index."""
     idx = WORKLOAD_ORDER.index(name)
@@ -186,6 +197,14 @@ def workload(name: str, device="cpu", **overrides) -> Case:
     if name == "chunked_prefill_quarter":
         return build_case(name, [2048], [8192], H=32, Hkv=8, E=4096, bias_std=0.5, seed=1002, device=device,
                           **overrides)
+    if name in HEADDIM_WORKLOADS:
+        base, d = name.rsplit("_d", 1)
+        D = int(d)
+        q, k = workload_lengths(base)
+        heads = dict(H=32, Hkv=8) if D == 64 else dict(H=24, Hkv=4)
+        extra = dict(E=1024) if base == "decode_batch" else dict(E=4096, bias_std=0.5)
+        seed = 1100 + list(HEADDIM_WORKLOADS).index(name) + 1
+        return build_case(name, q, k, D=D, seed=seed, device=device, **heads, **extra, **overrides)
     idx = WORKLOAD_ORDER.index(name)
     q_lens, kv_lens = workload_lengths(name)
     kw = dict(seed=1000 + idx, device=device)
