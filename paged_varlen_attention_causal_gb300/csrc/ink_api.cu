@@ -75,8 +75,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 struct Plan {
     int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0, bias_tok_log2 = 0;
-    int pf_kv_slots_bias = 3, pf_bias_slots = 3;  // prefill ring depths for calls with bias boxes
-    int pf_kv_slots_plain = 3;                     // ... and for calls without
     int S_dec = 1, S_pf = 1, chunk_dec = 1, chunk_pf = 1;
     int dec_rows = 0, lq_dec = 0;
     long long dec_cap = 0, pf_cap = 0, units_cap = 0;
@@ -151,12 +149,10 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     const int T = d->num_tokens, B = d->batch, H = d->num_heads, Hkv = d->num_kv_heads;
     pl.G = H / Hkv;
     pl.tpt = kTileRows / pl.G;
-    // prefill shared memory: a 3-slot K/V ring, and with bias boxes 3 bias stages holding as many
-    // tokens per box (up to 8) as the budget allows.  (Measured on the chunked prefill: K/V rings of
-    // 4 to 6 slots, with or without bias, and 4 slots with 2 bias stages are no faster.)
+    // prefill bias boxes: as many tokens per box (up to 8) as the shared-memory budget allows
     for (int lg = 3; lg >= 0; --lg) {
         if ((1 << lg) > pl.tpt) continue;
-        const size_t need = 1024 + pf_layout_bytes(pl.G, pl.tpt, 1 << lg, pl.pf_kv_slots_bias, pl.pf_bias_slots);
+        const size_t need = 1024 + pf_layout_bytes(pl.G, pl.tpt, 1 << lg);
         if (need <= kSmemLimit || lg == 0) {
             pl.bias_tok_log2 = lg;
             break;
@@ -558,11 +554,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
             pp.inv_scale = 1.0f / eff;
             pp.out_scale = kv.v_scale;
         }
-        pp.pf_kv_slots = pp.bias_tma ? pl.pf_kv_slots_bias : pl.pf_kv_slots_plain;
-        pp.pf_bias_slots = pp.bias_tma ? pl.pf_bias_slots : 0;
         // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
-        const size_t layout =
-            pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2, pp.pf_kv_slots, pp.pf_bias_slots);
+        const size_t layout = pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2);
         if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);

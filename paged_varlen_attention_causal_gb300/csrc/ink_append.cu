@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kAppendThreads)
                       uint4 *value_cache, const int64_t *__restrict__ slot_mapping, long long num_tokens,
                       int chunks_per_token, long long num_slots, uint32_t *flags)
 {
+    pdl_wait();  // the previous kernel of the stream may still be finishing
+    pdl_launch_dependents();
     const long long total = num_tokens * chunks_per_token;  // 16-byte chunks per tensor
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += stride) {
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kAppendThreads)
                           int chunks_per_token, long long num_slots, float k_scale, float v_scale, float k_rcp,
                           float v_rcp, uint32_t *flags)
 {
+    pdl_wait();  // the previous kernel of the stream may still be finishing
+    pdl_launch_dependents();
     const long long total = num_tokens * chunks_per_token;  // 16-byte bf16 chunks per tensor
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total; c += stride) {
@@ -105,11 +109,11 @@ cudaError_t launch_append_fp8(const ink_attn_dims *d, const void *key, const voi
     const long long total = (long long)d->num_tokens * chunks;
     const long long want = (total + kAppendThreads - 1) / kAppendThreads;
     const int grid = (int)(want < 8ll * sms ? (want > 0 ? want : 1) : 8ll * sms);
-    ink_append_fp8_kernel<<<grid, kAppendThreads, 0, stream>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
-        static_cast<uint2 *>(value_cache), slot_mapping, d->num_tokens, chunks,
-        (long long)d->num_blocks * d->block_size, k_scale, v_scale, 1.0f / k_scale, 1.0f / v_scale, flags);
-    return cudaGetLastError();
+    return launch_pdl(ink_append_fp8_kernel, (unsigned)grid, kAppendThreads, 0, stream,
+                      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                      static_cast<uint2 *>(key_cache), static_cast<uint2 *>(value_cache), slot_mapping,
+                      (long long)d->num_tokens, chunks, (long long)d->num_blocks * d->block_size, k_scale, v_scale,
+                      1.0f / k_scale, 1.0f / v_scale, flags);
 }
 
 cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,
@@ -121,11 +125,10 @@ cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *v
     // enough CTAs to fill every SM a few times over; each thread loops over its chunks
     const long long want = (total + kAppendThreads - 1) / kAppendThreads;
     const int grid = (int)(want < 8ll * sms ? (want > 0 ? want : 1) : 8ll * sms);
-    ink_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(key_cache),
-        static_cast<uint4 *>(value_cache), slot_mapping, d->num_tokens, chunks,
-        (long long)d->num_blocks * d->block_size, flags);
-    return cudaGetLastError();
+    return launch_pdl(ink_append_kernel, (unsigned)grid, kAppendThreads, 0, stream,
+                      static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                      static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
+                      (long long)d->num_tokens, chunks, (long long)d->num_blocks * d->block_size, flags);
 }
 
 }  // namespace ink

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
     __shared__ float s_acc[kWarpsPerRow > 1 ? kCombineThreads / 32 : 1][32][V];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = warp % kWarpsPerRow;  // this warp's share of the row's splits
+    pdl_wait();
+    pdl_launch_dependents();
     const long long nrows = (long long)*(volatile uint32_t *)&p.hdr->comb_tokens * p.H;
     // Grid-stride over the merge list; the trip count is the same for all warps of a CTA.
     for (long long row0 = (long long)blockIdx.x * kRowsPerCta; row0 < nrows; row0 += (long long)gridDim.x * kRowsPerCta) {
@@ -198,15 +200,15 @@ __global__ void __launch_bounds__(kCombineThreads) ink_combine_kernel(const Para
 }
 
 template <int D>
-void launch_combine_d(const Params &p, int sms, cudaStream_t stream)
+cudaError_t launch_combine_d(const Params &p, int sms, cudaStream_t stream)
 {
     const long long rows = (long long)p.T * p.H;
     if (rows * 8 <= 4ll * sms * (kCombineThreads / 32)) {
-        ink_combine_kernel<8, D><<<(unsigned)rows, kCombineThreads, 0, stream>>>(p);
+        return launch_pdl(ink_combine_kernel<8, D>, (unsigned)rows, kCombineThreads, 0, stream, p);
     } else {
         const long long per = kCombineThreads / 32;
         const long long grid = std::min<long long>((rows + per - 1) / per, 16ll * sms);
-        ink_combine_kernel<1, D><<<(unsigned)grid, kCombineThreads, 0, stream>>>(p);
+        return launch_pdl(ink_combine_kernel<1, D>, (unsigned)grid, kCombineThreads, 0, stream, p);
     }
 }
 
@@ -215,12 +217,11 @@ void launch_combine_d(const Params &p, int sms, cudaStream_t stream)
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream)
 {
     switch (p.D) {
-        case 64: launch_combine_d<64>(p, sms, stream); break;
-        case 128: launch_combine_d<128>(p, sms, stream); break;
-        case 256: launch_combine_d<256>(p, sms, stream); break;
+        case 64: return launch_combine_d<64>(p, sms, stream);
+        case 128: return launch_combine_d<128>(p, sms, stream);
+        case 256: return launch_combine_d<256>(p, sms, stream);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace ink

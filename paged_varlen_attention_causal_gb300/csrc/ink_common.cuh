@@ -81,8 +81,6 @@ struct Params {
     int fast_pack;       // prefill: warp-strided token packing (G divides 32)
     int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
     int bias_tok_log2;   // prefill: tokens per bias TMA box = 1 << bias_tok_log2
-    int pf_kv_slots;     // prefill: K/V ring depth (32 KB slots)
-    int pf_bias_slots;   // prefill: bias ring depth (half-tile stages; 0 without bias boxes)
 };
 
 // ---------------------------------------------------------------------------
@@ -162,8 +160,8 @@ __host__ __device__ __forceinline__ int stage_keys_of(int Lk) { return (Lk + kTi
 // token k + 1 starts one key later than token k's, so a common start rounded down to 16
 // bytes and a width of 64 + 3 + (nb - 1) floats, rounded up to 16 bytes, cover every token
 // of the box (the softmax reads 17 whole 16-byte chunks from the one holding a row's start).
-constexpr int kPfMaxKvSlots = 6;    // prefill K/V ring: 32 KB slots, as many as shared memory holds (up to 6)
-constexpr int kPfMaxBiasSlots = 3;  // prefill bias ring: half-tile stages (0 when the call has no bias boxes)
+constexpr int kPfKvSlots = 3;     // prefill K/V ring (32 KB slots; 4 to 6 slots measured no faster)
+constexpr int kPfBiasSlots = 3;   // prefill bias ring (half-tile stages)
 __host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (70 + nb) & ~3; }
 // Bytes a box transfers, and its shared-memory footprint (a TMA destination is 128-byte aligned).
 __host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb) { return nb * G * pf_bias_width(nb) * 4; }
@@ -174,9 +172,9 @@ __host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int 
     return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb);
 }
 // The prefill kernel's shared-memory layout: K/V ring, bias ring, bookkeeping.
-__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb, int kv_slots, int bias_slots)
+__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb)
 {
-    return (size_t)kv_slots * 32768 + (size_t)bias_slots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
+    return (size_t)kPfKvSlots * 32768 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
 }
 
 // Packed row of (token offset k, head j) inside a prefill tile, and back.
@@ -391,6 +389,32 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Programmatic dependent launch.  Every kernel of a call (and the KV append) is launched so that it
+// may begin while the kernel before it in the stream is finishing: its CTAs set up shared memory,
+// barriers and tensor memory, then pdl_wait() blocks until the previous kernel has completed and its
+// writes are visible -- before any global memory is read or written -- and pdl_launch_dependents()
+// lets the next kernel start its own set-up.  A kernel triggers only after its wait returns, so at
+// most two consecutive kernels of a stream overlap, and only in those set-up phases.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Host-side launchers, one per translation unit (ink_api.cu calls these).

@@ -179,6 +179,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // the work list and (for a staged call) the staging copy are complete
+    pdl_launch_dependents();
 
     if (warp == kDecComputeWarps) {
         // ------------------------------------------------------------ producer
@@ -909,9 +911,8 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kernel<<<grid, kDecThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias, nstages, stage_bytes, kv_bytes,
-                                                    bias_slot_bytes, k_scale, v_scale);
-        return cudaGetLastError();
+        return launch_pdl(kernel, (unsigned)grid, kDecThreads, smem, stream, p, tm_k, tm_v, tm_bias, nstages,
+                          stage_bytes, kv_bytes, bias_slot_bytes, k_scale, v_scale);
     };
     if (kv_fp8) {
         switch (8 / p.Hkv) {

@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kGenThreads, GenLayout<D>::kCtasPerSm) ink_gen
     auto s_v = [&](int buf) { return sbase + L::kQBytes + (2 * buf + 1) * L::kKvBytes; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    pdl_launch_dependents();
     const int total = (int)*(volatile uint32_t *)&p.hdr->pf_count;
     const float sl2 = p.scale_log2;
     const float log2e = 1.4426950408889634f;
@@ -316,8 +318,7 @@ cudaError_t launch_generic_d(const Params &p, int sms, cudaStream_t stream)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ink_generic_kernel<D>, kGenThreads, smem);
     if (e != cudaSuccess) return e;
     const long long grid = std::min<long long>((long long)sms * std::max(1, per_sm), std::max(1, p.pf_items_cap));
-    ink_generic_kernel<D><<<(unsigned)grid, kGenThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(ink_generic_kernel<D>, (unsigned)grid, kGenThreads, (size_t)smem, stream, p);
 }
 
 }  // namespace

@@ -10,15 +10,14 @@
 //   warp 0      page-gather producer: block_table entries are prefetched 32
 //               groups ahead; per 16-key page two TMA boxes of K (d halves,
 //               128-byte swizzle) and one 4-D box of V (both d halves) into
-//               a K/V ring of 32 KB slots, 3 to 6 deep as shared memory allows
-//               (a staged request: one 32 KB box per tile);
+//               a 3-slot K/V ring (a staged request: one 32 KB box per tile);
 //   warp 1      tensor-memory allocator and single-thread MMA issuer:
 //               S = Q K^T with Q read from tensor memory (M128 N128 K16 x 8),
 //               O += P V with P read from tensor memory (M128 N128 K16 x 8);
 //   warp 2      bias producer: per bias tile and key half one fp32 TMA box of
 //               rel_logits per 8 tokens (fewer when shared memory is short;
-//               out-of-range distances read as 0) into a ring of half-tile
-//               stages, each stage read by one softmax warpgroup;
+//               out-of-range distances read as 0) into a 3-stage ring of half
+//               tiles, each stage read by one softmax warpgroup;
 //   warps 4-11  online softmax in two warpgroups: warps 4-7 take keys 0-63 of
 //               every S tile, warps 8-11 keys 64-127 (thread = TMEM lane = row);
 //               each adds its half of the relative bias from the staged boxes
@@ -38,7 +37,9 @@ constexpr int kPfProducerRegs = 80;         // warpgroup 0 (warps 0-3) after set
 constexpr int kPfSoftmaxRegs = 208;        // warpgroups 1 and 2 (softmax) after setmaxnreg.inc
 static_assert(128 * kPfProducerRegs + 256 * kPfSoftmaxRegs <= kPfThreads * kPfLaunchRegs,
               "register split exceeds the launch allocation");
+constexpr int kKvSlots = kPfKvSlots;
 constexpr int kSSlots = 2;
+constexpr int kBiasSlots = kPfBiasSlots;      // half-tile bias stages
 constexpr int kSlotBytes = 32768;           // one K or V tile: 2 d halves x 128 rows x 128 B
 constexpr int kRescaleThreshold = 8;        // log2 units (factor 256)
 constexpr uint32_t kTmemCols = 512;         // S ring 2 x 128 | O 128 | Q 64 (bf16 pairs)
@@ -113,8 +114,8 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
         : "memory")
 
 struct PfShared {
-    uint64_t kv_full[kPfMaxKvSlots], kv_empty[kPfMaxKvSlots];
-    uint64_t bias_full[kPfMaxBiasSlots], bias_empty[kPfMaxBiasSlots];
+    uint64_t kv_full[kKvSlots], kv_empty[kKvSlots];
+    uint64_t bias_full[kBiasSlots], bias_empty[kBiasSlots];
     uint64_t q_full;
     uint64_t s_full[kSSlots], p_full[kSSlots], pv_done[kSSlots];
     uint64_t o_full;
@@ -222,35 +223,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    const int kv_slots = p.pf_kv_slots;      // K/V ring depth (32 KB slots)
-    const int bias_slots = p.pf_bias_slots;  // bias ring depth (half-tile stages)
-    uint8_t *kv_smem = base;                                  // kv_slots x 32 KB
-    uint8_t *bias_smem = kv_smem + kv_slots * kSlotBytes;     // bias_slots x (tpt x G rows of a key half)
+    uint8_t *kv_smem = base;                                  // kKvSlots x 32 KB
+    uint8_t *bias_smem = kv_smem + kKvSlots * kSlotBytes;     // kBiasSlots x (tpt x G rows of a key half)
     const int bias_nb = 1 << p.bias_tok_log2;  // tokens per bias box
     const int bias_w = pf_bias_width(bias_nb);   // floats per box row
     const int bias_box = pf_bias_box_stride(p.G, bias_nb);
     const int bias_stage = pf_bias_stage_bytes(p.G, p.tpt, bias_nb);
-    PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + bias_slots * bias_stage);
+    PfShared &sh = *reinterpret_cast<PfShared *>(bias_smem + kBiasSlots * bias_stage);
     volatile int *abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // The host requests at most the per-CTA limit, which leaves less than 1 KB for aligning
-    // the base when G = 1; if the window is too small after alignment, or the ring depths are
-    // outside what the barriers are sized for, do nothing (CTA-uniform).  The two softmax warpgroups
-    // consume alternate bias stages (key halves), so a bias ring needs at least two.
-    if ((uintptr_t)(reinterpret_cast<uint8_t *>(&sh + 1) - dsmem) > dynamic_smem_bytes() || kv_slots < 3 ||
-        kv_slots > kPfMaxKvSlots || bias_slots < (p.bias_tma ? 2 : 0) || bias_slots > kPfMaxBiasSlots) {
+    // the base when G = 1; if the window is too small after alignment, do nothing (CTA-uniform).
+    if ((uintptr_t)(reinterpret_cast<uint8_t *>(&sh + 1) - dsmem) > dynamic_smem_bytes()) {
+        pdl_wait();
         if (threadIdx.x == 0) report(p, INK_DEVERR_SMEM);
         return;
     }
-    const int total = (int)*(volatile uint32_t *)&p.hdr->pf_count;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kv_slots; ++s) {
+        for (int s = 0; s < kKvSlots; ++s) {
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 1);
         }
-        for (int s = 0; s < bias_slots; ++s) {
+        for (int s = 0; s < kBiasSlots; ++s) {
             mbar_init(&sh.bias_full[s], 1);
             mbar_init(&sh.bias_empty[s], kSoftmaxWarps / 2);
         }
@@ -277,6 +273,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();  // barriers and tensor memory are set up; now the work list, staging copy and inputs
+    pdl_launch_dependents();
+    const int total = (int)*(volatile uint32_t *)&p.hdr->pf_count;
     const uint32_t tmem = sh.tmem_base;
     const uint32_t tmem_o = tmem + kSSlots * 128;
     const uint32_t tmem_q = tmem_o + 128;
@@ -339,8 +338,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         key0 = sh.tile_keys[n % 4][lane & 7];
                     }
                     __syncwarp();
-                    const int slot = seq % kv_slots;
-                    if (!mbar_wait_warp(&sh.kv_empty[slot], ((seq / kv_slots) & 1) ^ 1, abort, p)) break;
+                    const int slot = seq % kKvSlots;
+                    if (!mbar_wait_warp(&sh.kv_empty[slot], ((seq / kKvSlots) & 1) ^ 1, abort, p)) break;
                     if (lane == 0) mbar_arrive_expect_tx(&sh.kv_full[slot], kSlotBytes);
                     __syncwarp();
                     if (so >= 0) {
@@ -367,8 +366,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         // let copies still in flight land before the CTA can exit
         if (lane == 0)
-            for (uint32_t k = (seq > kv_slots ? seq - kv_slots : 0); k < seq; ++k)
-                mbar_wait(&sh.kv_full[k % kv_slots], (k / kv_slots) & 1, abort, p);
+            for (uint32_t k = (seq > kKvSlots ? seq - kKvSlots : 0); k < seq; ++k)
+                mbar_wait(&sh.kv_full[k % kKvSlots], (k / kKvSlots) & 1, abort, p);
     } else if (warp == 2) {
         // ---------------------------------------------------------------- bias producer
         if (p.bias_tma) {
@@ -385,8 +384,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int nbox = (it.ntok + bias_nb - 1) >> p.bias_tok_log2;
                     // keys 64h .. 64h + 63 of the tile, read by softmax warpgroup h
                     for (int h = 0; h < 2; ++h) {
-                        const int bs = bseq % bias_slots;
-                        if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / bias_slots) & 1) ^ 1, abort, p)) {
+                        const int bs = bseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_empty[bs], ((bseq / kBiasSlots) & 1) ^ 1, abort, p)) {
                             stop = true;
                             break;
                         }
@@ -408,8 +407,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (*abort) break;
             }
             if (lane == 0)
-                for (uint32_t k = (bseq > bias_slots ? bseq - bias_slots : 0); k < bseq; ++k)
-                    mbar_wait(&sh.bias_full[k % bias_slots], (k / bias_slots) & 1, abort, p);
+                for (uint32_t k = (bseq > kBiasSlots ? bseq - kBiasSlots : 0); k < bseq; ++k)
+                    mbar_wait(&sh.bias_full[k % kBiasSlots], (k / kBiasSlots) & 1, abort, p);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -452,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             auto seq_v = [&](int m) { return seq + (m == it.ntiles - 1 ? (uint32_t)(2 * it.ntiles - 1) : (uint32_t)(2 * m + 2)); };
             auto issue_qk = [&](int n) {
                 const uint32_t t = tc0 + n, sq = seq_k(n);
-                const int ss = t % kSSlots, slot = sq % kv_slots;
+                const int ss = t % kSSlots, slot = sq % kKvSlots;
                 zero_tail(slot, n, false);
                 tc_fence_after();
                 if (lane == 0) {
@@ -472,7 +471,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             };
             auto issue_pv = [&](int m) {
                 const uint32_t t = tc0 + m, sq = seq_v(m);
-                const int ss = t % kSSlots, slot = sq % kv_slots;
+                const int ss = t % kSSlots, slot = sq % kKvSlots;
                 zero_tail(slot, m, true);
                 tc_fence_after();
                 if (lane == 0) {
@@ -501,7 +500,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 while (qk_todo || pv_todo) {
                     if (qk_todo) {
                         const uint32_t sq = seq_k(n);
-                        if (warp_poll(&sh.kv_full[sq % kv_slots], (sq / kv_slots) & 1)) {
+                        if (warp_poll(&sh.kv_full[sq % kKvSlots], (sq / kKvSlots) & 1)) {
                             issue_qk(n);
                             qk_todo = false;
                             continue;
@@ -510,7 +509,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (pv_todo) {
                         const uint32_t t = tc0 + n - 1, sq = seq_v(n - 1);
                         if (warp_poll(&sh.p_full[t % kSSlots], (t / kSSlots) & 1) &&
-                            warp_poll(&sh.kv_full[sq % kv_slots], (sq / kv_slots) & 1)) {
+                            warp_poll(&sh.kv_full[sq % kKvSlots], (sq / kKvSlots) & 1)) {
                             issue_pv(n - 1);
                             pv_todo = false;
                             continue;
@@ -636,8 +635,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (p.bias_tma) {
                         // the tile's two half stages are bias sequence numbers 2 bseq (keys 0-63) and 2 bseq + 1
                         const uint32_t hseq = 2 * bseq + h;
-                        const int bs = hseq % bias_slots;
-                        if (!mbar_wait_warp(&sh.bias_full[bs], (hseq / bias_slots) & 1, abort, p)) { ok = false; break; }
+                        const int bs = hseq % kBiasSlots;
+                        if (!mbar_wait_warp(&sh.bias_full[bs], (hseq / kBiasSlots) & 1, abort, p)) { ok = false; break; }
                         if (row_ok) {
                             const uint32_t box = box_row + bs * bias_stage;
                             switch (bo) {
@@ -816,8 +815,7 @@ cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUten
     if (fa.numRegs != kPfLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(ink_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    ink_prefill_kernel<<<grid, kPfThreads, smem, stream>>>(p, tm_k, tm_v, tm_bias, tm_ks, tm_vs);
-    return cudaGetLastError();
+    return launch_pdl(ink_prefill_kernel, (unsigned)grid, kPfThreads, smem, stream, p, tm_k, tm_v, tm_bias, tm_ks, tm_vs);
 }
 
 }  // namespace ink

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     int *unit_off = p.unit_off;
     int *comb_off = p.comb_off;
     const int tid = threadIdx.x;
+    pdl_wait();  // the previous kernel of the stream (e.g. the last call's merge, which reads this workspace)
+    pdl_launch_dependents();
 
     if (tid == 0) {
         p.hdr->errors = 0;
@@ -293,7 +295,8 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
 
 cudaError_t launch_prepass(const Params &p, cudaStream_t stream)
 {
-    ink_prepass_kernel<<<1, kPrepassThreads, 0, stream>>>(p);
+    const cudaError_t e = launch_pdl(ink_prepass_kernel, 1, kPrepassThreads, 0, stream, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

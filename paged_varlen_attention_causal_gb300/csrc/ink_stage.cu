@@ -42,6 +42,8 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint32_t lo, uint32_t hi)
 
 __global__ void __launch_bounds__(kStageThreads) ink_stage_kernel(const Params p)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int total = (int)*(volatile uint32_t *)&p.hdr->stage_pages;
     const int chunks = kKeyGroup * p.Hkv * (kHeadDim * 2 / 16);  // 16-byte chunks of one tensor's page
     for (int pg = blockIdx.x; pg < total; pg += gridDim.x) {
@@ -97,8 +99,7 @@ __global__ void __launch_bounds__(kStageThreads) ink_stage_kernel(const Params p
 // The grid covers every SM a few times; CTAs past the page list return at once.
 cudaError_t launch_stage(const Params &p, int sms, cudaStream_t stream)
 {
-    ink_stage_kernel<<<8 * sms, kStageThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(ink_stage_kernel, 8 * sms, kStageThreads, 0, stream, p);
 }
 
 }  // namespace ink
