@@ -529,7 +529,10 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         pd.bias_tma = bias_dec_tma ? 1 : 0;
         const int kv_bytes = Hkv * (kv.fp8 ? 2048 : 4096);  // one 16-key page of K (or V), all KV heads
         const int bias_slot = (H * 80 + 127) & ~127;
-        const int bias_bytes = (kDecodeRows / pl.G) * bias_slot;
+        // bias room for the most query tokens a decode-shaped request of this call can have (Lq <=
+        // max_seqlen_q, and Lq * G <= 16): with one token per request the stages are smaller and the ring
+        // holds more pages (an E4M3 decode batch: 6 stages instead of 5)
+        const int bias_bytes = pl.lq_dec * bias_slot;
         const int stage_bytes = (2 * kv_bytes + bias_bytes + 1023) & ~1023;
         int nst = (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
         nst = std::min(nst, kDecMaxStages);
