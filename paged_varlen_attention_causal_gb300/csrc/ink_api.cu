@@ -75,6 +75,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 struct Plan {
     int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0, bias_tok_log2 = 0;
+    bool pair = false;  // prefill units are pairs of q tiles for the 2-SM prefill kernel
     int S_dec = 1, S_pf = 1, chunk_dec = 1, chunk_pf = 1;
     int dec_rows = 0, lq_dec = 0;
     long long dec_cap = 0, pf_cap = 0, units_cap = 0;
@@ -183,6 +184,11 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     const long long sdec_eff = ceil_div(g_dec, pl.chunk_dec);
     const long long spf_eff = ceil_div(g_pf, pl.chunk_pf);
     pl.S_pf = (int)std::max(1ll, spf_eff);
+    // 2-SM prefill: unsplit prefill units become pairs of q tiles (the one-CTA prefill kernel keeps split
+    // units); a pair spans 2 tpt query positions, so its one chunk must cover the visible groups of that span
+    pl.pair = !generic && pl.any_prefill && pl.S_pf == 1 &&
+              pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2) + 1024 <= kSmemLimit;
+    if (pl.pair) pl.chunk_pf = (int)std::max(1ll, max_groups(d, 2 * pl.tpt, causal, wl, wr));
 
     pl.dec_cap = pl.any_decode ? (long long)B * sdec_eff : 0;
     pl.units_cap = pl.any_prefill ? ceil_div(T, pl.tpt) + B : 0;
@@ -424,6 +430,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.chunk_dec = pl.chunk_dec;
     p.chunk_pf = pl.chunk_pf;
     p.tpt = pl.tpt;
+    // 2-SM prefill: pairs of q tiles per cluster when the prefill units are not split
+    p.pair = pl.pair ? 1 : 0;
     p.fast_pack = pl.fast_pack;
     p.bias_tok_log2 = pl.bias_tok_log2;
     p.kv_fp8 = kv.fp8;
@@ -502,8 +510,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
 
     // staging planes as (64 d, keys, d half, Hkv): one (64, 128, 2, 1) box is a 128-key tile of one
     // KV head, 32 KB of consecutive bytes, landing as [d half][128 keys][128 B] (128-byte swizzle)
-    alignas(64) CUtensorMap tm_ks, tm_vs;
+    alignas(64) CUtensorMap tm_ks, tm_vs, tm_kh, tm_vh;
     memset(&tm_ks, 0, sizeof tm_ks); memset(&tm_vs, 0, sizeof tm_vs);
+    memset(&tm_kh, 0, sizeof tm_kh); memset(&tm_vh, 0, sizeof tm_vh);
     if (p.stage_cap > 0) {
         const cuuint64_t gds[4] = {64, (cuuint64_t)p.stage_cap, 2, (cuuint64_t)Hkv};
         const cuuint64_t gss[3] = {(cuuint64_t)kHeadDim * 2, 128, (cuuint64_t)p.stage_cap * kHeadDim * 2};
@@ -511,6 +520,13 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         if (!encode(&tm_ks, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.ks, gds, gss, boxs, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tm_vs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.vs, gds, gss, boxs, CU_TENSOR_MAP_SWIZZLE_128B))
             return INK_ERR_CUDA;
+        if (p.pair) {
+            // the 2-SM prefill's halves: 64 keys with both d halves (K), or one d half of 128 keys (V)
+            const cuuint32_t boxk[4] = {64, 64, 2, 1}, boxv[4] = {64, (cuuint32_t)kTileKeys, 1, 1};
+            if (!encode(&tm_kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.ks, gds, gss, boxk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode(&tm_vh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.vs, gds, gss, boxv, CU_TENSOR_MAP_SWIZZLE_128B))
+                return INK_ERR_CUDA;
+        }
     }
 
     // 1. device-side plan
@@ -562,8 +578,10 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);
-        if (timed_launch(INK_KERNEL_PREFILL, stream,
-                         [&] { return launch_prefill(pp, tm_k, tm_vp, tm_bpf, tm_ks, tm_vs, grid, smem, stream); }) != cudaSuccess)
+        if (timed_launch(INK_KERNEL_PREFILL, stream, [&] {
+                return p.pair ? launch_prefill_pair(pp, tm_k, tm_v, tm_bpf, tm_kh, tm_vh, pl.pf_cap, smem, stream)
+                              : launch_prefill(pp, tm_k, tm_vp, tm_bpf, tm_ks, tm_vs, grid, smem, stream);
+            }) != cudaSuccess)
             return INK_ERR_CUDA;
     }
 

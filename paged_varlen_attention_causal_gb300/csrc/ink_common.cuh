@@ -78,6 +78,7 @@ struct Params {
     int chunk_dec;       // 16-key groups per split for decode units
     int chunk_pf;        // 16-key groups per split for prefill units
     int tpt;             // prefill tokens per 128-row tile (128 / G)
+    int pair;            // prefill units are pairs of q tiles (2 tpt tokens) for the 2-SM prefill kernel
     int fast_pack;       // prefill: warp-strided token packing (G divides 32)
     int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
     int bias_tok_log2;   // prefill: tokens per bias TMA box = 1 << bias_tok_log2
@@ -427,6 +428,9 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_bias, const CUtensorMap &tm_ks, const CUtensorMap &tm_vs, int grid,
                            size_t smem, cudaStream_t stream);
+cudaError_t launch_prefill_pair(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                const CUtensorMap &tm_bias, const CUtensorMap &tm_kh, const CUtensorMap &tm_vh,
+                                long long max_pairs, size_t smem, cudaStream_t stream);
 cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_stage(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_generic(const Params &p, int sms, cudaStream_t stream);

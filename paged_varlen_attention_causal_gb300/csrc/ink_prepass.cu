@@ -75,7 +75,8 @@ __device__ long long block_exclusive_scan_ll(long long v, long long *out, long l
 
 __device__ __forceinline__ void pf_unit_of(const Params &p, const Req &r, int qt, int &qa0, int &qa1)
 {
-    const int i0 = qt * p.tpt, i1 = min(r.Lq, i0 + p.tpt) - 1;
+    const int ut = p.pair ? 2 * p.tpt : p.tpt;  // tokens per unit: one q tile, or a pair for the 2-SM prefill
+    const int i0 = qt * ut, i1 = min(r.Lq, i0 + ut) - 1;
     qa0 = i0 + r.Lk - r.Lq;
     qa1 = i1 + r.Lk - r.Lq;
 }
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     __shared__ int warp_sums[32];
     __shared__ int bucket_count[kCostBuckets];
     __shared__ int bucket_base[kCostBuckets];
-    __shared__ int s_carry[3];
+    __shared__ int s_carry[4];
     __shared__ long long warp_sums_ll[32];
     __shared__ long long s_stg_carry;
     __shared__ int s_pg_carry;
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         p.hdr->dec_next = 0;
         p.hdr->pf_next = 0;
         p.hdr->comb_tokens = 0;
-        s_carry[0] = s_carry[1] = s_carry[2] = 0;
+        s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
         s_stg_carry = 0;
         s_pg_carry = 0;
         p.hdr->stage_pages = 0;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     uint32_t my_err = 0;
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + tid;
-        int ndec = 0, nq = 0, nc = 0;
+        int ndec = 0, nq = 0, nc = 0, ntile = 0;  // ntile: q tiles of tpt tokens, for the budget check
         if (b < p.B) {
             Req r = load_req(p, b);
             my_err |= r.err;
@@ -183,16 +184,19 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
                     // an FP8 cache is read by the prefill only through the staging copy
                     my_err |= INK_DEVERR_STAGE;
                 } else {
-                    nq = (r.Lq + p.tpt - 1) / p.tpt;
+                    const int ut = p.pair ? 2 * p.tpt : p.tpt;
+                    nq = (r.Lq + ut - 1) / ut;
+                    ntile = (r.Lq + p.tpt - 1) / p.tpt;
                     nc = p.S_pf > 1 ? r.Lq : 0;
                 }
                 if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
             }
         }
-        int xd, xq, xc;
+        int xd, xq, xc, xt;
         const int td = block_exclusive_scan(ndec, &xd, warp_sums);
         const int tq = block_exclusive_scan(nq, &xq, warp_sums);
         const int tcb = block_exclusive_scan(nc, &xc, warp_sums);
+        const int tt = block_exclusive_scan(ntile, &xt, warp_sums);
         if (b < p.B) {
             dec_off[b] = s_carry[0] + xd;
             unit_off[b] = s_carry[1] + xq;
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
             s_carry[0] += td;
             s_carry[1] += tq;
             s_carry[2] += tcb;
+            s_carry[3] += tt;
         }
         __syncthreads();
     }
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         // Requests whose token ranges overlap (a cu_seqlens_q entry that steps back between valid
         // neighbours) can need more q tiles than T tokens allow, and the prefill partials are sized
         // for T: such a batch is flagged and runs nothing.
-        s_overflow = s_carry[1] > p.units_cap;
+        s_overflow = s_carry[3] > p.units_cap;  // counted in single q tiles, whichever kernel runs them
         if (s_overflow) s_err |= INK_DEVERR_CU_SEQLENS;
         p.hdr->comb_tokens = s_overflow ? 0u : (uint32_t)s_carry[2];
     }
