@@ -144,6 +144,7 @@ struct PfItem {
     int gb, ge, nact;    // 16-key groups of the split, splits of the unit
     int ntiles;          // 128-key tiles (8 groups each) of the split
     int lo_max, hi_min;  // keys visible to every valid row (inside the split)
+    int rot;             // processing order: tile n of the loop is tile (n + rot) mod ntiles of the split
 };
 
 __device__ __forceinline__ PfItem pf_item(const Params &p, int4 v)
@@ -164,10 +165,16 @@ __device__ __forceinline__ PfItem pf_item(const Params &p, int4 v)
     visible_range(it.qa_min, it.qa_min, it.Lk, p.causal, p.wl, p.wr, t, hi);
     it.lo_max = max(lo, it.gb * kKeyGroup);
     it.hi_min = min(hi, it.ge * kKeyGroup - 1);
+    it.rot = 0;
     return it;
 }
 
-__device__ __forceinline__ int pf_tile_key0(const PfItem &it, int n) { return (it.gb + 8 * n) * kKeyGroup; }
+// First key of the tile the loop handles at step n (the online softmax is the same in any tile order).
+__device__ __forceinline__ int pf_tile_key0(const PfItem &it, int n)
+{
+    const int m = n + it.rot;
+    return (it.gb + 8 * (m < it.ntiles ? m : m - it.ntiles)) * kKeyGroup;
+}
 
 __device__ __forceinline__ bool pf_tile_bias(const Params &p, const PfItem &it, int n)
 {
@@ -962,6 +969,14 @@ __device__ __forceinline__ PfItem pr_item(const Params &p, int4 v, int rank)
         it.lo_max = 0x7fffffff;
         it.hi_min = -1;
     }
+    // Items start their tiles at different offsets, so that the clusters running at any moment do not all
+    // stream their bias band (the last tiles before the diagonal) from HBM at the same time.  The offset is
+    // a function of the item alone (which cluster takes an item varies between calls; the result must
+    // not, and it is the same whether the item reads the staging copy or the pages).  Only long items (48
+    // tiles or more: the band is then a distinct tail; on the window-limited items of a continuous batch
+    // rotating costs time).
+    const unsigned h = ((unsigned)it.b * 131u + (unsigned)v.y * 17u + (unsigned)it.g * 7u + (unsigned)it.s) * 37u;
+    it.rot = it.ntiles >= 48 ? (int)(h % (unsigned)it.ntiles) : 0;
     return it;
 }
 
@@ -1056,17 +1071,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (it.ntiles == 0) continue;
             const int so = p.stage_cap > 0 ? __ldg(p.stg_off + it.b) : -1;
             const int32_t *bt_row = p.bt + (size_t)it.b * p.MAXBLK;
-            auto load_keys = [&](int chunk) {  // key coordinate of group gb + 32 chunk + lane (-16: zero fill)
-                const int gi = it.gb + 32 * chunk + lane;
+            // key coordinate of page (lane & 7) of the tile whose first key is j0 (-16, i.e. zero fill, past the
+            // split or on a bad page)
+            auto page_key_of = [&](int j0) {
+                const int gi = j0 / kKeyGroup + (lane & 7);
                 int key = -kKeyGroup;
                 if (gi < it.ge) {
                     const int pid = __ldg(bt_row + (gi * kKeyGroup) / p.BS);
                     if (pid >= 0 && pid < p.NB) key = pid * p.BS + (gi * kKeyGroup) % p.BS;
-                    else report(p, INK_DEVERR_PAGE_ID);
+                    else if (lane < 8) report(p, INK_DEVERR_PAGE_ID);
                 }
                 return key;
             };
-            int keys_cur = so >= 0 ? 0 : load_keys(0), keys_nxt = so >= 0 ? 0 : load_keys(1), chunk = 0;
             for (int step = 0; step <= it.ntiles; ++step) {
                 for (int which = 0; which < 2; ++which) {
                     int n, isV;
@@ -1076,12 +1092,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     int page_key = 0;  // paged: key coordinate of page (lane & 7) of tile n
                     if (so < 0) {
                         if (!isV) {
-                            while (chunk < n / 4) {
-                                keys_cur = keys_nxt;
-                                ++chunk;
-                                keys_nxt = load_keys(chunk + 1);
-                            }
-                            page_key = __shfl_sync(0xffffffffu, keys_cur, (n % 4) * 8 + (lane & 7));
+                            page_key = page_key_of(pf_tile_key0(it, n));
                             if (lane < 8) sh.tile_keys[n % 4][lane] = page_key;
                         } else {
                             page_key = sh.tile_keys[n % 4][lane & 7];
