@@ -130,6 +130,7 @@ struct PfShared {
     int32_t tile_keys[4][8];  // producer's record of recent tiles' key coordinates (reused by V)
     uint32_t tmem_base;
     int abort;
+    uint32_t mma_tiles;  // tiles whose MMAs were issued for this CTA (set by warp 1 at its end)
     float xchg[2][2][kTileRows];  // [buffer][key half][row]: partial row maxima, then row sums
 };
 static_assert(sizeof(PfShared) <= kPfSharedBytes, "prefill bookkeeping exceeds its shared-memory budget");
@@ -207,6 +208,20 @@ __device__ __forceinline__ bool pf_row(const Params &p, int L, int &k, int &j)
 __device__ __forceinline__ int pf_item_index(int r)
 {
     return r * gridDim.x + ((r & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x);
+}
+
+// Every PV commit arrives on a pv_done barrier, which the softmax waits on only
+// when it rescales O; the final phase of each slot (the CTA's last two tiles) is
+// awaited here before teardown, so that no arrival is still pending when the
+// CTA exits.  Called once every softmax warp has passed its last o_full wait: by
+// then no slot is more than one phase short of its final one, which is what the
+// parity waits need.
+template <typename Wait>
+__device__ __forceinline__ void drain_pv_done(uint64_t *pv_done, uint32_t ntiles, Wait wait)
+{
+    static_assert(kSSlots == 2, "one final phase per slot: tiles ntiles - 1 and ntiles - 2");
+    if (ntiles >= 1 && wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1) && ntiles >= 2)
+        wait(&pv_done[ntiles & 1], ((ntiles - 2) >> 1) & 1);
 }
 
 // One key half (64 columns) of a row's relative bias, added to its raw scores:
@@ -546,6 +561,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ++qseq;
             if (!ok) break;
         }
+        if (lane == 0) sh.mma_tiles = tc;
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfSoftmaxRegs));
@@ -811,6 +827,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (warp == 1 && !*abort)
+        drain_pv_done(sh.pv_done, sh.mma_tiles, [&](uint64_t *b, uint32_t par) { return mbar_wait_warp(b, par, abort, p); });
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -853,6 +871,7 @@ struct PrShared {
     int32_t tile_keys[4][8];
     uint32_t tmem_base;
     int abort;
+    uint32_t mma_tiles;  // tiles of this CTA's items (set by warp 1 at its end)
     float xchg[2][2][kTileRows];
 };
 static_assert(sizeof(PrShared) <= kPfSharedBytes, "pair bookkeeping exceeds its shared-memory budget");
@@ -1306,6 +1325,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ++qseq;
             if (!ok) break;
         }
+        if (lane == 0) sh.mma_tiles = tc;
+    } else if (warp == 1) {
+        // rank 1: the commits of rank 0's MMAs also arrive here; count the pair's tiles for the drain
+        uint32_t n = 0;
+        for (int r = 0;; ++r) {
+            const int idx = pr_item_index(r);
+            if (idx >= total) break;
+            n += (uint32_t)pr_item(p, p.pf_items[idx], rank).ntiles;
+        }
+        if (lane == 0) sh.mma_tiles = n;
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPrSoftmaxRegs));
@@ -1571,6 +1600,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (warp == 1 && !*abort)
+        drain_pv_done(sh.pv_done, sh.mma_tiles,
+                      [&](uint64_t *b, uint32_t par) { return mbar_wait_warp_cl(b, par, abort, p); });
     cluster_sync();  // neither CTA frees tensor memory or exits while its peer may still use the pair's
     tc_fence_after();
     if (warp == 1) {
