@@ -74,7 +74,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 struct Plan {
-    int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0, bias_tok_log2 = 0;
+    int G = 0, tpt = 0, fast_pack = 0, decode_kernel = 0, bias_tok_log2 = 0, bias_w = 0;
     bool pair = false;  // prefill units are pairs of q tiles for the 2-SM prefill kernel
     int S_dec = 1, S_pf = 1, chunk_dec = 1, chunk_pf = 1;
     int dec_rows = 0, lq_dec = 0;
@@ -144,6 +144,41 @@ int heuristic_splits_prefill(long long units, long long groups, int sms)
     return (int)std::max(1ll, s);
 }
 
+// Shared-memory wavefronts of the softmax's 16-byte bias loads (one load instruction of each of the four
+// lane quarters), for the worst start phase of a box: each 8-lane phase of a 128-bit load takes as many
+// wavefronts as the most 16-byte chunks it has in one bank group (address / 16 mod 8).  Rows follow the
+// kernels' packing (pf_row) and box layout: the row of token k, head j starts ((k mod nb) G + j) w floats
+// into box k / nb, plus whole chunks for the token's shift inside the box.
+int bias_load_waves(int G, int tpt, int fast_pack, int nb, int w)
+{
+    const int wc = w / 4, box_chunks = pf_bias_box_stride(G, nb, w) / 16;
+    int worst = 0;
+    for (int c0 = 0; c0 < 4; ++c0) {
+        int tot = 0;
+        for (int q = 0; q < 4; ++q)
+            for (int ph = 0; ph < 4; ++ph) {
+                int cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0}, mx = 0;
+                for (int l = 8 * ph; l < 8 * ph + 8; ++l) {
+                    int k, j;
+                    if (fast_pack) {
+                        k = 4 * (l / G) + q;
+                        j = l % G;
+                    } else {
+                        k = (32 * q + l) / G;
+                        j = (32 * q + l) % G;
+                    }
+                    if (k >= tpt) continue;
+                    const int kb = k / nb, ki = k % nb, ckb = (c0 + kb * nb) & 3;
+                    const int off = kb * box_chunks + (ki * G + j) * wc + ((ki + ckb) >> 2);
+                    mx = std::max(mx, ++cnt[off & 7]);
+                }
+                tot += mx;
+            }
+        worst = std::max(worst, tot);
+    }
+    return worst;
+}
+
 bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int causal, int wl, int wr, int sms,
                Plan &pl)
 {
@@ -153,12 +188,13 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     // prefill bias boxes: as many tokens per box (up to 8) as the shared-memory budget allows
     for (int lg = 3; lg >= 0; --lg) {
         if ((1 << lg) > pl.tpt) continue;
-        const size_t need = 1024 + pf_layout_bytes(pl.G, pl.tpt, 1 << lg);
+        const size_t need = 1024 + pf_layout_bytes(pl.G, pl.tpt, 1 << lg, pf_bias_width(1 << lg));
         if (need <= kSmemLimit || lg == 0) {
             pl.bias_tok_log2 = lg;
             break;
         }
     }
+    pl.bias_w = pf_bias_width(1 << pl.bias_tok_log2);
     const bool generic = d->head_dim != kHeadDim;  // head-size-generic kernel: every request as 128-row items
     pl.fast_pack = (!generic && 32 % pl.G == 0) ? 1 : 0;
     pl.decode_kernel = !generic && (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
@@ -186,9 +222,29 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     pl.S_pf = (int)std::max(1ll, spf_eff);
     // 2-SM prefill: unsplit prefill units become pairs of q tiles (the one-CTA prefill kernel keeps split
     // units); a pair spans 2 tpt query positions, so its one chunk must cover the visible groups of that span
-    pl.pair = !generic && pl.any_prefill && pl.S_pf == 1 &&
-              pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2) + 1024 <= kSmemLimit;
-    if (pl.pair) pl.chunk_pf = (int)std::max(1ll, max_groups(d, 2 * pl.tpt, causal, wl, wr));
+    // Its bias boxes: the shape (tokens per box, row width) with the fewest shared-memory wavefronts for
+    // the softmax's loads, then the smallest stage, then the most tokens per box, among those that fit.
+    int pr_lg = -1, pr_w = 0, pr_waves = 0, pr_stage = 0;
+    if (!generic && pl.any_prefill && pl.S_pf == 1) {
+        for (int lg = 3; lg >= 0; --lg) {
+            const int nb = 1 << lg;
+            if (nb > pl.tpt) continue;
+            for (int w = pf_bias_width(nb); w <= pf_bias_width(nb) + 32; w += 4) {
+                if (pr_layout_bytes(pl.G, pl.tpt, nb, w) + 1024 > kSmemLimit) break;
+                const int wv = bias_load_waves(pl.G, pl.tpt, pl.fast_pack, nb, w);
+                const int st = pf_bias_stage_bytes(pl.G, pl.tpt, nb, w);
+                if (pr_lg < 0 || wv < pr_waves || (wv == pr_waves && st < pr_stage)) {
+                    pr_lg = lg, pr_w = w, pr_waves = wv, pr_stage = st;
+                }
+            }
+        }
+    }
+    pl.pair = pr_lg >= 0;
+    if (pl.pair) {
+        pl.bias_tok_log2 = pr_lg;
+        pl.bias_w = pr_w;
+        pl.chunk_pf = (int)std::max(1ll, max_groups(d, 2 * pl.tpt, causal, wl, wr));
+    }
 
     pl.dec_cap = pl.any_decode ? (long long)B * sdec_eff : 0;
     pl.units_cap = pl.any_prefill ? ceil_div(T, pl.tpt) + B : 0;
@@ -434,6 +490,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.pair = pl.pair ? 1 : 0;
     p.fast_pack = pl.fast_pack;
     p.bias_tok_log2 = pl.bias_tok_log2;
+    p.bias_w = pl.bias_w;
     p.kv_fp8 = kv.fp8;
     p.out_scale = 1.f;
 
@@ -502,7 +559,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
             bias_dec_tma = encode(&tm_bdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box,
                                   CU_TENSOR_MAP_SWIZZLE_NONE);
         }
-        const cuuint32_t box2[3] = {(cuuint32_t)pf_bias_width(1 << pl.bias_tok_log2), (cuuint32_t)pl.G,
+        const cuuint32_t box2[3] = {(cuuint32_t)pl.bias_w, (cuuint32_t)pl.G,
                                     (cuuint32_t)(1 << pl.bias_tok_log2)};
         bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
                              CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -574,7 +631,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
             pp.out_scale = kv.v_scale;
         }
         // layout plus up to 1 KB for aligning the base (the kernel checks what it was given)
-        const size_t layout = pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2);
+        const size_t layout = p.pair ? pr_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2, pl.bias_w)
+                                     : pf_layout_bytes(pl.G, pl.tpt, 1 << pl.bias_tok_log2, pl.bias_w);
         if (layout > kSmemLimit) return INK_ERR_UNSUPPORTED;
         const size_t smem = std::min(layout + 1024, kSmemLimit);
         const int grid = (int)std::min<long long>(sms, pl.pf_cap);

@@ -82,6 +82,7 @@ struct Params {
     int fast_pack;       // prefill: warp-strided token packing (G divides 32)
     int bias_tma;        // prefill: bias staged by TMA (E % 4 == 0)
     int bias_tok_log2;   // prefill: tokens per bias TMA box = 1 << bias_tok_log2
+    int bias_w;          // prefill: floats per bias box row (at least pf_bias_width of the box's tokens)
 };
 
 // ---------------------------------------------------------------------------
@@ -164,18 +165,29 @@ __host__ __device__ __forceinline__ int stage_keys_of(int Lk) { return (Lk + kTi
 constexpr int kPfKvSlots = 3;     // prefill K/V ring (32 KB slots; 4 to 6 slots measured no faster)
 constexpr int kPfBiasSlots = 3;   // prefill bias ring (half-tile stages)
 __host__ __device__ __forceinline__ int pf_bias_width(int nb) { return (70 + nb) & ~3; }
-// Bytes a box transfers, and its shared-memory footprint (a TMA destination is 128-byte aligned).
-__host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb) { return nb * G * pf_bias_width(nb) * 4; }
-__host__ __device__ __forceinline__ int pf_bias_box_stride(int G, int nb) { return (pf_bias_box_bytes(G, nb) + 127) & ~127; }
-// One stage: the boxes of a q tile of tpt tokens, for one key half.
-__host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int nb)
+// Bytes a box of w-float rows transfers, and its shared-memory footprint (a TMA destination is
+// 128-byte aligned).  A wider row than the minimum changes where the rows fall among the shared-memory
+// banks (the host picks the width).
+__host__ __device__ __forceinline__ int pf_bias_box_bytes(int G, int nb, int w) { return nb * G * w * 4; }
+__host__ __device__ __forceinline__ int pf_bias_box_stride(int G, int nb, int w)
 {
-    return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb);
+    return (pf_bias_box_bytes(G, nb, w) + 127) & ~127;
+}
+// One stage: the boxes of a q tile of tpt tokens, for one key half.
+__host__ __device__ __forceinline__ int pf_bias_stage_bytes(int G, int tpt, int nb, int w)
+{
+    return (tpt + nb - 1) / nb * pf_bias_box_stride(G, nb, w);
 }
 // The prefill kernel's shared-memory layout: K/V ring, bias ring, bookkeeping.
-__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb)
+__host__ __device__ __forceinline__ size_t pf_layout_bytes(int G, int tpt, int nb, int w)
 {
-    return (size_t)kPfKvSlots * 32768 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb) + kPfSharedBytes;
+    return (size_t)kPfKvSlots * 32768 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb, w) + kPfSharedBytes;
+}
+// The 2-SM prefill kernel's: a ring of 16 KB K/V halves, then the same bias ring and bookkeeping.
+constexpr int kPrKvSlots = 4;
+__host__ __device__ __forceinline__ size_t pr_layout_bytes(int G, int tpt, int nb, int w)
+{
+    return (size_t)kPrKvSlots * 16384 + (size_t)kPfBiasSlots * pf_bias_stage_bytes(G, tpt, nb, w) + kPfSharedBytes;
 }
 
 // Packed row of (token offset k, head j) inside a prefill tile, and back.
@@ -390,6 +402,42 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Blackwell's three-input maximum and paired fp32 arithmetic (each lane of a pair rounds as the scalar op).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi) for a = (lo, hi)
+__device__ __forceinline__ void fma_x2(float &lo, float &hi, uint64_t b, uint64_t c)
+{
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%0, %1};\n\tfma.rn.f32x2 t, t, %2, %3;\n\tmov.b64 {%0, %1}, t;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "l"(b), "l"(c));
+}
+
+// acc += (lo, hi), lane by lane
+__device__ __forceinline__ void add_x2(uint64_t &acc, float lo, float hi)
+{
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tadd.rn.f32x2 %0, %0, t;\n\t}" : "+l"(acc) : "f"(lo), "f"(hi));
+}
+
+__device__ __forceinline__ float sum_x2(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
 }
 
 // Programmatic dependent launch.  Every kernel of a call (and the KV append) is launched so that it
