@@ -695,17 +695,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         if (key < lo || key > hi) sv[c] = __float_as_uint(-INFINITY);
                     }
                 }
-                // this half's maximum: eight independent chains, then a tree (max is exact in any order)
-                float mxs[8];
+                // this half's maximum: a tree of three-input maxima (max is exact in any order)
+                float m21[22];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mxs[e] = __uint_as_float(sv[e]);
+                for (int i = 0; i < 21; ++i)
+                    m21[i] = fmax3(__uint_as_float(sv[3 * i]), __uint_as_float(sv[3 * i + 1]), __uint_as_float(sv[3 * i + 2]));
+                m21[21] = __uint_as_float(sv[63]);
+                float m7[8];
 #pragma unroll
-                for (int c = 8; c < 64; c += 8) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mxs[e] = fmaxf(mxs[e], __uint_as_float(sv[c + e]));
-                }
-                float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                 fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+                for (int i = 0; i < 7; ++i) m7[i] = fmax3(m21[3 * i], m21[3 * i + 1], m21[3 * i + 2]);
+                m7[7] = m21[21];
+                float mx = fmax3(fmax3(m7[0], m7[1], m7[2]), fmax3(m7[3], m7[4], m7[5]), fmaxf(m7[6], m7[7]));
                 // Both halves now hold their S values in registers, so either may overwrite the slot.
                 float mx_other;
                 if (!exchange(mx, mx_other)) { ok = false; break; }
@@ -740,16 +740,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                 }
                 const float moff = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+                const uint64_t sl2x2 = f32x2(sl2, sl2), nmoff2 = f32x2(-moff, -moff);
                 uint32_t pk[32];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
+                uint64_t ls2[2] = {0ull, 0ull};  // four independent partial sums, as two pairs
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * c]), sl2, -moff));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -moff));
-                    ls[c & 3] += p0 + p1;
+                    float x0 = __uint_as_float(sv[2 * c]), x1 = __uint_as_float(sv[2 * c + 1]);
+                    fma_x2(x0, x1, sl2x2, nmoff2);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    add_x2(ls2[c & 1], p0, p1);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l += sum_x2(ls2[0]) + sum_x2(ls2[1]);
                 // P of keys 64h .. 64h + 63 as bf16 pairs: columns 32h .. 32h + 31 of the slot
                 INK_TMEM_ST32(tmem + lane_addr + ss * 128 + 32 * h, pk);
                 tc_wait_st();
