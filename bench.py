@@ -197,6 +197,16 @@ def _device_uuid(index: int) -> Optional[str]:
     return u if u.startswith("GPU-") else "GPU-" + u
 
 
+def hold_stream(stream, ms: float = 20.0):
+    """Queue a bounded spin kernel (torch's) ahead of a timed region, so that the host enqueues the region's
+    launches while the GPU is still busy: a stall of the launching thread (the clock sampler's thread holding
+    the interpreter lock, say) then leaves no idle gap between the timed kernels."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 1e-3 * 2.1e9))  # cycles, at about the maximum SM clock
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled while the timed region runs.
 
@@ -367,6 +377,7 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(local_rank) as clk:
+            hold_stream(stream)
             start.record(stream)
             for k in range(steps):
                 call(case, out, lse)
@@ -510,6 +521,7 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(local_rank) as clk:
+            hold_stream(stream)
             start.record(stream)
             for k in range(steps):
                 ink.set_timing_events("append", kev[k][0], kev[k][1])
@@ -547,6 +559,7 @@ def run_ours(args, rank, world, local_rank):
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier()
             torch.cuda.synchronize(dev)
+            hold_stream(stream)
             start.record(stream)
             for k in range(steps):  # the step time, nothing recorded between the kernels
                 call(case, out, lse, splits)
@@ -605,7 +618,7 @@ def run_ours(args, rank, world, local_rank):
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier()
             torch.cuda.synchronize(dev)
-            start.record(stream)
+            start.record(stream)  # no hold here: the host's own launch cost is part of what this compares
             for _ in range(steps):
                 fn()
             end.record(stream)
