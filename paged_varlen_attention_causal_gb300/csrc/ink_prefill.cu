@@ -946,6 +946,20 @@ __device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         : "memory");
 }
 
+// The same with the B descriptor's address field advanced by OFF (bytes / 16) inside the instruction's own
+// block, so that the compiler keeps one descriptor per tile rather than eight.
+template <uint32_t OFF>
+__device__ __forceinline__ void mma2_ts_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+        "add.s64 bd, %2, %5;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(acc), "n"((unsigned long long)OFF)
+        : "memory");
+}
+
 // Arrive on the barrier at this offset in both CTAs once the MMAs issued so far are complete.
 __device__ __forceinline__ void mma2_commit_both(uint64_t *bar)
 {
@@ -1260,12 +1274,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int ss = t % kSSlots, slot = sq % kPrKvSlots;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t kaddr = smem_u32(kv_smem + slot * kPrSlotBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // d 16 kk .. : d half kk / 4, 32-byte step kk % 4
-                        const uint64_t bdesc = smem_desc(kaddr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                        mma2_ts(tmem + ss * 128, tmem_q + kk * 8, bdesc, kIdescQK2, kk > 0 ? 1u : 0u);
-                    }
+                    // one descriptor for the slot; the k steps add their byte offset / 16 to its address field
+                    const uint64_t bdesc0 = smem_desc(smem_u32(kv_smem + slot * kPrSlotBytes), 16, 1024);
+                    const uint32_t sd = tmem + ss * 128;  // d 16 kk ..: d half kk / 4, 32-byte step kk % 4
+                    mma2_ts_off<0>(sd, tmem_q + 0, bdesc0, kIdescQK2, 0u);
+                    mma2_ts_off<2>(sd, tmem_q + 8, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<4>(sd, tmem_q + 16, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<6>(sd, tmem_q + 24, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<512>(sd, tmem_q + 32, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<514>(sd, tmem_q + 40, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<516>(sd, tmem_q + 48, bdesc0, kIdescQK2, 1u);
+                    mma2_ts_off<518>(sd, tmem_q + 56, bdesc0, kIdescQK2, 1u);
                     mma2_commit_both(&sh.s_full[ss]);
                     mma2_commit_both(&sh.kv_empty[slot]);
                 }
@@ -1276,12 +1295,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int ss = t % kSSlots, slot = sq % kPrKvSlots;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t vaddr = smem_u32(kv_smem + slot * kPrSlotBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // keys 16 kk ..: 8-key groups 1 KB apart
-                        const uint64_t bdesc = smem_desc(vaddr + kk * 2048, 16384, 1024);
-                        mma2_ts(tmem_o, tmem + ss * 128 + kk * 8, bdesc, kIdescPV2, (m > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    const uint64_t bdesc0 = smem_desc(smem_u32(kv_smem + slot * kPrSlotBytes), 16384, 1024);
+                    const uint32_t pa = tmem + ss * 128;  // keys 16 kk ..: 8-key groups 1 KB apart
+                    mma2_ts_off<0>(tmem_o, pa + 0, bdesc0, kIdescPV2, m > 0 ? 1u : 0u);
+                    mma2_ts_off<128>(tmem_o, pa + 8, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<256>(tmem_o, pa + 16, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<384>(tmem_o, pa + 24, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<512>(tmem_o, pa + 32, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<640>(tmem_o, pa + 40, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<768>(tmem_o, pa + 48, bdesc0, kIdescPV2, 1u);
+                    mma2_ts_off<896>(tmem_o, pa + 56, bdesc0, kIdescPV2, 1u);
                     mma2_commit_both(&sh.kv_empty[slot]);
                     mma2_commit_both(&sh.pv_done[ss]);
                 }
@@ -1290,7 +1313,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             bool ok = true;
             for (int n = 0; n <= it.ntiles && ok; ++n) {
                 bool qk_todo = n < it.ntiles, pv_todo = n >= 1;
-                const uint64_t t0 = global_timer_ns();
+                uint64_t t0 = 0;  // read on the first round that finds nothing to issue
                 while (qk_todo || pv_todo) {
                     if (qk_todo) {
                         const uint32_t sq = seq_k(n);
@@ -1311,7 +1334,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     }
                     if (*abort) { ok = false; break; }
                     __nanosleep(20);
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    if (t0 == 0) t0 = global_timer_ns();
+                    else if (global_timer_ns() - t0 > kWaitLimitNs) {
                         if (lane == 0) report(p, INK_DEVERR_TIMEOUT);
                         *abort = 1;
                         ok = false;
