@@ -130,6 +130,8 @@ int heuristic_splits_decode(long long batch, long long groups, int sms)
     long long s = ceil_div(groups, target_chunk);
     if (batch * s < 4ll * sms) s = s_wave;
     s = std::min<long long>(s, std::max<long long>(64, s_wave));  // long rows: whole waves, fewer partials
+    s = std::min<long long>(s, ceil_div(groups, 16));  // at least 256 keys a split: shorter items cost more
+                                                        // in per-item setup than they gain in balance
     s = std::min<long long>(s, groups);
     s = std::min<long long>(s, 1024);
     return (int)std::max(1ll, s);
