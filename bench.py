@@ -626,10 +626,10 @@ def run_ours(args, rank, world, local_rank):
             return start.elapsed_time(end) / steps
 
         n0 = ink.launch_count()
-        eager_ms = timed(run)
-        per_step = (ink.launch_count() - n0) / (steps + warmup)
-        want = out.clone()
-        with ClockSampler(local_rank) as clk:
+        with ClockSampler(local_rank) as clk:  # both arms under the same sampler thread
+            eager_ms = timed(run)
+            per_step = (ink.launch_count() - n0) / (steps + warmup)
+            want = out.clone()
             graph_ms = timed(graph.replay)
         if not torch.equal(out, want):
             raise RuntimeError("graph replay and direct call differ")
