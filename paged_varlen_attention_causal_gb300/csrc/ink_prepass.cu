@@ -16,6 +16,7 @@ namespace ink {
 
 constexpr int kPrepassThreads = 1024;
 constexpr int kCostBuckets = 1024;
+constexpr int kSmemReqs = 2048;  // batches up to this size keep their per-request offsets in shared memory too
 
 // Exclusive block-wide scan of one int per thread; returns the block total.
 __device__ int block_exclusive_scan(int v, int *out, int *warp_sums)
@@ -41,6 +42,47 @@ __device__ int block_exclusive_scan(int v, int *out, int *warp_sums)
     __syncthreads();
     const int total = warp_sums[31];
     *out = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    __syncthreads();
+    return total;
+}
+
+// Four such scans at once (one set of barriers for the four counts of pass 1).
+__device__ int4 block_exclusive_scan4(int4 v, int4 *out, int4 *warp_sums)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int4 x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(0xffffffffu, x.x, o), y1 = __shfl_up_sync(0xffffffffu, x.y, o);
+        const int y2 = __shfl_up_sync(0xffffffffu, x.z, o), y3 = __shfl_up_sync(0xffffffffu, x.w, o);
+        if (lane >= o) {
+            x.x += y0;
+            x.y += y1;
+            x.z += y2;
+            x.w += y3;
+        }
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int4 w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y0 = __shfl_up_sync(0xffffffffu, w.x, o), y1 = __shfl_up_sync(0xffffffffu, w.y, o);
+            const int y2 = __shfl_up_sync(0xffffffffu, w.z, o), y3 = __shfl_up_sync(0xffffffffu, w.w, o);
+            if (lane >= o) {
+                w.x += y0;
+                w.y += y1;
+                w.z += y2;
+                w.w += y3;
+            }
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int4 total = warp_sums[31];
+    const int4 before = warp > 0 ? warp_sums[warp - 1] : make_int4(0, 0, 0, 0);
+    *out = make_int4(x.x - v.x + before.x, x.y - v.y + before.y, x.z - v.z + before.z, x.w - v.w + before.w);
     __syncthreads();
     return total;
 }
@@ -92,6 +134,8 @@ __device__ __forceinline__ int pf_cost_bucket(const UnitSplit &u)
 __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params p)
 {
     __shared__ int warp_sums[32];
+    __shared__ int4 warp_sums4[32];
+    __shared__ int s_dec_off[kSmemReqs + 1], s_unit_off[kSmemReqs + 1];  // copies for the searches below
     __shared__ int bucket_count[kCostBuckets];
     __shared__ int bucket_base[kCostBuckets];
     __shared__ int s_carry[4];
@@ -192,22 +236,23 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
                 if (p.causal && r.Lk < r.Lq) my_err |= INK_DEVERR_EMPTY_ROWS;
             }
         }
-        int xd, xq, xc, xt;
-        const int td = block_exclusive_scan(ndec, &xd, warp_sums);
-        const int tq = block_exclusive_scan(nq, &xq, warp_sums);
-        const int tcb = block_exclusive_scan(nc, &xc, warp_sums);
-        const int tt = block_exclusive_scan(ntile, &xt, warp_sums);
+        int4 x;
+        const int4 tot = block_exclusive_scan4(make_int4(ndec, nq, nc, ntile), &x, warp_sums4);
         if (b < p.B) {
-            dec_off[b] = s_carry[0] + xd;
-            unit_off[b] = s_carry[1] + xq;
-            comb_off[b] = s_carry[2] + xc;
+            dec_off[b] = s_carry[0] + x.x;
+            unit_off[b] = s_carry[1] + x.y;
+            comb_off[b] = s_carry[2] + x.z;
+            if (p.B <= kSmemReqs) {
+                s_dec_off[b] = s_carry[0] + x.x;
+                s_unit_off[b] = s_carry[1] + x.y;
+            }
         }
         __syncthreads();
         if (tid == 0) {
-            s_carry[0] += td;
-            s_carry[1] += tq;
-            s_carry[2] += tcb;
-            s_carry[3] += tt;
+            s_carry[0] += tot.x;
+            s_carry[1] += tot.y;
+            s_carry[2] += tot.z;
+            s_carry[3] += tot.w;
         }
         __syncthreads();
     }
@@ -230,15 +275,26 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     const int n_dec = s_overflow ? 0 : min(s_carry[0], p.dec_items_cap);
     const int n_units = s_overflow ? 0 : s_carry[1];
 
+    const int *doff = p.B <= kSmemReqs ? s_dec_off : dec_off;
+    const int *uoff = p.B <= kSmemReqs ? s_unit_off : unit_off;
+
     // pass 2: decode items (request, split), request order; one item per thread, so that a
     // single long request's splits are written in parallel.
     for (int i = tid; i < n_dec; i += blockDim.x) {
         int lo = 0, hi = p.B - 1;  // request owning item i: last b with dec_off[b] <= i
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (dec_off[mid] <= i) lo = mid; else hi = mid - 1;
+            if (doff[mid] <= i) lo = mid; else hi = mid - 1;
         }
-        p.dec_items[i] = make_int2(lo, i - dec_off[lo]);
+        p.dec_items[i] = make_int2(lo, i - doff[lo]);
+    }
+    if (n_units == 0) {  // no prefill unit: nothing to sort
+        if (tid == 0) {
+            p.hdr->pf_count = 0u;
+            p.hdr->dec_count = (uint32_t)n_dec;
+            atomicOr(&p.hdr->errors, s_err);
+        }
+        return;
     }
 
     // pass 3: prefill units -> cost histogram of their splits.
@@ -246,9 +302,9 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         int lo = 0, hi = p.B - 1;  // request owning unit u: last b with unit_off[b] <= u
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (unit_off[mid] <= u) lo = mid; else hi = mid - 1;
+            if (uoff[mid] <= u) lo = mid; else hi = mid - 1;
         }
-        const int b = lo, qt = u - unit_off[b];
+        const int b = lo, qt = u - uoff[b];
         Req r = load_req(p, b);
         int qa0, qa1;
         pf_unit_of(p, r, qt, qa0, qa1);
@@ -279,9 +335,9 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         int lo = 0, hi = p.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (unit_off[mid] <= u) lo = mid; else hi = mid - 1;
+            if (uoff[mid] <= u) lo = mid; else hi = mid - 1;
         }
-        const int b = lo, qt = u - unit_off[b];
+        const int b = lo, qt = u - uoff[b];
         Req r = load_req(p, b);
         int qa0, qa1;
         pf_unit_of(p, r, qt, qa0, qa1);
