@@ -132,6 +132,8 @@ int heuristic_splits_decode(long long batch, long long groups, int sms)
     s = std::min<long long>(s, std::max<long long>(64, s_wave));  // long rows: whole waves, fewer partials
     s = std::min<long long>(s, ceil_div(groups, 16));  // at least 256 keys a split: shorter items cost more
                                                         // in per-item setup than they gain in balance
+    // ... unless that leaves SMs idle: then one full wave, with at least 128 keys a split
+    if (batch * s < sms && groups >= 8 * ceil_div(sms, batch)) s = ceil_div(sms, batch);
     s = std::min<long long>(s, groups);
     s = std::min<long long>(s, 1024);
     return (int)std::max(1ll, s);
