@@ -256,7 +256,7 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
     if (pl.dec_cap > (1ll << 30) || pl.pf_cap > (1ll << 30)) return false;
 
     size_t off = sizeof(WsHeader);
-    pl.off_dec_items = off; off = align256(off + sizeof(int2) * (size_t)pl.dec_cap);
+    pl.off_dec_items = off; off = align256(off + sizeof(int4) * (size_t)pl.dec_cap);
     pl.off_pf_items = off; off = align256(off + sizeof(int4) * (size_t)pl.pf_cap);
     pl.off_dec_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
     pl.off_unit_off = off; off = align256(off + sizeof(int) * (size_t)(B + 1));
@@ -457,7 +457,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.hdr = reinterpret_cast<WsHeader *>(ws);
-    p.dec_items = reinterpret_cast<int2 *>(ws + pl.off_dec_items);
+    p.dec_items = reinterpret_cast<int4 *>(ws + pl.off_dec_items);
     p.dec_items_cap = (int)pl.dec_cap;
     p.pf_items = reinterpret_cast<int4 *>(ws + pl.off_pf_items);
     p.pf_items_cap = (int)pl.pf_cap;
@@ -508,7 +508,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
                 return INK_ERR_CUDA;
         }
         if (pl.any_prefill && pl.S_pf > 1) {
-            if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, stream); }) != cudaSuccess)
+            if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, pl.S_pf, stream); }) !=
+                cudaSuccess)
                 return INK_ERR_CUDA;
         }
         return INK_OK;
@@ -652,7 +653,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
                                                    window_right),
                                         pl.chunk_dec);
     if ((pl.any_decode && sdec_eff > 1) || (pl.any_prefill && pl.S_pf > 1)) {
-        if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, stream); }) != cudaSuccess)
+        const int max_splits = (int)std::max<long long>(pl.any_decode ? sdec_eff : 1, pl.any_prefill ? pl.S_pf : 1);
+        if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, max_splits, stream); }) !=
+            cudaSuccess)
             return INK_ERR_CUDA;
     }
     return INK_OK;

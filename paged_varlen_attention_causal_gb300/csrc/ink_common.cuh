@@ -23,7 +23,7 @@ constexpr uint32_t kWaitHintNs = 100000;           // longest single suspension 
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned).
-//   header | dec_items[int2] | pf_items[int4] | part_lse[f32] | part_o[f32]
+//   header | dec_items[int4] | pf_items[int4] | part_lse[f32] | part_o[f32]
 // ---------------------------------------------------------------------------
 struct WsHeader {
     uint32_t errors;       // INK_DEVERR_* bits
@@ -52,7 +52,7 @@ struct Params {
     float *lse;
     // workspace
     WsHeader *hdr;
-    int2 *dec_items;
+    int4 *dec_items;  // (b, split | Lq << 27, t0, Lk): the request's fields ride with the item
     int dec_items_cap;
     int4 *pf_items;
     int pf_items_cap;
@@ -97,10 +97,10 @@ struct Req {
     uint32_t err;
 };
 
-__device__ __forceinline__ Req load_req(const Params &p, int b)
+// Request b from its cu_seqlens_q pair (c0, c1) and cache_seqlens entry lk, validated.
+__device__ __forceinline__ Req make_req(const Params &p, int c0, int c1, int lk)
 {
     Req r;
-    const int c0 = __ldg(p.cu + b), c1 = __ldg(p.cu + b + 1), lk = __ldg(p.seqk + b);
     r.t0 = c0;
     r.Lq = c1 - c0;
     r.Lk = lk;
@@ -110,6 +110,11 @@ __device__ __forceinline__ Req load_req(const Params &p, int b)
     if (lk < 0 || (long long)lk > (long long)p.MAXBLK * p.BS) r.err |= INK_DEVERR_SEQLEN_K;
     r.ok = (r.err == 0);
     return r;
+}
+
+__device__ __forceinline__ Req load_req(const Params &p, int b)
+{
+    return make_req(p, __ldg(p.cu + b), __ldg(p.cu + b + 1), __ldg(p.seqk + b));
 }
 
 __device__ __forceinline__ bool is_decode_req(const Params &p, const Req &r)
@@ -479,7 +484,8 @@ cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUten
 cudaError_t launch_prefill_pair(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 const CUtensorMap &tm_bias, const CUtensorMap &tm_kh, const CUtensorMap &tm_vh,
                                 long long max_pairs, size_t smem, cudaStream_t stream);
-cudaError_t launch_combine(const Params &p, int sms, cudaStream_t stream);
+// max_splits: the most splits any row of the call was cut into (sizes the warps a row gets)
+cudaError_t launch_combine(const Params &p, int sms, int max_splits, cudaStream_t stream);
 cudaError_t launch_stage(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_generic(const Params &p, int sms, cudaStream_t stream);
 cudaError_t launch_append(const ink_attn_dims *d, const void *key, const void *value, void *key_cache,

@@ -190,27 +190,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (p.bias_tma) prefetch_tmap(&tm_bias);
         }
         const uint64_t pol_kv = policy_evict_first();
+        // CTA c takes item c first and then items gridDim.x + k in the order of the shared counter, so
+        // the first item needs no atomic; its entry is read speculatively beside the item count.
         const int total = (int)*(volatile uint32_t *)&p.hdr->dec_count;
-        int next = 0;
-        if (lane == 0) next = (int)atomicAdd(&p.hdr->dec_next, 1u);
-        next = __shfl_sync(0xffffffffu, next, 0);
+        int next = blockIdx.x;
+        int4 di_next = make_int4(0, 0, 0, 0);
+        if (next < p.dec_items_cap) di_next = p.dec_items[next];
         uint32_t n = 0;  // stage sequence number
         for (uint32_t iseq = 0;; ++iseq) {
             const int cur = next;
+            const int4 di = di_next;
             if (cur < total) {
-                if (lane == 0) next = (int)atomicAdd(&p.hdr->dec_next, 1u);
+                if (lane == 0) next = (int)gridDim.x + (int)atomicAdd(&p.hdr->dec_next, 1u);
                 next = __shfl_sync(0xffffffffu, next, 0);
+                if (next < total) di_next = p.dec_items[next];
             }
             const int slot = iseq & 1;
             if (!mbar_wait_warp(&sh.item_empty[slot], ((iseq >> 1) & 1) ^ 1, abort, p)) break;
             DecItem it;
             it.valid = 0;
             if (cur < total) {
-                const int2 di = p.dec_items[cur];
-                const Req r = load_req(p, di.x);
-                const UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, di.y);
-                it.b = di.x; it.t0 = r.t0; it.Lq = r.Lq; it.Lk = r.Lk;
-                it.gb = u.gb; it.ge = u.ge; it.split = di.y; it.nact = u.nact; it.valid = 1;
+                const int split = di.y & ((1 << 27) - 1), Lq = (int)((unsigned)di.y >> 27);
+                const UnitSplit u = unit_split(di.w - Lq, di.w - 1, di.w, p.causal, p.wl, p.wr, p.chunk_dec, split);
+                it.b = di.x; it.t0 = di.z; it.Lq = Lq; it.Lk = di.w;
+                it.gb = u.gb; it.ge = u.ge; it.split = split; it.nact = u.nact; it.valid = 1;
                 it.index = cur;
             }
             if (lane == 0) {

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     __shared__ int s_pg_carry;
     __shared__ uint32_t s_err;
     __shared__ int s_overflow;
+    __shared__ int4 s_req[kPrepassThreads];  // (t0, Lq, Lk) of the first kPrepassThreads requests
 
     int *dec_off = p.dec_off;
     int *unit_off = p.unit_off;
@@ -151,6 +152,9 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     const int tid = threadIdx.x;
     pdl_wait();  // the previous kernel of the stream (e.g. the last call's merge, which reads this workspace)
     pdl_launch_dependents();
+    // this thread's request among the first kPrepassThreads (the whole batch, mostly), loaded here so that
+    // the loads overlap the header checks below
+    const Req pre = tid < p.B ? load_req(p, tid) : Req{};
 
     if (tid == 0) {
         p.hdr->errors = 0;
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
             long long need = 0;
             int pages = 0;
             if (b < p.B) {
-                const Req r = load_req(p, b);
+                const Req r = base == 0 ? pre : load_req(p, b);
                 if (r.ok && r.Lq > 0 && !is_decode_req(p, r) && r.Lk > 0) need = stage_keys_of(r.Lk);
             }
             long long x;
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
         const int b = base + tid;
         int ndec = 0, nq = 0, nc = 0, ntile = 0;  // ntile: q tiles of tpt tokens, for the budget check
         if (b < p.B) {
-            Req r = load_req(p, b);
+            Req r = base == 0 ? pre : load_req(p, b);
+            if (base == 0) s_req[b] = make_int4(r.t0, r.Lq, r.Lk, 0);
             my_err |= r.err;
             if (r.ok && r.Lq > 0) {
                 if (is_decode_req(p, r)) {
@@ -286,7 +291,14 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
             const int mid = (lo + hi + 1) >> 1;
             if (doff[mid] <= i) lo = mid; else hi = mid - 1;
         }
-        p.dec_items[i] = make_int2(lo, i - doff[lo]);
+        int4 rq;  // a decode item's request is valid (t0, Lq <= 16, Lk), and its split index < 2^27
+        if (lo < kPrepassThreads) {
+            rq = s_req[lo];
+        } else {
+            const Req r = load_req(p, lo);
+            rq = make_int4(r.t0, r.Lq, r.Lk, 0);
+        }
+        p.dec_items[i] = make_int4(lo, (int)((unsigned)(i - doff[lo]) | ((unsigned)rq.y << 27)), rq.x, rq.z);
     }
     if (n_units == 0) {  // no prefill unit: nothing to sort
         if (tid == 0) {
