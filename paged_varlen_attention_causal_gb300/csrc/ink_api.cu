@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA on sm_100-class SMs
+constexpr size_t kSmemPerSm = 233472;  // 228 KB of shared memory per SM
+constexpr size_t kSmemReserved = 1024;  // shared memory the system reserves per CTA
 constexpr int kDecSharedBytes = 512;   // mbarriers + item ring of the decode kernel (upper bound)
 constexpr int kDecMaxStages = 8;
 
@@ -612,14 +614,21 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         // holds more pages (an E4M3 decode batch: 6 stages instead of 5)
         const int bias_bytes = pl.lq_dec * bias_slot;
         const int stage_bytes = (2 * kv_bytes + bias_bytes + 1023) & ~1023;
-        int nst = (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
+        // Two CTAs an SM when half of its shared memory still holds a ring of three stages (E4M3 pages, or
+        // bf16 pages of at most 4 KV heads): twice the warps in flight for the per-page chain of dependent
+        // steps, at 96 registers a thread.
+        const int nst2 = (int)((kSmemPerSm / 2 - kSmemReserved - 1024 - kDecSharedBytes) / stage_bytes);
+        const int per_sm = nst2 >= 3 ? 2 : 1;
+        // every decode item has at most lq_dec tokens (longer ones are rejected against max_seqlen_q)
+        const int small = pl.lq_dec * pl.G <= 8 ? 1 : 0;
+        int nst = per_sm == 2 ? nst2 : (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
         nst = std::min(nst, kDecMaxStages);
         if (nst < 2) return INK_ERR_UNSUPPORTED;
         const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
-        const int grid = (int)std::min<long long>(sms, pl.dec_cap);
+        const int grid = (int)std::min<long long>((long long)per_sm * sms, pl.dec_cap);
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
                 return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, kv.fp8,
-                                     kv.k_scale, kv.v_scale, grid, smem, stream);
+                                     kv.k_scale, kv.v_scale, per_sm, small, grid, smem, stream);
             }) != cudaSuccess)
             return INK_ERR_CUDA;
     }

@@ -40,6 +40,8 @@
 //    tile holding even d, the odd bytes that of the tile holding odd d, so no
 //    conversion pass through shared memory is needed;
 //  * k_scale joins the softmax scale and v_scale the final normalisation.
+#include <type_traits>
+
 #include "ink_common.cuh"
 
 namespace ink {
@@ -150,8 +152,11 @@ __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
     return E > 0 && rd_max >= 0 && rd_min < E;
 }
 
-template <int kDSlices, bool kFp8>  // d-slices per KV head = 8 / Hkv; E4M3 K/V pages
-__global__ void __launch_bounds__(kDecThreads, 1)
+// kDSlices: d-slices per KV head = 8 / Hkv; kFp8: E4M3 K/V pages; kPerSm: CTAs an SM (2: half the shared
+// memory and registers each, twice the warps to hide the per-page dependency chain); kSmall: every item of
+// the call has at most 8 packed rows, so the 16-row path is left out (fewer registers)
+template <int kDSlices, bool kFp8, int kPerSm, bool kSmall>
+__global__ void __launch_bounds__(kDecThreads, kPerSm)
     ink_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
                       int nstages, int stage_bytes, int kv_bytes, int bias_slot_bytes, float k_scale,
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int rows = it.Lq * G;
         const int qa0 = it.Lk - it.Lq, qa1 = it.Lk - 1;
 
-        if (rows <= 8) {
+        if (kSmall || rows <= 8) {
             // ---- at most 8 packed rows: S^T = K Q^T and O^T += V^T P^T, so the 16 keys of a page fill
             // the mma's M and the rows its N = 8 (half the mma and softmax work of the 16-row block).
             // Fragments: this thread's S^T / O^T accumulators hold rows 2t and 2t + 1 at keys (or d)
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
             // two pages per step when the ring is deep enough to hold two and still prefetch (at least 4
             // stages): two independent QK chains, and one max exchange and rescale decision per 32 keys
-            const bool pair_pages = nstages >= 4;
+            const bool pair_pages = kPerSm == 1 && nstages >= 4;
             for (int gi = it.gb; gi < it.ge;) {
                 const bool two = pair_pages && gi + 1 < it.ge;
                 const int sa = n % nstages, sb = (n + 1) % nstages;
@@ -908,8 +913,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,
-                          int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int grid, size_t smem,
-                          cudaStream_t stream)
+                          int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int per_sm, int small,
+                          int grid, size_t smem, cudaStream_t stream)
 {
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -917,20 +922,25 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
         return launch_pdl(kernel, (unsigned)grid, kDecThreads, smem, stream, p, tm_k, tm_v, tm_bias, nstages,
                           stage_bytes, kv_bytes, bias_slot_bytes, k_scale, v_scale);
     };
-    if (kv_fp8) {
+    auto pick = [&](auto fp8, auto two, auto small) {
+        constexpr bool F = decltype(fp8)::value, M = decltype(small)::value;
+        constexpr int S = decltype(two)::value ? 2 : 1;
         switch (8 / p.Hkv) {
-            case 1: return go(ink_decode_kernel<1, true>);
-            case 2: return go(ink_decode_kernel<2, true>);
-            case 4: return go(ink_decode_kernel<4, true>);
-            default: return go(ink_decode_kernel<8, true>);
+            case 1: return go(ink_decode_kernel<1, F, S, M>);
+            case 2: return go(ink_decode_kernel<2, F, S, M>);
+            case 4: return go(ink_decode_kernel<4, F, S, M>);
+            default: return go(ink_decode_kernel<8, F, S, M>);
         }
+    };
+    using T = std::true_type;
+    using N = std::false_type;
+    // the small-rows variants only where the registers are capped (two CTAs an SM)
+    if (kv_fp8) {
+        if (per_sm != 2) return pick(T{}, N{}, N{});
+        return small ? pick(T{}, T{}, T{}) : pick(T{}, T{}, N{});
     }
-    switch (8 / p.Hkv) {
-        case 1: return go(ink_decode_kernel<1, false>);
-        case 2: return go(ink_decode_kernel<2, false>);
-        case 4: return go(ink_decode_kernel<4, false>);
-        default: return go(ink_decode_kernel<8, false>);
-    }
+    if (per_sm != 2) return pick(N{}, N{}, N{});
+    return small ? pick(N{}, T{}, T{}) : pick(N{}, T{}, N{});
 }
 
 }  // namespace ink
