@@ -618,7 +618,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         // bf16 pages of at most 4 KV heads): twice the warps in flight for the per-page chain of dependent
         // steps, at 96 registers a thread.
         const int nst2 = (int)((kSmemPerSm / 2 - kSmemReserved - 1024 - kDecSharedBytes) / stage_bytes);
-        const int per_sm = nst2 >= 3 ? 2 : 1;
+        // (the two-an-SM build reads the bias band only from its stages: a call whose bias cannot go by TMA
+        // keeps one CTA an SM)
+        const int per_sm = nst2 >= 3 && (E == 0 || bias_dec_tma) ? 2 : 1;
         // every decode item has at most lq_dec tokens (longer ones are rejected against max_seqlen_q)
         const int small = pl.lq_dec * pl.G <= 8 ? 1 : 0;
         int nst = per_sm == 2 ? nst2 : (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);

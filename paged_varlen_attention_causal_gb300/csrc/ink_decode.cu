@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                         const int qa = second ? qa_1 : qa_0;
                         const int rd = qa - key;
                         float bias = 0.f;
-                        if (p.bias_tma) {
+                        if (kPerSm == 2 || p.bias_tma) {  // two an SM: launched only with the bias by TMA
                             const int x0 = floor4(qa - (kbase_key + kKeyGroup - 1));
                             if (second ? v1 : v0)
                                 bias = bsm[((second ? tok1 : tok0) * bias_slot_bytes) / 4 + (second ? h1 : h0) * 20 +
@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                         const int qa = rowB ? qaB : qaA;
                         const int rd = qa - key;
                         float bias = 0.f;
-                        if (p.bias_tma) {
+                        if (kPerSm == 2 || p.bias_tma) {
                             const int tok = rowB ? tokB : tokA;
                             const int h = rowB ? hB : hA;
                             const int x0 = floor4(qa - (kbase_key + kKeyGroup - 1));
