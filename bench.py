@@ -641,8 +641,9 @@ def run_ours(args, rank, world, local_rank):
 
     steps, warmup = args.steps, args.warmup
     headline = args.workload
-    # head sizes 64 / 256 run every request in the head-size-generic kernel, timed under the prefill's id
-    head_kernel = "prefill" if headline.startswith("chunked_prefill") or headline in HEADDIM else "decode"
+    # head sizes 64 / 256: decodes run in the decode kernel, prefills in the head-size-generic kernel (timed
+    # under the prefill's id)
+    head_kernel = "prefill" if headline.startswith("chunked_prefill") else "decode"
     head = measure(headline, steps, warmup, head_kernel, fp8=args.kv_fp8)
     sec = {}
     skip = {x for x in args.skip.split(",") if x}
@@ -653,9 +654,9 @@ def run_ours(args, rank, world, local_rank):
             ("kv_append_fp8", lambda: measure_append(s2, w2, fp8=True)),
             ("graph_decode", lambda: measure_graph(max(50, steps * 10), max(5, warmup))),
             ("long_decode_splits", lambda: measure_split_sweep(max(5, steps // 2), w2)),
-            ("decode_batch_d64", lambda: measure("decode_batch_d64", s2, w2, "prefill")),
+            ("decode_batch_d64", lambda: measure("decode_batch_d64", s2, w2, "decode")),
             ("chunked_prefill_d64", lambda: measure("chunked_prefill_d64", s2, w2, "prefill")),
-            ("decode_batch_d256", lambda: measure("decode_batch_d256", s2, w2, "prefill")),
+            ("decode_batch_d256", lambda: measure("decode_batch_d256", s2, w2, "decode")),
             ("chunked_prefill_d256", lambda: measure("chunked_prefill_d256", s2, w2, "prefill")),
             ("decode_batch_fp8", lambda: measure("decode_batch", s2, w2, "decode", fp8=True)),
             ("long_decode", lambda: measure("long_decode", s2, w2, "decode")),
@@ -708,7 +709,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     fp8_head = args.kv_fp8
-    hkw = {"kernel": "ink_generic_kernel"} if headline in HEADDIM else {}
+    hkw = {"kernel": "ink_generic_kernel"} if headline in HEADDIM and headline.startswith("chunked") else {}
     if headline.startswith("chunked_prefill"):
         unit = "TFLOP/s"
         value = job_throughput(head["flops"], world, head["ms_per_step"]) / 1e12
@@ -752,7 +753,7 @@ def run_ours(args, rank, world, local_rank):
             continue
         fp8 = name.endswith("_fp8")
         base = name[:-4] if fp8 else name
-        kern = "ink_generic_kernel" if base in HEADDIM else None
+        kern = "ink_generic_kernel" if base in HEADDIM and base.startswith("chunked") else None
         kw = {"kernel": kern} if kern else {}
         entry = {"ms_per_step": round(r["ms_per_step"], 4), "kernel_ms": kernels_of(r),
                  "e2e_ms": round(r["e2e_ms"], 4), "gpu_launches": r["launches"], "clocks": clk_of(r)}

@@ -201,10 +201,18 @@ bool make_plan(const ink_attn_dims *d, int max_seqlen_q, int num_splits, int cau
         }
     }
     pl.bias_w = pf_bias_width(1 << pl.bias_tok_log2);
-    const bool generic = d->head_dim != kHeadDim;  // head-size-generic kernel: every request as 128-row items
+    const bool generic = d->head_dim != kHeadDim;  // head-size-generic kernel for the prefill-shaped requests
     pl.fast_pack = (!generic && 32 % pl.G == 0) ? 1 : 0;
-    pl.decode_kernel = !generic && (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows ? 1 : 0;
     const long long msq = std::min<long long>(max_seqlen_q, std::max(T, 1));
+    // the decode kernel serves every head size where a warp's d-slice (D * Hkv / 8) is at least 16 wide and
+    // its ring holds two stages of a bf16 page (K and V of every KV head, 16 keys) plus the bias room
+    const long long dec_stage =
+        (2ll * Hkv * 32 * d->head_dim + std::min<long long>(kDecodeRows / std::max(1, pl.G), msq) *
+                                            (((long long)H * 80 + 127) & ~127ll) + 1023) & ~1023ll;
+    pl.decode_kernel = (Hkv == 1 || Hkv == 2 || Hkv == 4 || Hkv == 8) && pl.G <= kDecodeRows &&
+                               d->head_dim * Hkv / 8 >= 16 && 1024 + 2 * dec_stage + kDecSharedBytes <= (long long)kSmemLimit
+                           ? 1
+                           : 0;
     pl.any_decode = pl.decode_kernel != 0;
     pl.any_prefill = !pl.decode_kernel || msq * pl.G > kDecodeRows;
     if (!pl.decode_kernel) pl.any_decode = false;
@@ -443,7 +451,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     Params p;
     memset(&p, 0, sizeof p);
-    const bool generic = dims->head_dim != kHeadDim;  // head size 64 or 256: the head-size-generic kernel
+    const bool generic = dims->head_dim != kHeadDim;  // head size 64 or 256: prefill by the head-size-generic kernel
     p.T = T; p.B = dims->batch; p.H = H; p.Hkv = Hkv; p.G = pl.G; p.NB = dims->num_blocks;
     p.D = dims->head_dim;
     p.BS = dims->block_size; p.MAXBLK = dims->max_blocks_per_seq; p.max_seqlen_q = max_seqlen_q;
@@ -500,23 +508,6 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.kv_fp8 = kv.fp8;
     p.out_scale = 1.f;
 
-    if (generic) {
-        // head size 64 or 256: the device plan, the head-size-generic kernel over every request's
-        // 128-row items (timed as the prefill kernel), and the split-KV merge
-        if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, stream); }) != cudaSuccess)
-            return INK_ERR_CUDA;
-        if (pl.any_prefill && pl.pf_cap > 0) {
-            if (timed_launch(INK_KERNEL_PREFILL, stream, [&] { return launch_generic(p, sms, stream); }) != cudaSuccess)
-                return INK_ERR_CUDA;
-        }
-        if (pl.any_prefill && pl.S_pf > 1) {
-            if (timed_launch(INK_KERNEL_COMBINE, stream, [&] { return launch_combine(p, sms, pl.S_pf, stream); }) !=
-                cudaSuccess)
-                return INK_ERR_CUDA;
-        }
-        return INK_OK;
-    }
-
     // tensor maps: K/V as (d, Hkv, keys) bf16 with 64 x 1 x 16 boxes, 128-byte swizzle
     alignas(64) CUtensorMap tm_k, tm_v, tm_vp, tm_kd, tm_vd, tm_bdec, tm_bpf;
     memset(&tm_k, 0, sizeof tm_k); memset(&tm_v, 0, sizeof tm_v); memset(&tm_vp, 0, sizeof tm_vp);
@@ -532,7 +523,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         if (!encode(&tm_kd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, key_cache, gd8, gs8, box8, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tm_vd, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, value_cache, gd8, gs8, box8, CU_TENSOR_MAP_SWIZZLE_128B))
             return INK_ERR_CUDA;
-    } else {
+    } else if (!generic) {
         const cuuint64_t gd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv,
                                   (cuuint64_t)dims->num_blocks * dims->block_size};
         const cuuint64_t gs[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Hkv * kHeadDim * 2};
@@ -547,14 +538,18 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const cuuint32_t box4[4] = {64, (cuuint32_t)kKeyGroup, 2, 1};
         if (!encode(&tm_vp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gd4, gs4, box4, CU_TENSOR_MAP_SWIZZLE_128B))
             return INK_ERR_CUDA;
-        // decode K and V: the same view with a box over every KV head, which lands as
-        // [KV head][d half][16 keys][128 B]: a whole page per copy (Hkv <= 8 for the decode kernel)
-        if (Hkv <= 8) {
-            const cuuint32_t boxd[4] = {64, (cuuint32_t)kKeyGroup, 2, (cuuint32_t)Hkv};
-            if (!encode(&tm_kd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, key_cache, gd4, gs4, boxd, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !encode(&tm_vd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gd4, gs4, boxd, CU_TENSOR_MAP_SWIZZLE_128B))
-                return INK_ERR_CUDA;
-        }
+    }
+    if (!kv.fp8 && pl.decode_kernel && Hkv <= 8) {
+        // decode K and V as (64 d, keys, D / 64 d-blocks, Hkv) with a box over every KV head, which lands as
+        // [KV head][d-block][16 keys][128 B]: a whole page per copy
+        const int D = dims->head_dim, nb = D / 64;
+        const cuuint64_t gdd[4] = {64, (cuuint64_t)dims->num_blocks * dims->block_size, (cuuint64_t)nb,
+                                   (cuuint64_t)Hkv};
+        const cuuint64_t gsd[3] = {(cuuint64_t)Hkv * D * 2, 128, (cuuint64_t)D * 2};
+        const cuuint32_t boxd[4] = {64, (cuuint32_t)kKeyGroup, (cuuint32_t)nb, (cuuint32_t)Hkv};
+        if (!encode(&tm_kd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, key_cache, gdd, gsd, boxd, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode(&tm_vd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, value_cache, gdd, gsd, boxd, CU_TENSOR_MAP_SWIZZLE_128B))
+            return INK_ERR_CUDA;
     }
     // bias maps: rel_logits as (E, H, T) fp32, no swizzle; needs 16-byte rows
     bool bias_dec_tma = false, bias_pf_tma = false;
@@ -568,8 +563,9 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         }
         const cuuint32_t box2[3] = {(cuuint32_t)pl.bias_w, (cuuint32_t)pl.G,
                                     (cuuint32_t)(1 << pl.bias_tok_log2)};
-        bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
-                             CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!generic)
+            bias_pf_tma = encode(&tm_bpf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rel_logits, gd, gs, box2,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE);
     }
 
     // staging planes as (64 d, keys, d half, Hkv): one (64, 128, 2, 1) box is a 128-key tile of one
@@ -607,7 +603,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     if (pl.any_decode && pl.dec_cap > 0) {
         Params pd = p;
         pd.bias_tma = bias_dec_tma ? 1 : 0;
-        const int kv_bytes = Hkv * (kv.fp8 ? 2048 : 4096);  // one 16-key page of K (or V), all KV heads
+        const int kv_bytes = Hkv * (kv.fp8 ? 2048 : 32 * dims->head_dim);  // one 16-key page of K (or V), all KV heads
         const int bias_slot = (H * 80 + 127) & ~127;
         // bias room for the most query tokens a decode-shaped request of this call can have (Lq <=
         // max_seqlen_q, and Lq * G <= 16): with one token per request the stages are smaller and the ring
@@ -635,8 +631,11 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
             return INK_ERR_CUDA;
     }
 
-    // 3. prefill kernel
-    if (pl.any_prefill && pl.pf_cap > 0) {
+    // 3. prefill kernel: head sizes 64 and 256 run the head-size-generic kernel over the 128-row items
+    if (generic && pl.any_prefill && pl.pf_cap > 0) {
+        if (timed_launch(INK_KERNEL_PREFILL, stream, [&] { return launch_generic(p, sms, stream); }) != cudaSuccess)
+            return INK_ERR_CUDA;
+    } else if (pl.any_prefill && pl.pf_cap > 0) {
         Params pp = p;
         pp.bias_tma = bias_pf_tma ? 1 : 0;
         if (kv.fp8) {

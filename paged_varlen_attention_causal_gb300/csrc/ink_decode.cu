@@ -152,10 +152,11 @@ __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
     return E > 0 && rd_max >= 0 && rd_min < E;
 }
 
-// kDSlices: d-slices per KV head = 8 / Hkv; kFp8: E4M3 K/V pages; kPerSm: CTAs an SM (2: half the shared
-// memory and registers each, twice the warps to hide the per-page dependency chain); kSmall: every item of
-// the call has at most 8 packed rows, so the 16-row path is left out (fewer registers)
-template <int kDSlices, bool kFp8, int kPerSm, bool kSmall>
+// kD: head size (64, 128 or 256; E4M3 pages at 128 only); kDSlices: d-slices per KV head = 8 / Hkv; kFp8:
+// E4M3 K/V pages; kPerSm: CTAs an SM (2: half the shared memory and registers each, twice the warps to hide
+// the per-page dependency chain); kSmall: every item of the call has at most 8 packed rows, so the 16-row
+// path is left out (fewer registers)
+template <int kD, int kDSlices, bool kFp8, int kPerSm, bool kSmall>
 __global__ void __launch_bounds__(kDecThreads, kPerSm)
     ink_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
@@ -277,7 +278,13 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
     // ---------------------------------------------------------------- compute
     const int g = warp % Hkv;
     const int dsl = warp / Hkv;                 // d-slice of this warp
-    constexpr int kDW = kHeadDim / kDSlices;    // d width per warp
+    static_assert(!kFp8 || kD == 128, "E4M3 pages are read at head size 128 only");
+    constexpr int kDW = kD / kDSlices;          // d width per warp
+    static_assert(kDW >= 16, "a warp's d-slice is at least one 16-wide mma tile");
+    constexpr int kKSteps = kD / 16;            // k-steps of 16 d in QK^T
+    // a stage holds, per tensor and KV head, kD / 64 blocks of [16 keys][64 d] (128-byte swizzled rows);
+    // E4M3: one [16 keys][128 B] block
+    constexpr int kHeadBytes = kFp8 ? 2048 : kD * 32;
     constexpr int kNT = kDW / 8;                // n-tiles of 8 in the PV product
     const int d0 = dsl * kDW;
     const float log2e = 1.4426950408889634f;
@@ -321,12 +328,12 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
             visible_range(qa0, qa0, it.Lk, p.causal, p.wl, p.wr, tmp, nhi);
 
             // Q^T fragments (B operand) of row gq, 8 k-steps over d
-            uint32_t qb[8][2];
+            uint32_t qb[kKSteps][2];
             {
                 const uint32_t *q_row =
-                    reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokq) * H + hq) * kHeadDim);
+                    reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokq) * H + hq) * kD);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < kKSteps; ++kk) {
                     if constexpr (kFp8) {  // d = 16 kk + 4t + {0,1} and + {2,3}: the E4M3 rows' order
                         const uint2 u = vq ? __ldg(reinterpret_cast<const uint2 *>(q_row + 8 * kk + 2 * t))
                                            : make_uint2(0u, 0u);
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                     }
                 } else {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    for (int kk = 0; kk < kKSteps; ++kk) {
                         const int chunk = ((kk & 3) << 1) + (lane >> 4);
                         uint32_t a[4];
                         ldsm_x4(kbase + (kk >> 2) * 2048 + lkey * 128 + ((chunk ^ (lkey & 7)) << 4), a[0], a[1],
@@ -463,8 +470,8 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 if (!mbar_wait_warp(&sh.full[sa], (n / nstages) & 1, abort, p)) break;
                 if (two && !mbar_wait_warp(&sh.full[sb], ((n + 1) / nstages) & 1, abort, p)) break;
                 const uint8_t *stA = ring + (size_t)sa * stage_bytes, *stB = ring + (size_t)sb * stage_bytes;
-                const uint32_t kA = smem_u32(stA) + g * (kFp8 ? 2048 : 4096);
-                const uint32_t kB = smem_u32(stB) + g * (kFp8 ? 2048 : 4096);
+                const uint32_t kA = smem_u32(stA) + g * kHeadBytes;
+                const uint32_t kB = smem_u32(stB) + g * kHeadBytes;
                 float scA[4], scB[4], xA[4], xB[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 qk_page(kA, scA);
                 if (two) qk_page(kB, scB);
@@ -548,11 +555,11 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                         const float e0 = o[2 * vb][2 * sec] * inv0, f0 = o[2 * vb + 1][2 * sec] * inv0;
                         const float e1 = o[2 * vb][2 * sec + 1] * inv1, f1 = o[2 * vb + 1][2 * sec + 1] * inv1;
                         if (it.nact == 1) {
-                            if (v0) *reinterpret_cast<uint32_t *>(p.out + row0 * kHeadDim + d) = pack_bf16x2(e0, f0);
-                            if (v1) *reinterpret_cast<uint32_t *>(p.out + row1 * kHeadDim + d) = pack_bf16x2(e1, f1);
+                            if (v0) *reinterpret_cast<uint32_t *>(p.out + row0 * kD + d) = pack_bf16x2(e0, f0);
+                            if (v1) *reinterpret_cast<uint32_t *>(p.out + row1 * kD + d) = pack_bf16x2(e1, f1);
                         } else {
-                            if (v0) *reinterpret_cast<float2 *>(p.part_dec_o + pr0 * kHeadDim + d) = make_float2(e0, f0);
-                            if (v1) *reinterpret_cast<float2 *>(p.part_dec_o + pr1 * kHeadDim + d) = make_float2(e1, f1);
+                            if (v0) *reinterpret_cast<float2 *>(p.part_dec_o + pr0 * kD + d) = make_float2(e0, f0);
+                            if (v1) *reinterpret_cast<float2 *>(p.part_dec_o + pr1 * kD + d) = make_float2(e1, f1);
                         }
                     }
                 }
@@ -570,12 +577,12 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 for (int mt = 0; mt < kMT; ++mt) {
                     const int d = d0 + 16 * mt + gq;
                     if (v0) {
-                        p.out[row0 * kHeadDim + d] = __float2bfloat16_rn(o[mt][0] * inv0);
-                        p.out[row0 * kHeadDim + d + 8] = __float2bfloat16_rn(o[mt][2] * inv0);
+                        p.out[row0 * kD + d] = __float2bfloat16_rn(o[mt][0] * inv0);
+                        p.out[row0 * kD + d + 8] = __float2bfloat16_rn(o[mt][2] * inv0);
                     }
                     if (v1) {
-                        p.out[row1 * kHeadDim + d] = __float2bfloat16_rn(o[mt][1] * inv1);
-                        p.out[row1 * kHeadDim + d + 8] = __float2bfloat16_rn(o[mt][3] * inv1);
+                        p.out[row1 * kD + d] = __float2bfloat16_rn(o[mt][1] * inv1);
+                        p.out[row1 * kD + d + 8] = __float2bfloat16_rn(o[mt][3] * inv1);
                     }
                 }
                 if (p.lse && dsl == 0 && gq == 0) {
@@ -589,12 +596,12 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 for (int mt = 0; mt < kMT; ++mt) {
                     const int d = d0 + 16 * mt + gq;
                     if (v0) {
-                        p.part_dec_o[pr0 * kHeadDim + d] = o[mt][0] * inv0;
-                        p.part_dec_o[pr0 * kHeadDim + d + 8] = o[mt][2] * inv0;
+                        p.part_dec_o[pr0 * kD + d] = o[mt][0] * inv0;
+                        p.part_dec_o[pr0 * kD + d + 8] = o[mt][2] * inv0;
                     }
                     if (v1) {
-                        p.part_dec_o[pr1 * kHeadDim + d] = o[mt][1] * inv1;
-                        p.part_dec_o[pr1 * kHeadDim + d + 8] = o[mt][3] * inv1;
+                        p.part_dec_o[pr1 * kD + d] = o[mt][1] * inv1;
+                        p.part_dec_o[pr1 * kD + d + 8] = o[mt][3] * inv1;
                     }
                 }
                 if (dsl == 0 && gq == 0) {
@@ -620,14 +627,14 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
         visible_range(qa0, qa0, it.Lk, p.causal, p.wl, p.wr, tmp, int_hi);
 
         // Q fragments (A operand): rows rA / rB, 8 k-steps over d
-        uint32_t qf[8][4];
+        uint32_t qf[kKSteps][4];
         {
-            const uint32_t *qa_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokA) * H + hA) * kHeadDim);
-            const uint32_t *qb_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokB) * H + hB) * kHeadDim);
+            const uint32_t *qa_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokA) * H + hA) * kD);
+            const uint32_t *qb_row = reinterpret_cast<const uint32_t *>(p.q + ((size_t)(it.t0 + tokB) * H + hB) * kD);
             if constexpr (kFp8) {
                 // fp16, d = 16 kk + c4 + {0,1} in a0 / a1 and + {2,3} in a2 / a3 (the key rows' order)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < kKSteps; ++kk) {
                     const int c = (kk * 16 + c4) >> 1;
                     const uint2 ua = vA ? __ldg(reinterpret_cast<const uint2 *>(qa_row + c)) : make_uint2(0u, 0u);
                     const uint2 ub = vB ? __ldg(reinterpret_cast<const uint2 *>(qb_row + c)) : make_uint2(0u, 0u);
@@ -638,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 }
             } else {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < kKSteps; ++kk) {
                     const int c = (kk * 16 + cq) >> 1;
                     qf[kk][0] = vA ? __ldg(qa_row + c) : 0u;
                     qf[kk][1] = vB ? __ldg(qb_row + c) : 0u;
@@ -658,7 +665,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
             const int stage = n % nstages;
             if (!mbar_wait_warp(&sh.full[stage], (n / nstages) & 1, abort, p)) break;
             const uint8_t *st = ring + (size_t)stage * stage_bytes;
-            const uint32_t kbase = smem_u32(st) + g * (kFp8 ? 2048 : 4096);
+            const uint32_t kbase = smem_u32(st) + g * kHeadBytes;
             const uint32_t vbase = kbase + kv_bytes;
 
             // S = Q K^T for 16 keys (2 n-tiles)
@@ -684,7 +691,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 const int mi = lane >> 3, rr = lane & 7;
                 const int key = rr + 8 * (mi >> 1);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < kKSteps; ++kk) {
                     const int dh = kk >> 2;
                     const int chunk = ((kk & 3) << 1) + (mi & 1);
                     const uint32_t addr = kbase + dh * 2048 + key * 128 + ((chunk ^ (key & 7)) << 4);
@@ -856,19 +863,19 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                     const int d = d0 + 32 * vb + 16 * sec + 4 * (lane & 3);
                     if (it.nact == 1) {
                         if (vA) {
-                            *reinterpret_cast<uint32_t *>(p.out + rowA * kHeadDim + d) = pack_bf16x2(o[je][0] * invA, o[jo][0] * invA);
-                            *reinterpret_cast<uint32_t *>(p.out + rowA * kHeadDim + d + 2) = pack_bf16x2(o[je][1] * invA, o[jo][1] * invA);
+                            *reinterpret_cast<uint32_t *>(p.out + rowA * kD + d) = pack_bf16x2(o[je][0] * invA, o[jo][0] * invA);
+                            *reinterpret_cast<uint32_t *>(p.out + rowA * kD + d + 2) = pack_bf16x2(o[je][1] * invA, o[jo][1] * invA);
                         }
                         if (vB) {
-                            *reinterpret_cast<uint32_t *>(p.out + rowB * kHeadDim + d) = pack_bf16x2(o[je][2] * invB, o[jo][2] * invB);
-                            *reinterpret_cast<uint32_t *>(p.out + rowB * kHeadDim + d + 2) = pack_bf16x2(o[je][3] * invB, o[jo][3] * invB);
+                            *reinterpret_cast<uint32_t *>(p.out + rowB * kD + d) = pack_bf16x2(o[je][2] * invB, o[jo][2] * invB);
+                            *reinterpret_cast<uint32_t *>(p.out + rowB * kD + d + 2) = pack_bf16x2(o[je][3] * invB, o[jo][3] * invB);
                         }
                     } else {
                         if (vA)
-                            *reinterpret_cast<float4 *>(p.part_dec_o + pA * kHeadDim + d) =
+                            *reinterpret_cast<float4 *>(p.part_dec_o + pA * kD + d) =
                                 make_float4(o[je][0] * invA, o[jo][0] * invA, o[je][1] * invA, o[jo][1] * invA);
                         if (vB)
-                            *reinterpret_cast<float4 *>(p.part_dec_o + pB * kHeadDim + d) =
+                            *reinterpret_cast<float4 *>(p.part_dec_o + pB * kD + d) =
                                 make_float4(o[je][2] * invB, o[jo][2] * invB, o[je][3] * invB, o[jo][3] * invB);
                     }
                 }
@@ -886,8 +893,8 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
 #pragma unroll
             for (int j = 0; j < kNT; ++j) {
                 const int d = d0 + j * 8 + cq;
-                if (vA) *reinterpret_cast<uint32_t *>(p.out + rowA * kHeadDim + d) = pack_bf16x2(o[j][0] * invA, o[j][1] * invA);
-                if (vB) *reinterpret_cast<uint32_t *>(p.out + rowB * kHeadDim + d) = pack_bf16x2(o[j][2] * invB, o[j][3] * invB);
+                if (vA) *reinterpret_cast<uint32_t *>(p.out + rowA * kD + d) = pack_bf16x2(o[j][0] * invA, o[j][1] * invA);
+                if (vB) *reinterpret_cast<uint32_t *>(p.out + rowB * kD + d) = pack_bf16x2(o[j][2] * invB, o[j][3] * invB);
             }
             if (p.lse && dsl == 0 && (lane & 3) == 0) {
                 if (vA) p.lse[rowA] = lseA;
@@ -900,8 +907,8 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
 #pragma unroll
             for (int j = 0; j < kNT; ++j) {
                 const int d = d0 + j * 8 + cq;
-                if (vA) *reinterpret_cast<float2 *>(p.part_dec_o + pA * kHeadDim + d) = make_float2(o[j][0] * invA, o[j][1] * invA);
-                if (vB) *reinterpret_cast<float2 *>(p.part_dec_o + pB * kHeadDim + d) = make_float2(o[j][2] * invB, o[j][3] * invB);
+                if (vA) *reinterpret_cast<float2 *>(p.part_dec_o + pA * kD + d) = make_float2(o[j][0] * invA, o[j][1] * invA);
+                if (vB) *reinterpret_cast<float2 *>(p.part_dec_o + pB * kD + d) = make_float2(o[j][2] * invB, o[j][3] * invB);
             }
             if (dsl == 0 && (lane & 3) == 0) {
                 if (vA) p.part_dec_lse[pA] = lseA;
@@ -922,25 +929,37 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
         return launch_pdl(kernel, (unsigned)grid, kDecThreads, smem, stream, p, tm_k, tm_v, tm_bias, nstages,
                           stage_bytes, kv_bytes, bias_slot_bytes, k_scale, v_scale);
     };
-    auto pick = [&](auto fp8, auto two, auto small) {
-        constexpr bool F = decltype(fp8)::value, M = decltype(small)::value;
+    // the d-slices of a KV head (8 / Hkv), for one head size and build
+    auto slices = [&](auto d, auto fp8, auto two, auto sm) -> cudaError_t {
+        constexpr int D = decltype(d)::value;
+        constexpr bool F = decltype(fp8)::value, M = decltype(sm)::value;
         constexpr int S = decltype(two)::value ? 2 : 1;
         switch (8 / p.Hkv) {
-            case 1: return go(ink_decode_kernel<1, F, S, M>);
-            case 2: return go(ink_decode_kernel<2, F, S, M>);
-            case 4: return go(ink_decode_kernel<4, F, S, M>);
-            default: return go(ink_decode_kernel<8, F, S, M>);
+            case 1: return go(ink_decode_kernel<D, 1, F, S, M>);
+            case 2: return go(ink_decode_kernel<D, 2, F, S, M>);
+            case 4: return go(ink_decode_kernel<D, 4, F, S, M>);
+            default:
+                if constexpr (D / 8 >= 16) return go(ink_decode_kernel<D, 8, F, S, M>);
+                else return cudaErrorInvalidValue;  // D = 64 with one KV head: d-slices narrower than a tile
         }
     };
-    using T = std::true_type;
-    using N = std::false_type;
-    // the small-rows variants only where the registers are capped (two CTAs an SM)
+    // the small-rows build only where the registers are capped (two CTAs an SM)
+    auto builds = [&](auto d, auto fp8) -> cudaError_t {
+        using T = std::true_type;
+        using N = std::false_type;
+        if (per_sm != 2) return slices(d, fp8, N{}, N{});
+        return small ? slices(d, fp8, T{}, T{}) : slices(d, fp8, T{}, N{});
+    };
     if (kv_fp8) {
-        if (per_sm != 2) return pick(T{}, N{}, N{});
-        return small ? pick(T{}, T{}, T{}) : pick(T{}, T{}, N{});
+        if (p.D != 128) return cudaErrorInvalidValue;
+        return builds(std::integral_constant<int, 128>{}, std::true_type{});
     }
-    if (per_sm != 2) return pick(N{}, N{}, N{});
-    return small ? pick(N{}, T{}, T{}) : pick(N{}, T{}, N{});
+    switch (p.D) {
+        case 64: return builds(std::integral_constant<int, 64>{}, std::false_type{});
+        case 128: return builds(std::integral_constant<int, 128>{}, std::false_type{});
+        case 256: return builds(std::integral_constant<int, 256>{}, std::false_type{});
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ink

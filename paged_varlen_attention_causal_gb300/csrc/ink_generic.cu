@@ -3,10 +3,11 @@
 //
 // It consumes the prefill work list the prepass builds (one item = request, q
 // tile of 128 / G tokens, split, KV head: 128 packed rows, row L = token L / G,
-// head L % G of the KV head's group) -- with no decode kernel on this path,
-// every request is cut into such items, decode-shaped ones included -- and
-// writes the same outputs: the bf16 rows and lse, or per-split partials that
-// the split-KV merge combines.
+// head L % G of the KV head's group) and writes the same outputs: the bf16 rows
+// and lse, or per-split partials that the split-KV merge combines.  Decode-shaped
+// requests go to the decode kernel (templated on the head size) unless a warp's
+// d-slice there would be narrower than 16 (D 64 with one KV head): those, too,
+// become items here.
 //
 // Eight warps, 16 rows each.  Per item: the q tile goes to shared memory once;
 // 64-key tiles of K and V are gathered page by page (block_table) with 16-byte
