@@ -9,11 +9,11 @@
 // d-slice there would be narrower than 16 (D 64 with one KV head): those, too,
 // become items here.
 //
-// Eight warps, 16 rows each.  Per item: the q tile goes to shared memory once;
-// 64-key tiles of K and V are gathered page by page (block_table) with 16-byte
-// cp.async copies into a ring (4 tiles deep at D = 64, two CTAs per SM; 2 deep
-// at D = 256), later tiles loading while the current one is used.  Per tile
-// and warp:
+// Eight warps, 16 rows each; persistent CTAs take items from a shared counter.
+// Per item: the q tile goes to shared memory once; 64-key tiles of K and V are
+// gathered page by page (block_table) with 16-byte cp.async copies into a ring
+// (4 tiles deep at D = 64, two CTAs per SM; 2 deep at D = 256), later tiles
+// loading while the current one is used.  Per tile and warp:
 //   S = Q K^T        mma.sync m16n8k16 (bf16 in, fp32 accumulate), Q and K
 //                    fragments by ldmatrix from padded rows (no bank conflicts)
 //   S += bias        rel_logits[token, head, q_abs - key] for 0 <= rd < E
@@ -92,7 +92,10 @@ __global__ void __launch_bounds__(kGenThreads, GenLayout<D>::kCtasPerSm) ink_gen
     const float sl2 = p.scale_log2;
     const float log2e = 1.4426950408889634f;
 
-    for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+    // CTA c takes item c first, then the next free item of the shared counter (items come longest first, so
+    // a CTA that lands late or shares its SM with a long item does not hold back the launch)
+    __shared__ int s_next;
+    for (int idx = blockIdx.x; idx < total;) {
         const int4 w = p.pf_items[idx];
         const int b = w.x, qt = w.y, s = w.z, g = w.w;
         const Req r = load_req(p, b);
@@ -306,6 +309,10 @@ __global__ void __launch_bounds__(kGenThreads, GenLayout<D>::kCtasPerSm) ink_gen
                 if ((lane & 3) == 0) p.part_pf_lse[prow] = lse;
             }
         }
+        // every thread reads s_next before the next item's barriers, which thread 0 passes before rewriting it
+        if (tid == 0) s_next = (int)gridDim.x + (int)atomicAdd(&p.hdr->pf_next, 1u);
+        __syncthreads();
+        idx = s_next;
     }
 }
 
