@@ -118,8 +118,8 @@ INK_API size_t ink_rel_attn_workspace_size(const ink_attn_dims *dims, int32_t ma
  * call copies, in request order, the pages of every prefill-shaped request
  * whose keys (rounded up to whole 128-key tiles) still fit, and the rest read
  * the paged cache.  Results do not depend on it.  Returns 0 for invalid dims
- * and for head sizes other than 128 (the head-size-generic kernel reads the
- * paged cache directly).
+ * and for head sizes other than 128 (the head-size-generic kernel, their
+ * prefill path, reads the paged cache directly).
  */
 INK_API size_t ink_rel_attn_stage_bytes(const ink_attn_dims *dims, int64_t prefill_kv_tokens);
 
@@ -168,8 +168,10 @@ INK_API int32_t ink_rel_attn_num_splits(const ink_attn_dims *dims, int32_t max_s
  *   stream        CUDA stream the kernels are launched on.
  * Head sizes: D = 128 runs the tcgen05 prefill and the decode kernel; D = 64
  * and 256 (the other head sizes the vLLM V1 attention page lists for a paged
- * backend; the PagedAttention V2 page's GQA example uses 256) run one
- * head-size-generic kernel (mma.sync, the same work list) for every request.
+ * backend; the PagedAttention V2 page's GQA example uses 256) run the decode
+ * kernel for decode-shaped requests (where a warp's share of the head, D * Hkv
+ * / 8, is at least 16 and two bf16 pages fit its ring) and a head-size-generic
+ * kernel (mma.sync, the same work list) for the rest.
  * Host-side checks return INK_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE
  * before anything is launched; a launch failure returns INK_ERR_CUDA.
  * Data errors found on the device are reported through the error word.

@@ -1,10 +1,13 @@
-"""Head sizes 64 and 256 on the GPU (the head-size-generic kernel) against the fp64 oracle.
+"""Head sizes 64 and 256 on the GPU against the fp64 oracle.
 
 The vLLM V1 attention page lists 64, 128 and 256 among the head sizes a paged
 backend serves; the PagedAttention V2 page's GQA example has H 24, Hkv 4 (G 6)
-at head size 256.  Same tolerances as head size 128; every request of a call
-runs in this kernel, decode-shaped ones included, with splits merged by the
-split-KV combine at the same head size.
+at head size 256.  Same tolerances as head size 128.  Decode-shaped requests run
+in the decode kernel templated on D (the head-size-generic kernel where a warp's
+share of the head would be narrower than 16, or two bf16 pages do not fit its
+ring: D 64 with one KV head, D 256 with eight), prefill-shaped ones in the
+head-size-generic kernel, with splits merged by the split-KV combine at the same
+head size.
 """
 import numpy as np
 import pytest
