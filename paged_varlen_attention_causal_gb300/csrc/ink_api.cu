@@ -619,6 +619,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const int per_sm = nst2 >= 3 && (E == 0 || bias_dec_tma) ? 2 : 1;
         // every decode item has at most lq_dec tokens (longer ones are rejected against max_seqlen_q)
         const int small = pl.lq_dec * pl.G <= 8 ? 1 : 0;
+        const int one_tok = pl.lq_dec == 1 ? 1 : 0;  // max_seqlen_q 1: one query token a request
         int nst = per_sm == 2 ? nst2 : (int)((kSmemLimit - 1024 - kDecSharedBytes) / stage_bytes);
         nst = std::min(nst, kDecMaxStages);
         if (nst < 2) return INK_ERR_UNSUPPORTED;
@@ -626,7 +627,7 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         const int grid = (int)std::min<long long>((long long)per_sm * sms, pl.dec_cap);
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
                 return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, kv.fp8,
-                                     kv.k_scale, kv.v_scale, per_sm, small, grid, smem, stream);
+                                     kv.k_scale, kv.v_scale, per_sm, small, one_tok, grid, smem, stream);
             }) != cudaSuccess)
             return INK_ERR_CUDA;
     }

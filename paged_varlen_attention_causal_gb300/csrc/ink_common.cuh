@@ -474,11 +474,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned 
 // Host-side launchers, one per translation unit (ink_api.cu calls these).
 cudaError_t launch_prepass(const Params &p, cudaStream_t stream);
 // kv_fp8: K/V pages are E4M3 bytes dequantized with k_scale / v_scale (decode kernel only); per_sm: CTAs an SM
-// the kernel is compiled and sized for (1 or 2); small: no item of the call has more than 8 packed rows.
+// the kernel is compiled and sized for (1 or 2); small: no item of the call has more than 8 packed rows;
+// one_tok: every decode-shaped request has one query token (max_seqlen_q 1).
 cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,
                           int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int per_sm, int small,
-                          int grid, size_t smem, cudaStream_t stream);
+                          int one_tok, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_prefill(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_bias, const CUtensorMap &tm_ks, const CUtensorMap &tm_vs, int grid,
                            size_t smem, cudaStream_t stream);

@@ -155,8 +155,9 @@ __device__ __forceinline__ bool group_in_band(int qa0, int qa1, int gi, int E)
 // kD: head size (64, 128 or 256; E4M3 pages at 128 only); kDSlices: d-slices per KV head = 8 / Hkv; kFp8:
 // E4M3 K/V pages; kPerSm: CTAs an SM (2: half the shared memory and registers each, twice the warps to hide
 // the per-page dependency chain); kSmall: every item of the call has at most 8 packed rows, so the 16-row
-// path is left out (fewer registers)
-template <int kD, int kDSlices, bool kFp8, int kPerSm, bool kSmall>
+// path is left out (fewer registers); kOneTok: every decode-shaped request has one query token (max_seqlen_q
+// 1), so a thread's rows share their token, position and visible range
+template <int kD, int kDSlices, bool kFp8, int kPerSm, bool kSmall, bool kOneTok>
 __global__ void __launch_bounds__(kDecThreads, kPerSm)
     ink_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_bias,
@@ -305,8 +306,8 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
         if (lane == 0) mbar_arrive(&sh.item_empty[slot]);
         if (!it.valid) break;
 
-        const int rows = it.Lq * G;
-        const int qa0 = it.Lk - it.Lq, qa1 = it.Lk - 1;
+        const int rows = kOneTok ? G : it.Lq * G;
+        const int qa0 = it.Lk - (kOneTok ? 1 : it.Lq), qa1 = it.Lk - 1;
 
         if (kSmall || rows <= 8) {
             // ---- at most 8 packed rows: S^T = K Q^T and O^T += V^T P^T, so the 16 keys of a page fill
@@ -316,8 +317,9 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
             const int gq = lane >> 2, t = lane & 3;
             const int r0 = 2 * t, r1 = 2 * t + 1;
             const bool v0 = r0 < rows, v1 = r1 < rows, vq = gq < rows;
-            const int tok0 = r0 / G, tok1 = r1 / G, tokq = gq / G;
-            const int h0 = g * G + r0 % G, h1 = g * G + r1 % G, hq = g * G + gq % G;
+            const int tok0 = kOneTok ? 0 : r0 / G, tok1 = kOneTok ? 0 : r1 / G, tokq = kOneTok ? 0 : gq / G;
+            const int h0 = g * G + (kOneTok ? r0 : r0 % G), h1 = g * G + (kOneTok ? r1 : r1 % G);
+            const int hq = g * G + (kOneTok ? gq : gq % G);
             const int qa_0 = qa0 + tok0, qa_1 = qa0 + tok1;
             int lo0, hi0, lo1, hi1, nlo, nhi, tmp;
             visible_range(qa_0, qa_0, it.Lk, p.causal, p.wl, p.wr, lo0, hi0);
@@ -921,7 +923,7 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
 cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                           const CUtensorMap &tm_bias, int nstages, int stage_bytes, int kv_bytes,
                           int bias_slot_bytes, int kv_fp8, float k_scale, float v_scale, int per_sm, int small,
-                          int grid, size_t smem, cudaStream_t stream)
+                          int one_tok, int grid, size_t smem, cudaStream_t stream)
 {
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -930,25 +932,26 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
                           stage_bytes, kv_bytes, bias_slot_bytes, k_scale, v_scale);
     };
     // the d-slices of a KV head (8 / Hkv), for one head size and build
-    auto slices = [&](auto d, auto fp8, auto two, auto sm) -> cudaError_t {
+    auto slices = [&](auto d, auto fp8, auto two, auto sm, auto one) -> cudaError_t {
         constexpr int D = decltype(d)::value;
-        constexpr bool F = decltype(fp8)::value, M = decltype(sm)::value;
+        constexpr bool F = decltype(fp8)::value, M = decltype(sm)::value, O = decltype(one)::value;
         constexpr int S = decltype(two)::value ? 2 : 1;
         switch (8 / p.Hkv) {
-            case 1: return go(ink_decode_kernel<D, 1, F, S, M>);
-            case 2: return go(ink_decode_kernel<D, 2, F, S, M>);
-            case 4: return go(ink_decode_kernel<D, 4, F, S, M>);
+            case 1: return go(ink_decode_kernel<D, 1, F, S, M, O>);
+            case 2: return go(ink_decode_kernel<D, 2, F, S, M, O>);
+            case 4: return go(ink_decode_kernel<D, 4, F, S, M, O>);
             default:
-                if constexpr (D / 8 >= 16) return go(ink_decode_kernel<D, 8, F, S, M>);
+                if constexpr (D / 8 >= 16) return go(ink_decode_kernel<D, 8, F, S, M, O>);
                 else return cudaErrorInvalidValue;  // D = 64 with one KV head: d-slices narrower than a tile
         }
     };
-    // the small-rows build only where the registers are capped (two CTAs an SM)
+    // the small-rows (and one-token) builds only where the registers are capped (two CTAs an SM)
     auto builds = [&](auto d, auto fp8) -> cudaError_t {
         using T = std::true_type;
         using N = std::false_type;
-        if (per_sm != 2) return slices(d, fp8, N{}, N{});
-        return small ? slices(d, fp8, T{}, T{}) : slices(d, fp8, T{}, N{});
+        if (per_sm != 2) return slices(d, fp8, N{}, N{}, N{});
+        if (!small) return slices(d, fp8, T{}, N{}, N{});
+        return one_tok ? slices(d, fp8, T{}, T{}, T{}) : slices(d, fp8, T{}, T{}, N{});
     };
     if (kv_fp8) {
         if (p.D != 128) return cudaErrorInvalidValue;
