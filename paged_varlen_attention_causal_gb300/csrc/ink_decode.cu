@@ -945,11 +945,12 @@ cudaError_t launch_decode(const Params &p, const CUtensorMap &tm_k, const CUtens
                 else return cudaErrorInvalidValue;  // D = 64 with one KV head: d-slices narrower than a tile
         }
     };
-    // the small-rows (and one-token) builds only where the registers are capped (two CTAs an SM)
+    // the small-rows builds where the registers are capped (two CTAs an SM), and at one CTA an SM for calls of
+    // one query token a request (no spills there either)
     auto builds = [&](auto d, auto fp8) -> cudaError_t {
         using T = std::true_type;
         using N = std::false_type;
-        if (per_sm != 2) return slices(d, fp8, N{}, N{}, N{});
+        if (per_sm != 2) return small && one_tok ? slices(d, fp8, N{}, T{}, T{}) : slices(d, fp8, N{}, N{}, N{});
         if (!small) return slices(d, fp8, T{}, N{}, N{});
         return one_tok ? slices(d, fp8, T{}, T{}, T{}) : slices(d, fp8, T{}, T{}, N{});
     };
