@@ -590,7 +590,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     }
 
     // 1. device-side plan
-    if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, stream); }) != cudaSuccess)
+    if (timed_launch(INK_KERNEL_PREPASS, stream, [&] { return launch_prepass(p, !pl.any_prefill, stream); }) !=
+        cudaSuccess)
         return INK_ERR_CUDA;
 
     // 1b. K/V staging copy for the prefill

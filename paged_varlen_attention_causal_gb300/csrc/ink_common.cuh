@@ -472,7 +472,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned 
 }
 
 // Host-side launchers, one per translation unit (ink_api.cu calls these).
-cudaError_t launch_prepass(const Params &p, cudaStream_t stream);
+// decode_only: the call can hold only decode-shaped requests (max_seqlen_q * G <= 16 with the decode kernel)
+cudaError_t launch_prepass(const Params &p, bool decode_only, cudaStream_t stream);
 // kv_fp8: K/V pages are E4M3 bytes dequantized with k_scale / v_scale (decode kernel only); per_sm: CTAs an SM
 // the kernel is compiled and sized for (1 or 2); small: no item of the call has more than 8 packed rows;
 // one_tok: every decode-shaped request has one query token (max_seqlen_q 1).

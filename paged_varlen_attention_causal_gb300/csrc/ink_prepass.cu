@@ -366,9 +366,84 @@ __global__ void __launch_bounds__(kPrepassThreads, 1) ink_prepass_kernel(Params 
     if (tid == 0) atomicOr(&p.hdr->errors, s_err);
 }
 
-cudaError_t launch_prepass(const Params &p, cudaStream_t stream)
+// The same plan for a call of at most 32 requests that can hold only decode-shaped ones (the host's bound
+// max_seqlen_q * G <= 16): one warp, a lane per request, warp scans instead of block-wide barriers.  It writes
+// what the block version writes for such a call: the header, the per-request offsets (no unit, no staging),
+// the merge list and the decode items.
+constexpr int kSmallBatch = 32;
+
+__global__ void __launch_bounds__(32, 1) ink_prepass_small_kernel(Params p)
 {
-    const cudaError_t e = launch_pdl(ink_prepass_kernel, 1, kPrepassThreads, 0, stream, p);
+    __shared__ int s_off[kSmallBatch + 1];
+    __shared__ int4 s_rq[kSmallBatch];
+    const int lane = threadIdx.x;
+    pdl_wait();  // the previous kernel of the stream (e.g. the last call's merge, which reads this workspace)
+    pdl_launch_dependents();
+    const bool have = lane < p.B;
+    const Req r = have ? load_req(p, lane) : Req{};
+    uint32_t err = 0;
+    int ndec = 0, nc = 0;
+    if (have) {
+        err = r.err;
+        if (r.ok && r.Lq > 0) {  // decode-shaped: the host's bound on max_seqlen_q leaves no other kind
+            const UnitSplit u = unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0);
+            ndec = u.nact;
+            nc = ndec > 1 ? r.Lq : 0;
+            if (p.causal && r.Lk < r.Lq) err |= INK_DEVERR_EMPTY_ROWS;
+        }
+    }
+    if (lane == 0 && (__ldg(p.cu) != 0 || __ldg(p.cu + p.B) != p.T)) err |= INK_DEVERR_CU_SEQLENS;
+    int xd = ndec, xc = nc;  // inclusive scans of the decode items and merge tokens
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yd = __shfl_up_sync(0xffffffffu, xd, o), yc = __shfl_up_sync(0xffffffffu, xc, o);
+        if (lane >= o) {
+            xd += yd;
+            xc += yc;
+        }
+    }
+    const int dec_total = __shfl_sync(0xffffffffu, xd, 31), comb_total = __shfl_sync(0xffffffffu, xc, 31);
+    err = __reduce_or_sync(0xffffffffu, err);
+    if (have) {
+        p.dec_off[lane] = xd - ndec;
+        p.unit_off[lane] = 0;
+        p.comb_off[lane] = xc - nc;
+        p.stg_off[lane] = -1;
+        s_off[lane] = xd - ndec;
+        s_rq[lane] = make_int4(r.t0, r.Lq, r.Lk, 0);
+    }
+    if (lane == 0) {
+        p.dec_off[p.B] = dec_total;
+        p.unit_off[p.B] = 0;
+        p.comb_off[p.B] = comb_total;
+    }
+    __syncwarp();
+    const int n_dec = min(dec_total, p.dec_items_cap);
+    for (int i = lane; i < n_dec; i += 32) {
+        int lo = 0, hi = p.B - 1;  // request owning item i: last b with dec_off[b] <= i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int4 rq = s_rq[lo];
+        p.dec_items[i] = make_int4(lo, (int)((unsigned)(i - s_off[lo]) | ((unsigned)rq.y << 27)), rq.x, rq.z);
+    }
+    if (lane == 0) {
+        p.hdr->errors = err;  // this kernel ran every check the block version would
+        p.hdr->dec_count = (uint32_t)n_dec;
+        p.hdr->pf_count = 0u;
+        p.hdr->dec_next = 0u;
+        p.hdr->pf_next = 0u;
+        p.hdr->comb_tokens = (uint32_t)comb_total;
+        p.hdr->stage_pages = 0u;
+    }
+}
+
+cudaError_t launch_prepass(const Params &p, bool decode_only, cudaStream_t stream)
+{
+    const cudaError_t e = decode_only && p.B <= kSmallBatch
+                              ? launch_pdl(ink_prepass_small_kernel, 1, 32, 0, stream, p)
+                              : launch_pdl(ink_prepass_kernel, 1, kPrepassThreads, 0, stream, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
