@@ -129,11 +129,12 @@ __global__ void __launch_bounds__(combine_threads<kWarpsPerRow>()) ink_combine_k
     __shared__ int s_doff[kCombSmemReqs + 1], s_uoff[kCombSmemReqs + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = warp % kWarpsPerRow;  // this warp's share of the row's splits
-    pdl_wait();
-    pdl_launch_dependents();
+    // The prepass's outputs (merge-list size, per-request offsets) and the call's inputs are complete before
+    // this grid can start: it launches early only once every CTA of the kernel before it has passed its own
+    // wait, and so on back to the prepass.  Only the split partials, written by that kernel, need the wait.
     const long long nrows = (long long)*(volatile uint32_t *)&p.hdr->comb_tokens * p.H;
     CombMeta mt{p.cu, p.seqk, p.comb_off, p.dec_off, p.unit_off};
-    if (p.B <= kCombSmemReqs) {  // one round of loads for all of them (written by the prepass, read-only here)
+    if (p.B <= kCombSmemReqs) {  // one round of loads for all of them (read-only here)
         for (int i = threadIdx.x; i <= p.B; i += kCombineThreads) {
             s_cu[i] = __ldg(p.cu + i);
             s_comb[i] = __ldg(p.comb_off + i);
@@ -144,6 +145,8 @@ __global__ void __launch_bounds__(combine_threads<kWarpsPerRow>()) ink_combine_k
         mt = CombMeta{s_cu, s_seqk, s_comb, s_doff, s_uoff};
         __syncthreads();
     }
+    pdl_wait();
+    pdl_launch_dependents();
     // Grid-stride over the merge list; the trip count is the same for all warps of a CTA.
     for (long long row0 = (long long)blockIdx.x * kRowsPerCta; row0 < nrows; row0 += (long long)gridDim.x * kRowsPerCta) {
         const long long row = row0 + warp / kWarpsPerRow;
