@@ -497,6 +497,8 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.units_cap = (int)pl.units_cap;
     p.S_pf = pl.S_pf;
     p.decode_kernel = pl.decode_kernel;
+    // decode-only and at most 32 requests: the one-warp prepass, and each decode CTA finds its first item itself
+    p.dec_local = (!pl.any_prefill && dims->batch <= 32) ? 1 : 0;
     p.chunk_dec = pl.chunk_dec;
     p.chunk_pf = pl.chunk_pf;
     p.tpt = pl.tpt;

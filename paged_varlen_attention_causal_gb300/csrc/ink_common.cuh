@@ -75,6 +75,7 @@ struct Params {
     int S_pf;                          // splits per prefill unit (1: no partials)
     // scheduling
     int decode_kernel;   // 1: decode-shaped requests go to the decode kernel
+    int dec_local;       // 1: a decode-only call of at most 32 requests (each decode CTA finds its first item)
     int chunk_dec;       // 16-key groups per split for decode units
     int chunk_pf;        // 16-key groups per split for prefill units
     int tpt;             // prefill tokens per 128-row tile (128 / G)

@@ -186,8 +186,14 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_wait();  // the work list and (for a staged call) the staging copy are complete
-    pdl_launch_dependents();
+    // The work list and (for a staged call) the staging copy are complete after the wait.  In a decode-only
+    // call of at most 32 requests the producer waits only after its first item, whose pages stream while the
+    // prepass runs; the compute warps read nothing the prepass writes.  Dependents launch only after a wait,
+    // so a kernel that follows can rely on the prepass's outputs.
+    if (!p.dec_local) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     if (warp == kDecComputeWarps) {
         // ------------------------------------------------------------ producer
@@ -199,19 +205,48 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
         const uint64_t pol_kv = policy_evict_first();
         // CTA c takes item c first and then items gridDim.x + k in the order of the shared counter, so
         // the first item needs no atomic; its entry is read speculatively beside the item count.
-        const int total = (int)*(volatile uint32_t *)&p.hdr->dec_count;
-        int next = blockIdx.x;
+        int total = 0, next = blockIdx.x;
         int4 di_next = make_int4(0, 0, 0, 0);
-        if (next < p.dec_items_cap) di_next = p.dec_items[next];
-        uint32_t n = 0;  // stage sequence number
-        for (uint32_t iseq = 0;; ++iseq) {
-            const int cur = next;
-            const int4 di = di_next;
+        bool waited = !p.dec_local;
+        uint32_t held_err = 0;  // page-id errors found before the wait (the prepass rewrites the error word)
+        if (p.dec_local) {
+            // item c from the inputs, by the prepass's own rule: requests in order, each cut by unit_split,
+            // item c owned by the last request whose first item is at or before c
+            const Req r = lane < p.B ? load_req(p, lane) : Req{};
+            const int na = (lane < p.B && r.ok && r.Lq > 0)
+                               ? unit_split(r.Lk - r.Lq, r.Lk - 1, r.Lk, p.causal, p.wl, p.wr, p.chunk_dec, 0).nact
+                               : 0;
+            int x = na;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int off = x - na;
+            total = min(__shfl_sync(0xffffffffu, x, 31), p.dec_items_cap);
+            const unsigned own = __ballot_sync(0xffffffffu, lane < p.B && off <= next);
+            const int b = own ? 31 - __clz(own) : 0;
+            const int split = next - __shfl_sync(0xffffffffu, off, b);
+            const int t0 = __shfl_sync(0xffffffffu, r.t0, b), lq = __shfl_sync(0xffffffffu, r.Lq, b);
+            const int lk = __shfl_sync(0xffffffffu, r.Lk, b);
+            if (next < total) di_next = make_int4(b, (int)((unsigned)split | ((unsigned)lq << 27)), t0, lk);
+        } else {
+            total = (int)*(volatile uint32_t *)&p.hdr->dec_count;
+            if (next < p.dec_items_cap) di_next = p.dec_items[next];
+        }
+        // the plan's queue: the next item after a wait on the prepass
+        auto claim_next = [&](int cur) {
             if (cur < total) {
                 if (lane == 0) next = (int)gridDim.x + (int)atomicAdd(&p.hdr->dec_next, 1u);
                 next = __shfl_sync(0xffffffffu, next, 0);
                 if (next < total) di_next = p.dec_items[next];
             }
+        };
+        uint32_t n = 0;  // stage sequence number
+        for (uint32_t iseq = 0;; ++iseq) {
+            const int cur = next;
+            const int4 di = di_next;
+            if (waited) claim_next(cur);
             const int slot = iseq & 1;
             if (!mbar_wait_warp(&sh.item_empty[slot], ((iseq >> 1) & 1) ^ 1, abort, p)) break;
             DecItem it;
@@ -239,7 +274,10 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                     if (gl < it.ge) {
                         const int pid = __ldg(bt_row + (gl * kKeyGroup) / p.BS);
                         pages = (pid >= 0 && pid < p.NB) ? pid : -1;
-                        if (pages < 0) report(p, INK_DEVERR_PAGE_ID);
+                        if (pages < 0) {
+                            if (waited) report(p, INK_DEVERR_PAGE_ID);
+                            else held_err |= INK_DEVERR_PAGE_ID;
+                        }
                     }
                 }
                 const int page = __shfl_sync(0xffffffffu, pages, rel);
@@ -269,7 +307,15 @@ __global__ void __launch_bounds__(kDecThreads, kPerSm)
                 ++n;
             }
             if (*abort) break;
+            if (!waited) {  // first item issued: from here on the prepass's plan is needed
+                pdl_wait();
+                pdl_launch_dependents();
+                waited = true;
+                if (held_err) report(p, held_err);
+                claim_next(cur);
+            }
         }
+        if (!waited) pdl_wait();  // this CTA ends only after the prepass, so that kernels after it can rely on it
         // let copies still in flight land before the CTA can exit
         for (uint32_t k = (n > (uint32_t)nstages ? n - nstages : 0); k < n; ++k)
             mbar_wait(&sh.full[k % nstages], (k / nstages) & 1, abort, p);
