@@ -8,6 +8,7 @@ need it).  Each case below lands in one of those variants; all must agree with
 the oracle at the bf16 path's tolerances, splits and windows included.
 """
 import pytest
+import torch
 
 import paged_varlen_attention_causal_gb300 as ink
 from test_gpu_fp8 import parity_fp8
@@ -78,4 +79,51 @@ def test_decode_variants_with_window(fp8):
         out, lse = gpu_run(case)
         ref_out, ref_lse = oracle_run(case)
         check(out, lse, ref_out, ref_lse, what="bf16 window")
+    assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+
+
+# --- decode-only calls of at most 32 requests: each decode CTA finds its first item from the inputs and streams
+# it while the prepass runs, waiting on the prepass only after that item
+
+def test_small_call_bad_page_in_a_first_item_is_flagged():
+    """A bad page id met while the first item streams (before the producer's wait on the prepass) is reported
+    after that wait, so the prepass's error word does not hide it; the other requests are untouched."""
+    case = decode_case(16, 4, 1, seed=91)
+    good_out, good_lse = gpu_run(case, num_splits=1)
+    assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
+    case.block_table[1, 0] = case.num_blocks + 3  # request 1's first page: item 1's first group
+    out, lse = gpu_run(case, num_splits=1)
+    assert ink.read_device_errors() & ink.DEVERR["PAGE_ID"]
+    cu = case.cu_seqlens_q.tolist()
+    keep = torch.ones(case.T, dtype=torch.bool)
+    keep[cu[1]:cu[2]] = False
+    assert torch.equal(out[keep.cuda()], good_out[keep.cuda()])
+
+
+def test_small_call_request_beyond_max_seqlen_q_is_flagged_and_others_exact():
+    """Request 1 has 3 tokens against max_seqlen_q 2 (so the call is decode-only: 2 x G <= 16): it is flagged
+    and gets no items, by the prepass and by the decode CTAs' own first-item rule alike; the others match the
+    oracle."""
+    case = build_case("dv-msq", [1, 3, 1, 2], [700, 500, 90, 3000], H=16, Hkv=4, E=200, seed=17, device="cuda",
+                      max_seqlen_q=2)
+    out, lse = gpu_run(case)
+    assert ink.read_device_errors() & ink.DEVERR["SEQLEN_Q"]
+    cu = case.cu_seqlens_q.tolist()
+    rows = [t * case.H + h for t in list(range(cu[0], cu[1])) + list(range(cu[2], cu[4])) for h in range(case.H)]
+    ref_out, ref_lse = oracle_run(case, rows=rows)
+    check(out, lse, ref_out, ref_lse, rows=rows, what="requests within max_seqlen_q")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_small_call_with_more_items_than_ctas(fp8):
+    """Three long decodes cut into more splits than there are CTAs: each CTA streams its first item before the
+    prepass is done and takes the rest from the prepass's queue."""
+    case = build_case("dv-many", [1, 1, 1], [60000, 45000, 70000], H=32, Hkv=8, E=1024, seed=23, device="cuda")
+    if fp8:
+        parity_fp8(case, "fp8 many items", num_splits=400)
+    else:
+        out, lse = gpu_run(case, num_splits=400)
+        ref_rows = list(range(case.T * case.H))
+        ref_out, ref_lse = oracle_run(case, rows=ref_rows)
+        check(out, lse, ref_out, ref_lse, rows=ref_rows, what="bf16 many items")
     assert ink.read_device_errors() & ~ink.DEVERR["EMPTY_ROWS"] == 0
