@@ -497,8 +497,6 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
     p.units_cap = (int)pl.units_cap;
     p.S_pf = pl.S_pf;
     p.decode_kernel = pl.decode_kernel;
-    // decode-only and at most 32 requests: the one-warp prepass, and each decode CTA finds its first item itself
-    p.dec_local = (!pl.any_prefill && dims->batch <= 32) ? 1 : 0;
     p.chunk_dec = pl.chunk_dec;
     p.chunk_pf = pl.chunk_pf;
     p.tpt = pl.tpt;
@@ -628,6 +626,10 @@ ink_status attn_impl(const ink_attn_dims *dims, const void *q, const void *key_c
         if (nst < 2) return INK_ERR_UNSUPPORTED;
         const size_t smem = 1024 + (size_t)nst * stage_bytes + kDecSharedBytes;
         const int grid = (int)std::min<long long>((long long)per_sm * sms, pl.dec_cap);
+        // A decode-only call of at most 32 requests (the one-warp prepass) whose items all fit one wave of CTAs:
+        // each decode CTA finds its one item itself and streams it while the prepass runs.  With more items
+        // than CTAs the early start measured slower (the next item is claimed only after the wait).
+        pd.dec_local = (!pl.any_prefill && dims->batch <= 32 && pl.dec_cap <= (long long)per_sm * sms) ? 1 : 0;
         if (timed_launch(INK_KERNEL_DECODE, stream, [&] {
                 return launch_decode(pd, tm_kd, tm_vd, tm_bdec, nst, stage_bytes, kv_bytes, bias_slot, kv.fp8,
                                      kv.k_scale, kv.v_scale, per_sm, small, one_tok, grid, smem, stream);
