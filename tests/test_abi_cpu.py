@@ -164,8 +164,8 @@ def test_fp8_append_host_validation(lib):
 
 
 def test_head_sizes_64_and_256(lib):
-    """D = 64 and 256 are served (head-size-generic kernel): workspace sizes follow D, nothing is staged,
-    and an FP8 cache is refused at those sizes."""
+    """D = 64 and 256 are served (decode items by the decode kernel, prefill tiles by the head-size-generic
+    kernel): workspace sizes follow D, nothing is staged, and an FP8 cache is refused at those sizes."""
     sizes = {D: ink.workspace_size(_dims(head_dim=D), 128, 8) for D in (64, 128, 256)}
     assert 0 < sizes[64] < sizes[256]
     assert ink.stage_bytes(_dims(head_dim=64), 1000) == 0 and ink.stage_bytes(_dims(head_dim=256), 1000) == 0
